@@ -1,0 +1,210 @@
+/*
+ * pst.h -- C ABI of the prefix-shared KV-tree attention library (libpst.so).
+ *
+ * ChunkAttention (Ye et al., "ChunkAttention: Efficient Self-Attention with
+ * Prefix-Aware KV Cache and Two-Phase Partition"):
+ *   Knowl 1  prefix-aware KV cache: K/V split into chunks of c tokens, kept in
+ *            a prefix tree; sequences sharing leading full chunks share them.
+ *   Knowl 2  two-phase partition decode: chunk-first over shared chunks,
+ *            sequence-first over each sequence's own chunks.
+ *   Knowl 3  partial_attn, attn_reduce (online-softmax merge), final divide.
+ *   Knowl 5  chunk -> batch-range tables rebuilt and copied only on
+ *            structural change (lazy context copy).
+ * Chunked Prefill (onnx-genai wiki), sections 1-2: a W-row causal query block
+ * attends to an append-only cache and equals single-pass prefill.
+ *
+ * Conventions for every entry point:
+ *   - Returns a pst_status; on failure pst_last_error() holds a message for
+ *     the calling thread.  No C++ exception crosses this boundary.
+ *   - "device" pointers are CUDA device memory on the pool's device; "host"
+ *     pointers are ordinary host memory.  The caller owns every buffer it
+ *     passes; the library never frees or retains caller pointers.
+ *   - Tensors are dense, row-major, in the pool dtype (pst_config.dtype).
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Device work
+ *     is enqueued asynchronously on it; host-side tree changes happen before
+ *     the call returns.  All calls on one pool must be issued from one host
+ *     thread and be ordered on the GPU (one stream, or caller-synchronised).
+ *   - Attention scale is 1/sqrt(head_dim) (the textbook definition on the
+ *     CachedAttention page, "Load-bearing equations"); query head h reads KV
+ *     head h * n_kv_heads / n_q_heads (contiguous groups).
+ */
+#ifndef PST_H
+#define PST_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  PST_OK = 0,
+  PST_ERR_INVALID = 1,   /* bad argument, shape, dtype or unsupported config */
+  PST_ERR_OOM = 2,       /* chunk pool (or sequence table) exhausted; nothing was changed */
+  PST_ERR_NOT_FOUND = 3, /* unknown or already removed sequence id */
+  PST_ERR_CUDA = 4,      /* a CUDA runtime call failed (message has the CUDA error) */
+  PST_ERR_STATE = 5,     /* call not valid in this state (e.g. device call on a host-only pool) */
+  PST_ERR_DEVICE = 6     /* a kernel reported an error (bounded wait timed out, bad index) */
+} pst_status;
+
+typedef enum { PST_F16 = 0, PST_BF16 = 1, PST_F32 = 2 } pst_dtype;
+
+/* pst_config.flags */
+enum {
+  PST_FLAG_NO_TENSOR_CORES = 1, /* run the chunk-first phase on the CUDA-core kernel too */
+  PST_FLAG_SERIAL_PHASES = 2    /* launch both phases on the caller's stream (no fork/join) */
+};
+
+typedef struct {
+  int32_t n_q_heads;   /* Hq >= 1 */
+  int32_t n_kv_heads;  /* Hkv >= 1, divides Hq, Hq/Hkv in {1,2,4,8} */
+  int32_t head_dim;    /* d in {64, 128} */
+  int32_t chunk_size;  /* c in {32, 64} */
+  int64_t max_chunks;  /* pool capacity in chunks (>= 1) */
+  int32_t dtype;       /* pst_dtype */
+  int32_t min_share;   /* chunk-first threshold: a chunk covered by >= min_share live
+                          sequences is computed chunk-first (Knowl 2 "covered by
+                          multiple sequences"); 0 means 2; INT32_MAX disables phase 1 */
+  int32_t max_seqs;    /* capacity of live sequences; 0 means 4096 */
+  int32_t flags;       /* PST_FLAG_* */
+} pst_config;
+
+typedef struct pst_pool pst_pool;
+
+typedef struct {
+  int64_t live_seqs;
+  int64_t used_chunks;     /* chunks on live paths */
+  int64_t free_chunks;
+  int64_t max_chunks;
+  int64_t shared_chunks;   /* chunks computed chunk-first (after the last table build) */
+  int64_t unique_tokens;   /* tokens stored in live chunks */
+  int64_t logical_tokens;  /* sum of live sequence lengths */
+  int64_t table_version;   /* bumps on every structural change */
+  int64_t rebuild_count;   /* host table builds performed */
+  double last_rebuild_us;  /* host time of the last table build */
+  int64_t phase1_items;    /* work items of the last build (chunk-first) */
+  int64_t phase2_items;    /* work items of the last build (sequence-first) */
+  int64_t partial_rows;    /* (o, m, n) partial rows of the last build */
+} pst_stats_t;
+
+/* Create a pool.  device >= 0: CUDA device ordinal; the pool allocates its
+ * chunk slab (2 * max_chunks * Hkv * c * d elements), tables and scratch there
+ * and keeps them until pst_pool_free.  device == -1: host-only pool that runs
+ * the prefix tree and tables but owns no device memory; every call that needs
+ * the GPU then returns PST_ERR_STATE (k/v must be NULL on insert).
+ * On success *out receives the pool. */
+pst_status pst_pool_create(const pst_config* cfg, int device, pst_pool** out);
+
+/* Free the pool and all of its device memory (synchronises the device). */
+pst_status pst_pool_free(pst_pool* pool);
+
+/* Prefix lookup (Knowl 1, sequence arrival): *n_matched = number of leading
+ * tokens (a multiple of c) covered by existing full chunks.  tokens: host
+ * int32[n].  Does not modify the pool. */
+pst_status pst_match(const pst_pool* pool, const int32_t* tokens, int64_t n, int64_t* n_matched);
+
+/* Sequence arrival (Knowl 1): match the longest full-chunk prefix, share it,
+ * allocate chunks for the rest and copy their K/V into the pool.
+ * tokens: host int32[n], n >= 1.  k, v: device [n][Hkv][d]; only rows
+ * >= n_matched are read (they may be NULL when n_matched == n).
+ * Atomic: on PST_ERR_OOM nothing changed.  *seq_id receives the new id (ids
+ * count up from 0 and are never reused), *n_matched the shared token count. */
+pst_status pst_insert(pst_pool* pool, const int32_t* tokens, int64_t n, const void* k, const void* v,
+                      void* stream, int64_t* seq_id, int64_t* n_matched);
+
+/* Decode append (Knowl 1, decoding iteration): write one token's K/V
+ * (device [Hkv][d] each) into the sequence's leaf chunk, or into a new chunk
+ * when the leaf is full. */
+pst_status pst_append(pst_pool* pool, int64_t seq_id, int32_t token, const void* k, const void* v,
+                      void* stream);
+
+/* Batched decode append: n tokens for n distinct sequences.  seq_ids: host
+ * int64[n]; tokens: host int32[n]; k, v: device [n][Hkv][d].  One kernel
+ * launch.  Atomic on PST_ERR_OOM / NOT_FOUND / INVALID (duplicate ids). */
+pst_status pst_append_batch(pst_pool* pool, int64_t n, const int64_t* seq_ids, const int32_t* tokens,
+                            const void* k, const void* v, void* stream);
+
+/* Sequence departure (Knowl 1): prune the path; chunks no live sequence
+ * uses return to the free list (device memory is kept). */
+pst_status pst_remove(pst_pool* pool, int64_t seq_id);
+
+/* Batch order (Knowl 1 contiguity): the live sequence ids in the depth-first
+ * order that rows of q/out follow.  seq_ids: host int64[cap] (may be NULL
+ * when cap == 0); *B receives the live count (call with cap 0 to size). */
+pst_status pst_batch_order(const pst_pool* pool, int64_t* seq_ids, int64_t cap, int64_t* B);
+
+/* Length in tokens of a live sequence. */
+pst_status pst_seq_length(const pst_pool* pool, int64_t seq_id, int64_t* n_tokens);
+
+/* Decode attention (Knowl 2 + 3): out[u][h] = softmax(q[u][h] K_u^T / sqrt(d)) V_u
+ * for every live sequence u in batch order, over all of its cached tokens.
+ * q, out: device [B][Hq][d], B = live count.  Rebuilds and uploads the chunk
+ * tables first if the tree changed (Knowl 5).  Chunk-first partials run on the
+ * tensor cores (tcgen05) for f16/bf16 with c = 64, sequence-first partials on
+ * the CUDA cores, then an online-softmax merge writes out. */
+pst_status pst_decode_attention(pst_pool* pool, const void* q, void* out, void* stream);
+
+/* Same as pst_decode_attention with HOST q/out: copies q host->device, runs
+ * the decode and copies out device->host on `stream`, then synchronises the
+ * stream.  q_host, out_host: host [B][Hq][d] (pinned memory avoids staging
+ * copies inside the CUDA runtime). */
+pst_status pst_decode_attention_host(pst_pool* pool, const void* q_host, void* out_host, void* stream);
+
+/* Chunked-prefill attend (Chunked Prefill, sections 1-2): append W tokens
+ * (host tokens int32[W], device k_new/v_new [W][Hkv][d]) to sequence seq_id at
+ * positions [p0, p0+W), p0 = its current length, then out[t][h] =
+ * softmax(q[t][h] K^T / sqrt(d)) V over keys [0, p0+t] of the sequence.
+ * q, out: device [W][Hq][d].  Appended tokens are never merged with other
+ * sequences' chunks.  Atomic on PST_ERR_OOM. */
+pst_status pst_prefill_attend(pst_pool* pool, int64_t seq_id, const int32_t* tokens, int64_t W,
+                              const void* q, const void* k_new, const void* v_new, void* out,
+                              void* stream);
+
+/* Read a sequence's cached K/V back into device k_out, v_out [n][Hkv][d]
+ * (n = its length), byte-exact. */
+pst_status pst_gather_kv(const pst_pool* pool, int64_t seq_id, void* k_out, void* v_out, void* stream);
+
+/* Canonical (chunk-id free) tables, for bit-exact comparison:
+ *   shared_rows: int32[n_shared][4] = (depth, i, j, n_tokens) for every chunk
+ *                covered by >= min_share sequences, in depth-first preorder;
+ *                [i, j) is the half-open batch range it covers.
+ *   seq_offsets: int64[B+1]; entries of batch row u are
+ *                seq_entries[2*e .. 2*e+1] = (depth, kind), e in
+ *                [seq_offsets[u], seq_offsets[u+1]), root to leaf;
+ *                kind 1 = chunk-first, 0 = sequence-first.
+ * Any buffer may be NULL with cap 0; the counts are always written.  Returns
+ * PST_ERR_INVALID (counts still written) if a capacity is too small. */
+pst_status pst_export_tables(const pst_pool* pool, int32_t* shared_rows, int64_t shared_cap,
+                             int64_t* n_shared, int32_t* seq_entries, int64_t entries_cap,
+                             int64_t* n_entries, int64_t* seq_offsets, int64_t offsets_cap, int64_t* B);
+
+/* Pool statistics (Knowl 4 quantities: sharing, fragmentation). */
+pst_status pst_stats(const pst_pool* pool, pst_stats_t* out);
+
+/* Record CUDA events around each decode kernel (phase 1, phase 2, merge). */
+pst_status pst_set_profiling(pst_pool* pool, int enable);
+
+/* Durations in ms of the last profiled decode's kernels: ms[0] chunk-first,
+ * ms[1] sequence-first, ms[2] merge (0 when the kernel did not run).  Waits
+ * for those events. */
+pst_status pst_phase_times(pst_pool* pool, float* ms3);
+
+/* Kernel launches issued by the last pst_decode_attention call. */
+pst_status pst_last_launch_count(const pst_pool* pool, int32_t* n);
+
+/* Read and clear the device error word written by kernels whose bounded
+ * waits timed out or whose index checks failed (synchronises the device).
+ * *code == 0 means no error. */
+pst_status pst_check_device(pst_pool* pool, int32_t* code);
+
+/* Thread-local message of the last failing call on this thread ("" if none). */
+const char* pst_last_error(void);
+
+/* Library version string. */
+const char* pst_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PST_H */

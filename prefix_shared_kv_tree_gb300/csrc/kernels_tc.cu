@@ -1,0 +1,382 @@
+// Chunk-first partial attention on the 5th-generation tensor cores (tcgen05).
+//
+// ChunkAttention, Knowl 2 phase 1: the queries of every sequence that shares
+// a chunk are stacked into one matrix and multiplied by the chunk's K/V, which
+// turns per-sequence matrix-vector work into a small dense contraction
+// (Knowl 9).  Knowl 3 gives partial_attn: W = Q K^T, m = rowmax W,
+// E = exp(W - m), n = rowsum E, O = E V.  The same kernel, with a per-row
+// causal key limit and a normalised output, runs a W-row chunked-prefill block
+// (Chunked Prefill, sections 1-2).
+//
+// One CTA handles one work item: up to 128 stacked query rows of one KV head
+// against a list of 64-token chunks.  Warp roles:
+//   warp 0      : producer -- one bulk async copy (TMA engine) per chunk moves
+//                 the 32 KB K + V^T tile image from the pool into a 4-stage
+//                 shared-memory ring; the pool already stores the tile in the
+//                 tensor cores' K-major core-matrix layout.
+//   warp 1      : allocates TMEM; lane 0 issues tcgen05.mma:
+//                 S = Q K^T (M=128, N=64, K=D) and O_k = P V (M=128, N=D, K=64),
+//                 both double-buffered in TMEM, and commits to mbarriers.
+//   warps 2..5  : one thread per query row: read S from TMEM, online softmax in
+//                 log2 units, write the rounded probabilities P to shared
+//                 memory as the A operand of the PV product, and fold each
+//                 chunk's O_k into fp32 registers (o = o * alpha + O_k).
+// Every wait is bounded; on a timeout the CTA records an error, drains its
+// copies and MMAs, frees TMEM and exits.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <climits>
+#include <cmath>
+#include <type_traits>
+
+#include "ptx.cuh"
+#include "pst_internal.h"
+
+namespace pst {
+
+namespace {
+
+constexpr int kC = 64;     // tokens per chunk
+constexpr int kBM = 128;   // stacked query rows per CTA
+constexpr int kNS = 4;     // K/V tile stages
+
+__host__ __device__ constexpr uint32_t tc_tile_bytes(int D) { return 2u * kC * D * 2u; }
+__host__ __device__ constexpr uint32_t tc_q_bytes(int D) { return kBM * D * 2u; }
+__host__ __device__ constexpr uint32_t tc_p_bytes() { return kBM * kC * 2u; }
+__host__ __device__ constexpr size_t tc_smem_bytes(int D) {
+  return 1024 + tc_q_bytes(D) + kNS * tc_tile_bytes(D) + 2 * tc_p_bytes() + 256;
+}
+
+template <typename T>
+__device__ __forceinline__ uint32_t pack2(float a, float b, float& sum) {
+  if constexpr (std::is_same<T, __half>::value) {
+    const __half2 h = __floats2half2_rn(a, b);
+    const float2 f = __half22float2(h);
+    sum += f.x + f.y;
+    return *reinterpret_cast<const uint32_t*>(&h);
+  } else {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    const float2 f = __bfloat1622float2(h);
+    sum += f.x + f.y;
+    return *reinterpret_cast<const uint32_t*>(&h);
+  }
+}
+
+template <typename T>
+__device__ __forceinline__ uint32_t pack2_plain(float a, float b) {
+  if constexpr (std::is_same<T, __half>::value) {
+    const __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<const uint32_t*>(&h);
+  } else {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<const uint32_t*>(&h);
+  }
+}
+
+template <typename T, int D>
+__global__ void __launch_bounds__(192, 1) attn_tc_kernel(const AttnParams p) {
+  constexpr uint32_t HALF = kC * D * 2;
+  constexpr uint32_t TILE = tc_tile_bytes(D);
+  constexpr uint32_t QB = tc_q_bytes(D);
+  constexpr uint32_t PB = tc_p_bytes();
+  constexpr int DCH = D / 8;    // 16-byte chunks per row when the reduction runs over D
+  constexpr int CCH = kC / 8;   // 16-byte chunks per row when the reduction runs over keys
+  constexpr uint32_t TMEM_COLS = (128 + 2 * D) <= 256 ? 256u : 512u;
+  constexpr uint32_t S_COL = 0;    // S double buffer: columns [0, 64), [64, 128)
+  constexpr uint32_t O_COL = 128;  // O double buffer: [128, 128 + D), [128 + D, 128 + 2D)
+  constexpr bool BF = std::is_same<T, __nv_bfloat16>::value;
+  constexpr uint32_t ID_S = ptx::idesc_f16(kBM, kC, BF);
+  constexpr uint32_t ID_O = ptx::idesc_f16(kBM, D, BF);
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* qs = smem;
+  uint8_t* kvs = qs + QB;
+  uint8_t* ps = kvs + kNS * TILE;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(ps + 2 * PB);
+  uint64_t* full = bars;             // [kNS] tile landed
+  uint64_t* empty = bars + kNS;      // [kNS] tile no longer read by the tensor cores
+  uint64_t* qfull = bars + 2 * kNS;  // Q tile written (128 arrivals)
+  uint64_t* sfull = qfull + 1;       // [2] S ready in TMEM
+  uint64_t* sfree = sfull + 2;       // [2] S read by the softmax threads (128)
+  uint64_t* pfull = sfree + 2;       // [2] P written (128)
+  uint64_t* ofull = pfull + 2;       // [2] O_k ready in TMEM
+  uint64_t* ofree = ofull + 2;       // [2] O_k read (128)
+  uint64_t* done = ofree + 2;        // all MMAs of this CTA completed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* issued_slot = abort_flag + 1;
+  volatile int* consumed_slot = abort_flag + 2;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const WorkItem w = p.items[blockIdx.x];
+  const int nk = w.n_chunks;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kNS; ++s) {
+      ptx::mbar_init(&full[s], 1);
+      ptx::mbar_init(&empty[s], 1);
+    }
+    ptx::mbar_init(qfull, 128);
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(&sfull[b], 1);
+      ptx::mbar_init(&sfree[b], 128);
+      ptx::mbar_init(&pfull[b], 128);
+      ptx::mbar_init(&ofull[b], 1);
+      ptx::mbar_init(&ofree[b], 128);
+    }
+    ptx::mbar_init(done, 1);
+    *abort_flag = 0;
+    *issued_slot = 0;
+    *consumed_slot = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 1) ptx::tmem_alloc(tmem_slot, TMEM_COLS);
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      const uint64_t pol = ptx::policy_evict_last();
+      for (int k = 0; k < nk; ++k) {
+        const int s = k % kNS;
+        if (k >= kNS && !ptx::mbar_wait(&empty[s], ((k / kNS) - 1) & 1, abort_flag, p.err)) break;
+        const int chunk = p.chunks[w.chunk_off + k];
+        const uint8_t* src = p.pool + (static_cast<size_t>(chunk) * p.Hkv + w.kv) * TILE;
+        ptx::mbar_arrive_expect_tx(&full[s], TILE);
+        ptx::bulk_g2s_hint(kvs + s * TILE, src, TILE, &full[s], pol);
+        *issued_slot = k + 1;
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t q_addr = ptx::smem_u32(qs);
+      const uint32_t kv_addr = ptx::smem_u32(kvs);
+      const uint32_t p_addr = ptx::smem_u32(ps);
+      auto issue_s = [&](int k) -> bool {
+        const int s = k % kNS, b = k & 1;
+        if (!ptx::mbar_wait(&full[s], (k / kNS) & 1, abort_flag, p.err)) return false;
+        *consumed_slot = k + 1;
+        if (k >= 2 && !ptx::mbar_wait(&sfree[b], ((k - 2) >> 1) & 1, abort_flag, p.err)) return false;
+        ptx::tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint64_t a = ptx::smem_desc(q_addr + kk * 256, 128, DCH * 128);
+          const uint64_t bd = ptx::smem_desc(kv_addr + s * TILE + kk * 256, 128, DCH * 128);
+          ptx::mma_f16(tbase + S_COL + b * kC, a, bd, ID_S, kk > 0 ? 1u : 0u);
+        }
+        ptx::mma_commit(&sfull[b]);
+        return true;
+      };
+      auto issue_pv = [&](int k) -> bool {
+        const int s = k % kNS, b = k & 1;
+        if (!ptx::mbar_wait(&pfull[b], (k >> 1) & 1, abort_flag, p.err)) return false;
+        if (k >= 2 && !ptx::mbar_wait(&ofree[b], ((k - 2) >> 1) & 1, abort_flag, p.err)) return false;
+        ptx::tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < kC / 16; ++kk) {
+          const uint64_t a = ptx::smem_desc(p_addr + b * PB + kk * 256, 128, CCH * 128);
+          const uint64_t bd = ptx::smem_desc(kv_addr + s * TILE + HALF + kk * 256, 128, CCH * 128);
+          ptx::mma_f16(tbase + O_COL + b * D, a, bd, ID_O, kk > 0 ? 1u : 0u);
+        }
+        ptx::mma_commit(&ofull[b]);
+        ptx::mma_commit(&empty[s]);
+        return true;
+      };
+      bool ok = ptx::mbar_wait(qfull, 0, abort_flag, p.err);
+      if (ok) {
+        ptx::tc_fence_after();
+        ok = issue_s(0);
+      }
+      for (int k = 0; k < nk && ok; ++k) {
+        if (k + 1 < nk) ok = issue_s(k + 1);
+        if (ok) ok = issue_pv(k);
+      }
+      // Every MMA of this CTA must have finished before TMEM is released.
+      ptx::mma_commit(done);
+      ptx::mbar_wait(done, 0, nullptr, p.err);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------- softmax / epilogue
+    const int quad = warp & 3;
+    const int r = quad * 32 + lane;
+    const bool row_valid = r < w.n_rows;
+    int grp = 0, hg = 0;
+    if (row_valid) {
+      const int rr = w.row0 + r;
+      grp = w.group0 + rr / p.g;
+      hg = rr % p.g;
+    }
+    const T* qrow = static_cast<const T*>(p.q) + (static_cast<size_t>(grp) * p.Hq + w.kv * p.g + hg) * D;
+#pragma unroll
+    for (int j = 0; j < DCH; ++j) {
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (row_valid) v = *reinterpret_cast<const uint4*>(qrow + j * 8);
+      *reinterpret_cast<uint4*>(qs + cm_off(r, j, DCH)) = v;
+    }
+    ptx::fence_proxy_async_smem();
+    ptx::mbar_arrive(qfull);
+
+    const int key_limit = (p.causal_p0 >= 0 && row_valid) ? p.causal_p0 + grp + 1 : INT_MAX;
+    const uint32_t tl = tbase + (static_cast<uint32_t>(quad * 32) << 16);
+    float o[D];
+#pragma unroll
+    for (int i = 0; i < D; ++i) o[i] = 0.f;
+    float m = -INFINITY, l = 0.f, alpha_pend = 0.f;
+    bool ok = true;
+
+    for (int k = 0; k < nk; ++k) {
+      const int b = k & 1;
+      const int chunk = p.chunks[w.chunk_off + k];
+      const int lim = min(p.chunk_len[chunk], key_limit - k * kC);
+      if (!ptx::mbar_wait(&sfull[b], (k >> 1) & 1, abort_flag, p.err)) {
+        ok = false;
+        break;
+      }
+      ptx::tc_fence_after();
+      uint32_t sv0[32], sv1[32];
+      ptx::tmem_ld32(tl + S_COL + b * kC, sv0);
+      ptx::tmem_ld32(tl + S_COL + b * kC + 32, sv1);
+      ptx::tmem_ld_wait(sv0);
+      ptx::tmem_ld_wait(sv1);
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(&sfree[b]);
+
+      float x[kC];
+      float mx = -INFINITY;
+#pragma unroll
+      for (int t = 0; t < kC; ++t) {
+        const uint32_t raw = t < 32 ? sv0[t] : sv1[t - 32];
+        x[t] = (t < lim) ? __uint_as_float(raw) * p.scale_log2 : -INFINITY;
+        mx = fmaxf(mx, x[t]);
+      }
+      const float m_new = fmaxf(m, mx);
+      const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+      const float alpha = exp2f(m - m_use);
+      float psum = 0.f;
+      uint8_t* prow = ps + b * PB;
+#pragma unroll
+      for (int j = 0; j < CCH; ++j) {
+        uint4 pk;
+        pk.x = pack2<T>(exp2f(x[8 * j + 0] - m_use), exp2f(x[8 * j + 1] - m_use), psum);
+        pk.y = pack2<T>(exp2f(x[8 * j + 2] - m_use), exp2f(x[8 * j + 3] - m_use), psum);
+        pk.z = pack2<T>(exp2f(x[8 * j + 4] - m_use), exp2f(x[8 * j + 5] - m_use), psum);
+        pk.w = pack2<T>(exp2f(x[8 * j + 6] - m_use), exp2f(x[8 * j + 7] - m_use), psum);
+        *reinterpret_cast<uint4*>(prow + cm_off(r, j, CCH)) = pk;
+      }
+      ptx::fence_proxy_async_smem();
+      ptx::mbar_arrive(&pfull[b]);
+      l = l * alpha + psum;
+
+      if (k >= 1) {
+        const int b1 = (k - 1) & 1;
+        if (!ptx::mbar_wait(&ofull[b1], ((k - 1) >> 1) & 1, abort_flag, p.err)) {
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+#pragma unroll
+        for (int cg = 0; cg < D / 32; ++cg) {
+          uint32_t ov[32];
+          ptx::tmem_ld32(tl + O_COL + b1 * D + 32 * cg, ov);
+          ptx::tmem_ld_wait(ov);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[32 * cg + e] = fmaf(o[32 * cg + e], alpha_pend, __uint_as_float(ov[e]));
+        }
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(&ofree[b1]);
+      }
+      alpha_pend = alpha;
+      m = m_new;
+    }
+
+    if (ok && nk > 0) {
+      const int b1 = (nk - 1) & 1;
+      if (ptx::mbar_wait(&ofull[b1], ((nk - 1) >> 1) & 1, abort_flag, p.err)) {
+        ptx::tc_fence_after();
+#pragma unroll
+        for (int cg = 0; cg < D / 32; ++cg) {
+          uint32_t ov[32];
+          ptx::tmem_ld32(tl + O_COL + b1 * D + 32 * cg, ov);
+          ptx::tmem_ld_wait(ov);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[32 * cg + e] = fmaf(o[32 * cg + e], alpha_pend, __uint_as_float(ov[e]));
+        }
+        ptx::tc_fence_before();
+        if (row_valid) {
+          if (p.final_mode) {
+            T* out = static_cast<T*>(p.out) + (static_cast<size_t>(grp) * p.Hq + w.kv * p.g + hg) * D;
+            const float inv = 1.f / l;
+#pragma unroll
+            for (int j = 0; j < DCH; ++j) {
+              uint4 pk;
+              pk.x = pack2_plain<T>(o[8 * j + 0] * inv, o[8 * j + 1] * inv);
+              pk.y = pack2_plain<T>(o[8 * j + 2] * inv, o[8 * j + 3] * inv);
+              pk.z = pack2_plain<T>(o[8 * j + 4] * inv, o[8 * j + 5] * inv);
+              pk.w = pack2_plain<T>(o[8 * j + 6] * inv, o[8 * j + 7] * inv);
+              *reinterpret_cast<uint4*>(out + 8 * j) = pk;
+            }
+          } else {
+            const size_t prow_i = static_cast<size_t>(w.part_base) + r;
+            float4* po = reinterpret_cast<float4*>(p.part_o + prow_i * D);
+#pragma unroll
+            for (int j = 0; j < D / 4; ++j) po[j] = make_float4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
+            p.part_ml[2 * prow_i] = m;
+            p.part_ml[2 * prow_i + 1] = l;
+          }
+        }
+      }
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (threadIdx.x == 0 && *abort_flag) {
+    // Let every bulk copy still in flight land before the CTA exits.
+    for (int k = *consumed_slot; k < *issued_slot; ++k) ptx::mbar_wait(&full[k % kNS], (k / kNS) & 1, nullptr, p.err);
+  }
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tbase, TMEM_COLS);
+  }
+}
+
+template <typename T, int D>
+cudaError_t launch_tc_t(const AttnParams& p, int grid, cudaStream_t s) {
+  const size_t smem = tc_smem_bytes(D);
+  auto fn = attn_tc_kernel<T, D>;
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  fn<<<grid, 192, smem, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool tc_supported(int dtype, int D, int C) {
+  return (dtype == kF16 || dtype == kBF16) && (D == 64 || D == 128) && C == kC;
+}
+
+size_t attn_tc_smem(int D) { return tc_smem_bytes(D); }
+
+cudaError_t launch_attn_tc(int dtype, int D, const AttnParams& p, int grid, cudaStream_t s) {
+  if (grid <= 0) return cudaSuccess;
+  if (dtype == kF16) {
+    if (D == 128) return launch_tc_t<__half, 128>(p, grid, s);
+    if (D == 64) return launch_tc_t<__half, 64>(p, grid, s);
+  } else if (dtype == kBF16) {
+    if (D == 128) return launch_tc_t<__nv_bfloat16, 128>(p, grid, s);
+    if (D == 64) return launch_tc_t<__nv_bfloat16, 64>(p, grid, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace pst

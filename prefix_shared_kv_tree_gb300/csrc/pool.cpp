@@ -1,0 +1,1087 @@
+// Host side of libpst: the prefix-aware KV cache tree, the chunk pool's free
+// list, the table builder, and the C ABI declared in include/pst.h.
+//
+// ChunkAttention, Knowl 1 (PAKV): a forest of c-token chunks; arrival does a
+// prefix lookup and shares matched full chunks, decode appends to the leaf,
+// departure prunes and frees chunks nobody uses (device memory is kept).
+// Knowl 5: the kernels are driven by flattened chunk -> batch-range tables that
+// are rebuilt on the host and copied to the GPU only when the tree changes
+// structurally (a chunk is added or freed, a sequence joins or leaves); the
+// per-chunk valid length lives on the device and is updated by the scatter
+// kernel, so ordinary decode appends need no table copy.
+//
+// Readings taken where the pages leave a step open:
+//   * only full chunks are matched/shared, by equality of all c token ids under
+//     an already matched parent; the first such child in creation order wins;
+//   * batch order: depth-first preorder from a virtual root, children in
+//     creation order, sequences ending at a node (by id) before its children;
+//   * a chunk covered by >= min_share live sequences is computed chunk-first;
+//   * sequence ids count up from 0 and are never reused.
+#include <algorithm>
+#include <chrono>
+#include <climits>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <unordered_map>
+#include <vector>
+
+#include "../../include/pst.h"
+#include "pst_internal.h"
+
+using namespace pst;
+
+namespace {
+
+thread_local std::string g_last_error;
+
+pst_status fail(pst_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return st;
+}
+
+#define CUDA_TRY(expr)                                                                  \
+  do {                                                                                  \
+    cudaError_t _e = (expr);                                                            \
+    if (_e != cudaSuccess) return fail(PST_ERR_CUDA, "%s: %s", #expr, cudaGetErrorString(_e)); \
+  } while (0)
+
+uint64_t hash_tokens(const int32_t* t, int n) {
+  uint64_t h = 1469598103934665603ull;
+  for (int i = 0; i < n; ++i) {
+    h ^= static_cast<uint32_t>(t[i]);
+    h *= 1099511628211ull;
+  }
+  return h;
+}
+
+struct Node {
+  int32_t parent = -1;
+  int32_t depth = -1;
+  int32_t chunk = -1;
+  int32_t n_tokens = 0;
+  int32_t refs = 0;
+  uint64_t hash = 0;  // of the tokens once the chunk is full
+  bool live = false;
+  std::vector<int32_t> tokens;
+  std::vector<int32_t> children;  // creation order
+  std::vector<int64_t> ending;     // ids of sequences whose path ends here, ascending
+};
+
+struct Seq {
+  std::vector<int32_t> path;  // node ids, root to leaf
+  int64_t length = 0;
+};
+
+inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+}  // namespace
+
+struct pst_pool {
+  pst_config cfg{};
+  int device = -1;
+  bool host_only = true;
+  int es = 2;
+  int C = 64, D = 128, g = 1;
+  size_t half_bytes = 0, tile_bytes = 0;
+  int n_sm = 1;
+  bool use_tc = false;
+  float scale_log2 = 0.f;
+
+  // ---- tree
+  std::vector<Node> nodes;  // nodes[0] is the virtual root
+  std::vector<int32_t> free_nodes;
+  std::vector<int32_t> free_chunks;  // LIFO
+  std::unordered_map<int64_t, Seq> seqs;
+  int64_t next_seq = 0;
+
+  // ---- tables
+  bool dirty = true;
+  int64_t version = 0, rebuild_count = 0;
+  double last_rebuild_us = 0;
+  std::vector<int64_t> batch;  // live ids in batch order
+  std::vector<int32_t> h_tab;
+  size_t off_chunks = 0, off_tc = 0, off_simt = 0, off_warp = 0, off_moff = 0, off_ment = 0;
+  int32_t n_tc_items = 0, n_simt_items = 0, n_simt_warps = 0;
+  int32_t simt_grid = 0, simt_stages = 3, simt_wpc = 4;
+  int64_t n_part_rows = 0, shared_chunks = 0;
+  std::vector<int32_t> canon_shared;   // 4 per row
+  std::vector<int32_t> canon_entries;  // 2 per entry
+  std::vector<int64_t> canon_offsets;  // B + 1
+
+  // ---- device
+  uint8_t* d_pool = nullptr;
+  int32_t* d_chunk_len = nullptr;
+  int32_t* d_tab = nullptr;
+  size_t tab_cap = 0;  // int32 elements
+  bool tab_uploaded = false;
+  float* d_part_o = nullptr;
+  float* d_part_ml = nullptr;
+  size_t part_cap = 0;  // rows
+  int32_t* d_err = nullptr;
+  int32_t* d_pre = nullptr;
+  size_t pre_cap = 0;
+  int32_t* h_stage = nullptr;  // pinned upload staging
+  size_t stage_cap = 0;
+  cudaEvent_t ev_stage = nullptr;
+  bool stage_pending = false;
+  void* d_q = nullptr;
+  void* d_out = nullptr;
+  size_t qo_cap = 0;  // bytes each
+  cudaStream_t aux = nullptr;
+  cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
+  bool profiling = false;
+  cudaEvent_t pev[6] = {};
+  bool pran[3] = {false, false, false};
+  int32_t last_launches = 0;
+};
+
+namespace {
+
+// =========================================================== tree operations
+int32_t new_node(pst_pool* p, int32_t parent) {
+  int32_t id;
+  if (!p->free_nodes.empty()) {
+    id = p->free_nodes.back();
+    p->free_nodes.pop_back();
+  } else {
+    id = static_cast<int32_t>(p->nodes.size());
+    p->nodes.emplace_back();
+  }
+  Node& n = p->nodes[id];
+  n = Node();
+  n.parent = parent;
+  n.depth = p->nodes[parent].depth + 1;
+  n.live = true;
+  n.chunk = p->free_chunks.back();
+  p->free_chunks.pop_back();
+  n.tokens.reserve(p->C);
+  p->nodes[parent].children.push_back(id);
+  return id;
+}
+
+void release_node(pst_pool* p, int32_t id) {
+  Node& n = p->nodes[id];
+  auto& sib = p->nodes[n.parent].children;
+  sib.erase(std::find(sib.begin(), sib.end(), id));
+  p->free_chunks.push_back(n.chunk);
+  n.live = false;
+  n.tokens.clear();
+  n.tokens.shrink_to_fit();
+  n.children.clear();
+  n.ending.clear();
+  p->free_nodes.push_back(id);
+}
+
+int32_t find_full_child(const pst_pool* p, int32_t parent, const int32_t* tok) {
+  const uint64_t h = hash_tokens(tok, p->C);
+  for (int32_t ch : p->nodes[parent].children) {
+    const Node& n = p->nodes[ch];
+    if (n.n_tokens == p->C && n.hash == h && std::memcmp(n.tokens.data(), tok, sizeof(int32_t) * p->C) == 0) return ch;
+  }
+  return -1;
+}
+
+// Longest run of existing full chunks matching the leading tokens.
+int64_t match_path(const pst_pool* p, const int32_t* tokens, int64_t n, std::vector<int32_t>* path) {
+  int32_t cur = 0;
+  int64_t pos = 0;
+  while (pos + p->C <= n) {
+    const int32_t ch = find_full_child(p, cur, tokens + pos);
+    if (ch < 0) break;
+    if (path) path->push_back(ch);
+    cur = ch;
+    pos += p->C;
+  }
+  return pos;
+}
+
+void push_token(pst_pool* p, int32_t id, int32_t tok) {
+  Node& n = p->nodes[id];
+  n.tokens.push_back(tok);
+  n.n_tokens++;
+  if (n.n_tokens == p->C) n.hash = hash_tokens(n.tokens.data(), p->C);
+}
+
+void mark_structural(pst_pool* p) {
+  p->dirty = true;
+  p->version++;
+}
+
+// Launch scatter ops in batches of kScatterMax.
+pst_status run_scatter(pst_pool* p, const std::vector<ScatterOp>& ops, const void* k, const void* v,
+                       cudaStream_t s, bool gather) {
+  if (p->host_only || ops.empty()) return PST_OK;
+  ScatterParams sp;
+  sp.k = static_cast<const uint8_t*>(k);
+  sp.v = static_cast<const uint8_t*>(v);
+  sp.pool = p->d_pool;
+  sp.chunk_len = p->d_chunk_len;
+  sp.Hkv = p->cfg.n_kv_heads;
+  for (size_t i = 0; i < ops.size(); i += kScatterMax) {
+    const size_t n = std::min<size_t>(kScatterMax, ops.size() - i);
+    sp.n_ops = static_cast<int32_t>(n);
+    std::memcpy(sp.ops, ops.data() + i, n * sizeof(ScatterOp));
+    cudaError_t e = gather ? launch_gather(p->cfg.dtype, p->D, p->C, sp, s) : launch_scatter(p->cfg.dtype, p->D, p->C, sp, s);
+    if (e != cudaSuccess) return fail(PST_ERR_CUDA, "scatter launch: %s", cudaGetErrorString(e));
+  }
+  return PST_OK;
+}
+
+// ================================================================ tables
+struct Stream {  // a run of tiles for the CUDA-core kernel: chunks of one list, one KV head, one group
+  int32_t chunk_off, n, kv, group;
+};
+
+pst_status upload(pst_pool* p, int32_t** dbuf, size_t* dcap, const std::vector<int32_t>& src, cudaStream_t s) {
+  const size_t n = src.size();
+  if (n == 0) return PST_OK;
+  if (n > *dcap) {
+    if (*dbuf) {
+      CUDA_TRY(cudaStreamSynchronize(s));
+      CUDA_TRY(cudaFree(*dbuf));
+    }
+    size_t cap = std::max<size_t>(n * 3 / 2, 4096);
+    CUDA_TRY(cudaMalloc(dbuf, cap * sizeof(int32_t)));
+    *dcap = cap;
+  }
+  if (p->stage_pending) {
+    CUDA_TRY(cudaEventSynchronize(p->ev_stage));
+    p->stage_pending = false;
+  }
+  if (n > p->stage_cap) {
+    if (p->h_stage) CUDA_TRY(cudaFreeHost(p->h_stage));
+    size_t cap = std::max<size_t>(n * 3 / 2, 4096);
+    CUDA_TRY(cudaMallocHost(&p->h_stage, cap * sizeof(int32_t)));
+    p->stage_cap = cap;
+  }
+  std::memcpy(p->h_stage, src.data(), n * sizeof(int32_t));
+  CUDA_TRY(cudaMemcpyAsync(*dbuf, p->h_stage, n * sizeof(int32_t), cudaMemcpyHostToDevice, s));
+  CUDA_TRY(cudaEventRecord(p->ev_stage, s));
+  p->stage_pending = true;
+  return PST_OK;
+}
+
+void push_item(std::vector<int32_t>& v, const WorkItem& w) {
+  const int32_t* x = reinterpret_cast<const int32_t*>(&w);
+  v.insert(v.end(), x, x + 8);
+}
+
+// Rebuild batch order, canonical tables and the device work tables.
+pst_status rebuild(pst_pool* p) {
+  const auto t0 = std::chrono::steady_clock::now();
+  const int g = p->g, Hkv = p->cfg.n_kv_heads;
+  const int min_share = p->cfg.min_share;
+  const size_t NN = p->nodes.size();
+  std::vector<int32_t> ni(NN, 0), nj(NN, 0);
+  std::vector<int32_t> preorder;
+  p->batch.clear();
+  // iterative DFS from the virtual root
+  {
+    std::vector<std::pair<int32_t, size_t>> st;
+    st.emplace_back(0, 0);
+    ni[0] = 0;
+    while (!st.empty()) {
+      auto& top = st.back();
+      const int32_t id = top.first;
+      if (top.second == 0) {
+        ni[id] = static_cast<int32_t>(p->batch.size());
+        if (id != 0) preorder.push_back(id);
+        for (int64_t sid : p->nodes[id].ending) p->batch.push_back(sid);
+      }
+      const auto& ch = p->nodes[id].children;
+      if (top.second < ch.size()) {
+        const int32_t c = ch[top.second++];
+        st.emplace_back(c, 0);
+      } else {
+        nj[id] = static_cast<int32_t>(p->batch.size());
+        st.pop_back();
+      }
+    }
+  }
+  const int32_t B = static_cast<int32_t>(p->batch.size());
+  auto shared = [&](int32_t id) { return nj[id] - ni[id] >= min_share; };
+
+  // canonical tables
+  p->canon_shared.clear();
+  p->canon_entries.clear();
+  p->canon_offsets.assign(1, 0);
+  int64_t n_shared = 0;
+  for (int32_t id : preorder) {
+    if (!shared(id)) continue;
+    const Node& n = p->nodes[id];
+    p->canon_shared.insert(p->canon_shared.end(), {n.depth, ni[id], nj[id], n.n_tokens});
+    ++n_shared;
+  }
+  for (int64_t sid : p->batch) {
+    for (int32_t id : p->seqs[sid].path) {
+      p->canon_entries.push_back(p->nodes[id].depth);
+      p->canon_entries.push_back(shared(id) ? 1 : 0);
+    }
+    p->canon_offsets.push_back(static_cast<int64_t>(p->canon_entries.size() / 2));
+  }
+  p->shared_chunks = n_shared;
+
+  // runs of shared chunks with an identical batch range
+  std::vector<int32_t> run_of(NN, -1);
+  std::vector<std::vector<int32_t>> runs;  // node ids root->leaf
+  for (int32_t id : preorder) {
+    if (!shared(id)) continue;
+    const int32_t par = p->nodes[id].parent;
+    if (par != 0 && run_of[par] >= 0 && ni[par] == ni[id] && nj[par] == nj[id]) {
+      run_of[id] = run_of[par];
+    } else {
+      run_of[id] = static_cast<int32_t>(runs.size());
+      runs.emplace_back();
+    }
+    runs[run_of[id]].push_back(id);
+  }
+
+  std::vector<int32_t> chunks;
+  std::vector<int32_t> tc_items, simt_items, warp_items;
+  std::vector<std::pair<int32_t, int32_t>> ment;  // (u*Hkv + kv, partial row base)
+  std::vector<Stream> streams;
+  int64_t prow = 0;
+
+  // ---- phase 1: chunk-first over the runs
+  int64_t p1_iters = 0;
+  for (const auto& r : runs) {
+    const int32_t id0 = r.front();
+    const int64_t rows = static_cast<int64_t>(nj[id0] - ni[id0]) * g;
+    p1_iters += static_cast<int64_t>(r.size()) * Hkv * (p->use_tc ? ceil_div(rows, 128) : (nj[id0] - ni[id0]));
+  }
+  const int64_t split1 = std::min<int64_t>(32, std::max<int64_t>(4, (p1_iters + p->n_sm - 1) / std::max(1, p->n_sm)));
+  for (const auto& r : runs) {
+    const int32_t i = ni[r.front()], j = nj[r.front()];
+    const int32_t rows = (j - i) * g;
+    const int32_t L = static_cast<int32_t>(r.size());
+    const int32_t nsplit = static_cast<int32_t>(ceil_div(L, split1));
+    for (int32_t sp = 0; sp < nsplit; ++sp) {
+      const int32_t a = static_cast<int32_t>(static_cast<int64_t>(sp) * L / nsplit);
+      const int32_t b = static_cast<int32_t>(static_cast<int64_t>(sp + 1) * L / nsplit);
+      const int32_t off = static_cast<int32_t>(chunks.size());
+      for (int32_t x = a; x < b; ++x) chunks.push_back(p->nodes[r[x]].chunk);
+      if (p->use_tc) {
+        for (int kv = 0; kv < Hkv; ++kv) {
+          for (int32_t r0 = 0; r0 < rows; r0 += 128) {
+            WorkItem w{};
+            w.chunk_off = off;
+            w.n_chunks = b - a;
+            w.kv = kv;
+            w.group0 = i;
+            w.row0 = r0;
+            w.n_rows = std::min(128, rows - r0);
+            w.part_base = static_cast<int32_t>(prow);
+            push_item(tc_items, w);
+            for (int32_t u = i + r0 / g; u < i + (r0 + w.n_rows) / g; ++u)
+              ment.emplace_back(u * Hkv + kv, static_cast<int32_t>(prow + (u - i) * g - r0));
+            prow += w.n_rows;
+          }
+        }
+      } else {
+        for (int32_t u = i; u < j; ++u)
+          for (int kv = 0; kv < Hkv; ++kv) streams.push_back({off, b - a, kv, u});
+      }
+    }
+  }
+  p->n_tc_items = static_cast<int32_t>(tc_items.size() / 8);
+
+  // ---- phase 2: sequence-first over each sequence's own chunks
+  for (int32_t u = 0; u < B; ++u) {
+    const Seq& sq = p->seqs[p->batch[u]];
+    const int32_t off = static_cast<int32_t>(chunks.size());
+    int32_t n = 0;
+    for (int32_t id : sq.path) {
+      if (shared(id)) continue;
+      chunks.push_back(p->nodes[id].chunk);
+      ++n;
+    }
+    if (n == 0) continue;
+    for (int kv = 0; kv < Hkv; ++kv) streams.push_back({off, n, kv, u});
+  }
+
+  // ---- split the CUDA-core tile streams evenly over all warps of the grid
+  int64_t T = 0;
+  for (const auto& st : streams) T += st.n;
+  const int64_t warps_needed = std::max<int64_t>(1, ceil_div(T, 2));
+  p->simt_grid = static_cast<int32_t>(std::min<int64_t>(p->n_sm, ceil_div(warps_needed, p->simt_wpc)));
+  p->n_simt_warps = p->simt_grid * p->simt_wpc;
+  const int64_t W = p->n_simt_warps;
+  warp_items.assign(W + 1, 0);
+  {
+    int64_t t_base = 0;  // global index of the current stream's first tile
+    size_t si = 0;
+    int64_t wcur = 0;
+    int32_t item_count = 0;
+    for (int64_t w = 0; w < W; ++w) {
+      warp_items[w] = item_count;
+      const int64_t lo = w * T / W, hi = (w + 1) * T / W;
+      int64_t t = lo;
+      while (t < hi) {
+        while (si < streams.size() && t_base + streams[si].n <= t) {
+          t_base += streams[si].n;
+          ++si;
+        }
+        const Stream& st = streams[si];
+        const int64_t a = t - t_base;
+        const int64_t b = std::min<int64_t>(st.n, hi - t_base);
+        WorkItem it{};
+        it.chunk_off = st.chunk_off + static_cast<int32_t>(a);
+        it.n_chunks = static_cast<int32_t>(b - a);
+        it.kv = st.kv;
+        it.group0 = st.group;
+        it.row0 = 0;
+        it.n_rows = g;
+        it.part_base = static_cast<int32_t>(prow);
+        push_item(simt_items, it);
+        ment.emplace_back(st.group * Hkv + st.kv, static_cast<int32_t>(prow));
+        prow += g;
+        ++item_count;
+        t = t_base + b;
+      }
+      wcur = w;
+    }
+    (void)wcur;
+    warp_items[W] = item_count;
+  }
+  p->n_simt_items = static_cast<int32_t>(simt_items.size() / 8);
+  p->n_part_rows = prow;
+
+  // ---- merge CSR per (batch row, KV head), emission order kept
+  std::vector<int32_t> moff(static_cast<size_t>(B) * Hkv + 1, 0), ments(ment.size());
+  for (const auto& e : ment) moff[e.first + 1]++;
+  for (size_t x = 1; x < moff.size(); ++x) moff[x] += moff[x - 1];
+  {
+    std::vector<int32_t> fill(moff.begin(), moff.end() - 1);
+    for (const auto& e : ment) ments[fill[e.first]++] = e.second;
+  }
+
+  // ---- pack the table image
+  auto& t = p->h_tab;
+  t.clear();
+  p->off_chunks = t.size();
+  t.insert(t.end(), chunks.begin(), chunks.end());
+  while (t.size() % 8) t.push_back(0);  // 32-byte alignment of the item arrays
+  p->off_tc = t.size();
+  t.insert(t.end(), tc_items.begin(), tc_items.end());
+  p->off_simt = t.size();
+  t.insert(t.end(), simt_items.begin(), simt_items.end());
+  p->off_warp = t.size();
+  t.insert(t.end(), warp_items.begin(), warp_items.end());
+  p->off_moff = t.size();
+  t.insert(t.end(), moff.begin(), moff.end());
+  p->off_ment = t.size();
+  t.insert(t.end(), ments.begin(), ments.end());
+  if (t.empty()) t.push_back(0);
+
+  p->rebuild_count++;
+  p->dirty = false;
+  p->tab_uploaded = false;
+  p->last_rebuild_us =
+      std::chrono::duration<double, std::micro>(std::chrono::steady_clock::now() - t0).count();
+  return PST_OK;
+}
+
+// Copy the table image and size the partial buffers, on the decode stream.
+pst_status sync_device_tables(pst_pool* p, cudaStream_t s) {
+  if (p->tab_uploaded) return PST_OK;
+  if (static_cast<size_t>(p->n_part_rows) > p->part_cap) {
+    if (p->d_part_o) {
+      CUDA_TRY(cudaStreamSynchronize(s));
+      CUDA_TRY(cudaFree(p->d_part_o));
+      CUDA_TRY(cudaFree(p->d_part_ml));
+    }
+    const size_t cap = std::max<size_t>(static_cast<size_t>(p->n_part_rows) * 3 / 2, 1024);
+    CUDA_TRY(cudaMalloc(&p->d_part_o, cap * p->D * sizeof(float)));
+    CUDA_TRY(cudaMalloc(&p->d_part_ml, cap * 2 * sizeof(float)));
+    p->part_cap = cap;
+  }
+  pst_status st = upload(p, &p->d_tab, &p->tab_cap, p->h_tab, s);
+  if (st != PST_OK) return st;
+  p->tab_uploaded = true;
+  return PST_OK;
+}
+
+pst_status ensure_tables(const pst_pool* cp) {
+  pst_pool* p = const_cast<pst_pool*>(cp);
+  if (!p->dirty) return PST_OK;
+  return rebuild(p);
+}
+
+pst_status need_device(const pst_pool* p) {
+  if (!p) return fail(PST_ERR_INVALID, "null pool");
+  if (p->host_only) return fail(PST_ERR_STATE, "host-only pool has no device");
+  cudaError_t e = cudaSetDevice(p->device);
+  if (e != cudaSuccess) return fail(PST_ERR_CUDA, "cudaSetDevice: %s", cudaGetErrorString(e));
+  return PST_OK;
+}
+
+AttnParams base_params(const pst_pool* p) {
+  AttnParams a{};
+  a.pool = p->d_pool;
+  a.chunk_len = p->d_chunk_len;
+  a.Hq = p->cfg.n_q_heads;
+  a.Hkv = p->cfg.n_kv_heads;
+  a.g = p->g;
+  a.chunk_size = p->C;
+  a.causal_p0 = -1;
+  a.scale_log2 = p->scale_log2;
+  a.stages = p->simt_stages;
+  a.warps_per_cta = p->simt_wpc;
+  a.err = p->d_err;
+  return a;
+}
+
+}  // namespace
+
+// =================================================================== C ABI
+extern "C" {
+
+const char* pst_last_error(void) { return g_last_error.c_str(); }
+
+const char* pst_version(void) { return "pst 0.1 (sm_103a)"; }
+
+pst_status pst_pool_create(const pst_config* cfg, int device, pst_pool** out) {
+  g_last_error.clear();
+  if (!cfg || !out) return fail(PST_ERR_INVALID, "null argument");
+  const pst_config& c = *cfg;
+  if (c.n_q_heads < 1 || c.n_kv_heads < 1 || c.n_q_heads % c.n_kv_heads)
+    return fail(PST_ERR_INVALID, "n_q_heads must be a positive multiple of n_kv_heads");
+  const int g = c.n_q_heads / c.n_kv_heads;
+  if (c.dtype < 0 || c.dtype > 2) return fail(PST_ERR_INVALID, "bad dtype %d", c.dtype);
+  if (!simt_supported(c.dtype, c.head_dim, g))
+    return fail(PST_ERR_INVALID, "unsupported head_dim %d / group %d", c.head_dim, g);
+  if (c.chunk_size != 32 && c.chunk_size != 64) return fail(PST_ERR_INVALID, "chunk_size must be 32 or 64");
+  if (c.max_chunks < 1 || c.max_chunks > (int64_t(1) << 30)) return fail(PST_ERR_INVALID, "bad max_chunks");
+  if (c.min_share < 0 || c.max_seqs < 0) return fail(PST_ERR_INVALID, "negative min_share / max_seqs");
+  if (device < -1) return fail(PST_ERR_INVALID, "bad device");
+
+  pst_pool* p = new pst_pool();
+  p->cfg = c;
+  if (p->cfg.min_share == 0) p->cfg.min_share = 2;
+  if (p->cfg.max_seqs == 0) p->cfg.max_seqs = 4096;
+  p->device = device;
+  p->host_only = device < 0;
+  p->es = dtype_size(c.dtype);
+  p->C = c.chunk_size;
+  p->D = c.head_dim;
+  p->g = g;
+  p->half_bytes = static_cast<size_t>(p->C) * p->D * p->es;
+  p->tile_bytes = 2 * p->half_bytes;
+  p->scale_log2 = static_cast<float>(1.0 / std::log(2.0) / std::sqrt(static_cast<double>(p->D)));
+  p->nodes.emplace_back();  // virtual root
+  p->nodes[0].live = true;
+  p->free_chunks.reserve(c.max_chunks);
+  for (int64_t x = c.max_chunks - 1; x >= 0; --x) p->free_chunks.push_back(static_cast<int32_t>(x));
+
+  // CUDA-core kernel shape: 4 warps x 3 half-tile stages when it fits
+  p->simt_wpc = 4;
+  p->simt_stages = 3;
+  while (attn_simt_smem(c.dtype, p->D, p->C, g, p->simt_stages, p->simt_wpc) > 200 * 1024) {
+    if (p->simt_stages > 2) p->simt_stages--;
+    else p->simt_wpc--;
+  }
+
+  if (!p->host_only) {
+    auto bail = [&](cudaError_t e, const char* what) {
+      pst_status st = fail(PST_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+      pst_pool_free(p);
+      return st;
+    };
+    cudaError_t e = cudaSetDevice(device);
+    if (e != cudaSuccess) return bail(e, "cudaSetDevice");
+    int major = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, device);
+    cudaDeviceGetAttribute(&p->n_sm, cudaDevAttrMultiProcessorCount, device);
+    p->use_tc = major == 10 && tc_supported(c.dtype, p->D, p->C) && !(c.flags & PST_FLAG_NO_TENSOR_CORES);
+    const size_t slab = static_cast<size_t>(c.max_chunks) * c.n_kv_heads * p->tile_bytes;
+    if ((e = cudaMalloc(&p->d_pool, slab)) != cudaSuccess) return bail(e, "cudaMalloc(pool)");
+    if ((e = cudaMemset(p->d_pool, 0, slab)) != cudaSuccess) return bail(e, "cudaMemset(pool)");
+    if ((e = cudaMalloc(&p->d_chunk_len, sizeof(int32_t) * c.max_chunks)) != cudaSuccess) return bail(e, "cudaMalloc");
+    if ((e = cudaMemset(p->d_chunk_len, 0, sizeof(int32_t) * c.max_chunks)) != cudaSuccess) return bail(e, "cudaMemset");
+    if ((e = cudaMalloc(&p->d_err, sizeof(int32_t))) != cudaSuccess) return bail(e, "cudaMalloc");
+    if ((e = cudaMemset(p->d_err, 0, sizeof(int32_t))) != cudaSuccess) return bail(e, "cudaMemset");
+    if ((e = cudaStreamCreateWithFlags(&p->aux, cudaStreamNonBlocking)) != cudaSuccess) return bail(e, "stream");
+    if ((e = cudaEventCreateWithFlags(&p->ev_fork, cudaEventDisableTiming)) != cudaSuccess) return bail(e, "event");
+    if ((e = cudaEventCreateWithFlags(&p->ev_join, cudaEventDisableTiming)) != cudaSuccess) return bail(e, "event");
+    if ((e = cudaEventCreateWithFlags(&p->ev_stage, cudaEventDisableTiming)) != cudaSuccess) return bail(e, "event");
+    for (auto& ev : p->pev)
+      if ((e = cudaEventCreate(&ev)) != cudaSuccess) return bail(e, "event");
+    if ((e = cudaDeviceSynchronize()) != cudaSuccess) return bail(e, "cudaDeviceSynchronize");
+  }
+  *out = p;
+  return PST_OK;
+}
+
+pst_status pst_pool_free(pst_pool* p) {
+  if (!p) return fail(PST_ERR_INVALID, "null pool");
+  if (!p->host_only) {
+    cudaSetDevice(p->device);
+    cudaDeviceSynchronize();
+    cudaFree(p->d_pool);
+    cudaFree(p->d_chunk_len);
+    cudaFree(p->d_tab);
+    cudaFree(p->d_part_o);
+    cudaFree(p->d_part_ml);
+    cudaFree(p->d_err);
+    cudaFree(p->d_pre);
+    cudaFree(p->d_q);
+    cudaFree(p->d_out);
+    if (p->h_stage) cudaFreeHost(p->h_stage);
+    if (p->aux) cudaStreamDestroy(p->aux);
+    if (p->ev_fork) cudaEventDestroy(p->ev_fork);
+    if (p->ev_join) cudaEventDestroy(p->ev_join);
+    if (p->ev_stage) cudaEventDestroy(p->ev_stage);
+    for (auto& ev : p->pev)
+      if (ev) cudaEventDestroy(ev);
+  }
+  delete p;
+  return PST_OK;
+}
+
+pst_status pst_match(const pst_pool* p, const int32_t* tokens, int64_t n, int64_t* n_matched) {
+  if (!p || !n_matched || (n > 0 && !tokens) || n < 0) return fail(PST_ERR_INVALID, "bad argument");
+  *n_matched = match_path(p, tokens, n, nullptr);
+  return PST_OK;
+}
+
+pst_status pst_insert(pst_pool* p, const int32_t* tokens, int64_t n, const void* k, const void* v, void* stream,
+                      int64_t* seq_id, int64_t* n_matched) {
+  if (!p || !tokens || n < 1 || !seq_id) return fail(PST_ERR_INVALID, "bad argument");
+  if (static_cast<int64_t>(p->seqs.size()) >= p->cfg.max_seqs)
+    return fail(PST_ERR_OOM, "max_seqs (%d) live sequences", p->cfg.max_seqs);
+  std::vector<int32_t> path;
+  const int64_t m = match_path(p, tokens, n, &path);
+  const int64_t need = ceil_div(n - m, p->C);
+  if (need > static_cast<int64_t>(p->free_chunks.size()))
+    return fail(PST_ERR_OOM, "pool exhausted: need %lld chunks, %zu free", (long long)need, p->free_chunks.size());
+  if (m < n) {
+    if (p->host_only) {
+      if (k || v) return fail(PST_ERR_STATE, "host-only pool takes no K/V");
+    } else if (!k || !v) {
+      return fail(PST_ERR_INVALID, "k/v required for %lld unmatched tokens", (long long)(n - m));
+    }
+  }
+  if (!p->host_only) {
+    pst_status st = need_device(p);
+    if (st != PST_OK) return st;
+  }
+  std::vector<ScatterOp> ops;
+  int32_t cur = path.empty() ? 0 : path.back();
+  for (int64_t pos = m; pos < n; pos += p->C) {
+    const int32_t id = new_node(p, cur);
+    const int64_t end = std::min<int64_t>(pos + p->C, n);
+    for (int64_t x = pos; x < end; ++x) push_token(p, id, tokens[x]);
+    ops.push_back({p->nodes[id].chunk, static_cast<int32_t>(pos), 0, static_cast<int32_t>(end - pos), 1});
+    path.push_back(id);
+    cur = id;
+  }
+  for (int32_t id : path) p->nodes[id].refs++;
+  const int64_t sid = p->next_seq++;
+  p->nodes[path.back()].ending.push_back(sid);
+  Seq sq;
+  sq.path = std::move(path);
+  sq.length = n;
+  p->seqs.emplace(sid, std::move(sq));
+  mark_structural(p);
+  *seq_id = sid;
+  if (n_matched) *n_matched = m;
+  return run_scatter(p, ops, k, v, static_cast<cudaStream_t>(stream), false);
+}
+
+// Apply one appended token to the tree; fills *op with its scatter op.
+static void append_one(pst_pool* p, Seq& sq, int64_t sid, int32_t token, ScatterOp* op, int32_t src_row) {
+  const int32_t leaf = sq.path.back();
+  if (p->nodes[leaf].n_tokens < p->C) {
+    const int32_t r = p->nodes[leaf].n_tokens;
+    push_token(p, leaf, token);
+    *op = {p->nodes[leaf].chunk, src_row, r, r + 1, 0};
+  } else {
+    const int32_t id = new_node(p, leaf);
+    push_token(p, id, token);
+    p->nodes[id].refs = 1;
+    auto& end = p->nodes[leaf].ending;
+    end.erase(std::find(end.begin(), end.end(), sid));
+    p->nodes[id].ending.push_back(sid);
+    sq.path.push_back(id);
+    *op = {p->nodes[id].chunk, src_row, 0, 1, 1};
+    mark_structural(p);
+  }
+  sq.length++;
+}
+
+pst_status pst_append(pst_pool* p, int64_t seq_id, int32_t token, const void* k, const void* v, void* stream) {
+  return pst_append_batch(p, 1, &seq_id, &token, k, v, stream);
+}
+
+pst_status pst_append_batch(pst_pool* p, int64_t n, const int64_t* seq_ids, const int32_t* tokens, const void* k,
+                            const void* v, void* stream) {
+  if (!p || n < 0 || (n > 0 && (!seq_ids || !tokens))) return fail(PST_ERR_INVALID, "bad argument");
+  if (n == 0) return PST_OK;
+  if (p->host_only ? (k || v) : (!k || !v)) return fail(PST_ERR_INVALID, "k/v pointers do not match pool kind");
+  int64_t need = 0;
+  std::vector<int64_t> sorted(seq_ids, seq_ids + n);
+  std::sort(sorted.begin(), sorted.end());
+  if (std::adjacent_find(sorted.begin(), sorted.end()) != sorted.end())
+    return fail(PST_ERR_INVALID, "duplicate sequence id in batch append");
+  for (int64_t x = 0; x < n; ++x) {
+    auto it = p->seqs.find(seq_ids[x]);
+    if (it == p->seqs.end()) return fail(PST_ERR_NOT_FOUND, "unknown sequence %lld", (long long)seq_ids[x]);
+    if (p->nodes[it->second.path.back()].n_tokens == p->C) ++need;
+  }
+  if (need > static_cast<int64_t>(p->free_chunks.size())) return fail(PST_ERR_OOM, "pool exhausted on append");
+  if (!p->host_only) {
+    pst_status st = need_device(p);
+    if (st != PST_OK) return st;
+  }
+  std::vector<ScatterOp> ops(n);
+  for (int64_t x = 0; x < n; ++x) append_one(p, p->seqs[seq_ids[x]], seq_ids[x], tokens[x], &ops[x], static_cast<int32_t>(x));
+  return run_scatter(p, ops, k, v, static_cast<cudaStream_t>(stream), false);
+}
+
+pst_status pst_remove(pst_pool* p, int64_t seq_id) {
+  if (!p) return fail(PST_ERR_INVALID, "null pool");
+  auto it = p->seqs.find(seq_id);
+  if (it == p->seqs.end()) return fail(PST_ERR_NOT_FOUND, "unknown sequence %lld", (long long)seq_id);
+  Seq& sq = it->second;
+  auto& end = p->nodes[sq.path.back()].ending;
+  end.erase(std::find(end.begin(), end.end(), seq_id));
+  for (int32_t id : sq.path) p->nodes[id].refs--;
+  for (auto r = sq.path.rbegin(); r != sq.path.rend(); ++r)
+    if (p->nodes[*r].refs == 0) release_node(p, *r);
+  p->seqs.erase(it);
+  mark_structural(p);
+  return PST_OK;
+}
+
+pst_status pst_batch_order(const pst_pool* p, int64_t* seq_ids, int64_t cap, int64_t* B) {
+  if (!p || !B || cap < 0 || (cap > 0 && !seq_ids)) return fail(PST_ERR_INVALID, "bad argument");
+  pst_status st = ensure_tables(p);
+  if (st != PST_OK) return st;
+  *B = static_cast<int64_t>(p->batch.size());
+  for (int64_t x = 0; x < std::min<int64_t>(cap, *B); ++x) seq_ids[x] = p->batch[x];
+  return PST_OK;
+}
+
+pst_status pst_seq_length(const pst_pool* p, int64_t seq_id, int64_t* n_tokens) {
+  if (!p || !n_tokens) return fail(PST_ERR_INVALID, "bad argument");
+  auto it = p->seqs.find(seq_id);
+  if (it == p->seqs.end()) return fail(PST_ERR_NOT_FOUND, "unknown sequence %lld", (long long)seq_id);
+  *n_tokens = it->second.length;
+  return PST_OK;
+}
+
+static pst_status decode_impl(pst_pool* p, const void* q, void* out, cudaStream_t s) {
+  pst_status st = ensure_tables(p);
+  if (st != PST_OK) return st;
+  st = sync_device_tables(p, s);
+  if (st != PST_OK) return st;
+  p->last_launches = 0;
+  p->pran[0] = p->pran[1] = p->pran[2] = false;
+  const int32_t B = static_cast<int32_t>(p->batch.size());
+  if (B == 0) return PST_OK;
+  AttnParams a = base_params(p);
+  a.q = q;
+  a.part_o = p->d_part_o;
+  a.part_ml = p->d_part_ml;
+  a.chunks = p->d_tab + p->off_chunks;
+  const bool fork = p->n_tc_items > 0 && p->n_simt_items > 0 && !(p->cfg.flags & PST_FLAG_SERIAL_PHASES);
+  cudaStream_t s1 = fork ? p->aux : s;
+  if (fork) {
+    CUDA_TRY(cudaEventRecord(p->ev_fork, s));
+    CUDA_TRY(cudaStreamWaitEvent(p->aux, p->ev_fork, 0));
+  }
+  if (p->n_tc_items > 0) {
+    AttnParams a1 = a;
+    a1.items = reinterpret_cast<const WorkItem*>(p->d_tab + p->off_tc);
+    a1.n_items = p->n_tc_items;
+    if (p->profiling) CUDA_TRY(cudaEventRecord(p->pev[0], s1));
+    cudaError_t e = launch_attn_tc(p->cfg.dtype, p->D, a1, p->n_tc_items, s1);
+    if (e != cudaSuccess) return fail(PST_ERR_CUDA, "chunk-first launch: %s", cudaGetErrorString(e));
+    if (p->profiling) CUDA_TRY(cudaEventRecord(p->pev[1], s1));
+    p->pran[0] = true;
+    p->last_launches++;
+  }
+  if (p->n_simt_items > 0) {
+    AttnParams a2 = a;
+    a2.items = reinterpret_cast<const WorkItem*>(p->d_tab + p->off_simt);
+    a2.n_items = p->n_simt_items;
+    a2.warp_items = p->d_tab + p->off_warp;
+    a2.n_warps = p->n_simt_warps;
+    if (p->profiling) CUDA_TRY(cudaEventRecord(p->pev[2], s));
+    cudaError_t e = launch_attn_simt(p->cfg.dtype, p->D, p->g, a2, p->simt_grid, s);
+    if (e != cudaSuccess) return fail(PST_ERR_CUDA, "sequence-first launch: %s", cudaGetErrorString(e));
+    if (p->profiling) CUDA_TRY(cudaEventRecord(p->pev[3], s));
+    p->pran[1] = true;
+    p->last_launches++;
+  }
+  if (fork) {
+    CUDA_TRY(cudaEventRecord(p->ev_join, p->aux));
+    CUDA_TRY(cudaStreamWaitEvent(s, p->ev_join, 0));
+  }
+  MergeParams mp{};
+  mp.off = p->d_tab + p->off_moff;
+  mp.ent = p->d_tab + p->off_ment;
+  mp.part_o = p->d_part_o;
+  mp.part_ml = p->d_part_ml;
+  mp.out = out;
+  mp.B = B;
+  mp.Hq = p->cfg.n_q_heads;
+  mp.Hkv = p->cfg.n_kv_heads;
+  mp.g = p->g;
+  mp.err = p->d_err;
+  if (p->profiling) CUDA_TRY(cudaEventRecord(p->pev[4], s));
+  cudaError_t e = launch_merge(p->cfg.dtype, p->D, mp, s);
+  if (e != cudaSuccess) return fail(PST_ERR_CUDA, "merge launch: %s", cudaGetErrorString(e));
+  if (p->profiling) CUDA_TRY(cudaEventRecord(p->pev[5], s));
+  p->pran[2] = true;
+  p->last_launches++;
+  return PST_OK;
+}
+
+pst_status pst_decode_attention(pst_pool* p, const void* q, void* out, void* stream) {
+  pst_status st = need_device(p);
+  if (st != PST_OK) return st;
+  if (!q || !out) return fail(PST_ERR_INVALID, "null q/out");
+  return decode_impl(p, q, out, static_cast<cudaStream_t>(stream));
+}
+
+pst_status pst_decode_attention_host(pst_pool* p, const void* q_host, void* out_host, void* stream) {
+  pst_status st = need_device(p);
+  if (st != PST_OK) return st;
+  if (!q_host || !out_host) return fail(PST_ERR_INVALID, "null q/out");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  st = ensure_tables(p);
+  if (st != PST_OK) return st;
+  const size_t bytes = p->batch.size() * p->cfg.n_q_heads * p->D * p->es;
+  if (bytes == 0) return PST_OK;
+  if (bytes > p->qo_cap) {
+    CUDA_TRY(cudaStreamSynchronize(s));
+    cudaFree(p->d_q);
+    cudaFree(p->d_out);
+    p->d_q = p->d_out = nullptr;
+    CUDA_TRY(cudaMalloc(&p->d_q, bytes));
+    CUDA_TRY(cudaMalloc(&p->d_out, bytes));
+    p->qo_cap = bytes;
+  }
+  CUDA_TRY(cudaMemcpyAsync(p->d_q, q_host, bytes, cudaMemcpyHostToDevice, s));
+  st = decode_impl(p, p->d_q, p->d_out, s);
+  if (st != PST_OK) return st;
+  CUDA_TRY(cudaMemcpyAsync(out_host, p->d_out, bytes, cudaMemcpyDeviceToHost, s));
+  CUDA_TRY(cudaStreamSynchronize(s));
+  return PST_OK;
+}
+
+pst_status pst_prefill_attend(pst_pool* p, int64_t seq_id, const int32_t* tokens, int64_t W, const void* q,
+                              const void* k_new, const void* v_new, void* out, void* stream) {
+  pst_status st = need_device(p);
+  if (st != PST_OK) return st;
+  if (!tokens || W < 1 || !q || !k_new || !v_new || !out) return fail(PST_ERR_INVALID, "bad argument");
+  auto it = p->seqs.find(seq_id);
+  if (it == p->seqs.end()) return fail(PST_ERR_NOT_FOUND, "unknown sequence %lld", (long long)seq_id);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  Seq& sq = it->second;
+  const int64_t p0 = sq.length;
+  const int32_t leaf = sq.path.back();
+  const int64_t room = p->C - p->nodes[leaf].n_tokens;
+  const int64_t need = ceil_div(std::max<int64_t>(0, W - room), p->C);
+  if (need > static_cast<int64_t>(p->free_chunks.size())) return fail(PST_ERR_OOM, "pool exhausted on prefill");
+  if (p0 + W > INT32_MAX / 2) return fail(PST_ERR_INVALID, "sequence too long");
+
+  // append the block's tokens (never shared with other sequences)
+  std::vector<ScatterOp> ops;
+  int64_t pos = 0;
+  if (room > 0) {
+    const int32_t r0 = p->nodes[leaf].n_tokens;
+    const int64_t take = std::min<int64_t>(room, W);
+    for (int64_t x = 0; x < take; ++x) push_token(p, leaf, tokens[x]);
+    ops.push_back({p->nodes[leaf].chunk, 0, r0, static_cast<int32_t>(r0 + take), 0});
+    pos = take;
+  }
+  while (pos < W) {
+    const int32_t cur = sq.path.back();
+    const int32_t id = new_node(p, cur);
+    const int64_t end = std::min<int64_t>(pos + p->C, W);
+    for (int64_t x = pos; x < end; ++x) push_token(p, id, tokens[x]);
+    p->nodes[id].refs = 1;
+    auto& e = p->nodes[cur].ending;
+    e.erase(std::find(e.begin(), e.end(), seq_id));
+    p->nodes[id].ending.push_back(seq_id);
+    sq.path.push_back(id);
+    ops.push_back({p->nodes[id].chunk, static_cast<int32_t>(pos), 0, static_cast<int32_t>(end - pos), 1});
+    pos = end;
+  }
+  sq.length += W;
+  if (need > 0) mark_structural(p);
+  st = run_scatter(p, ops, k_new, v_new, s, false);
+  if (st != PST_OK) return st;
+
+  // work: the sequence's chunk list, then one item per (KV head, row tile)
+  std::vector<int32_t> tab;
+  for (int32_t id : sq.path) tab.push_back(p->nodes[id].chunk);
+  while (tab.size() % 8) tab.push_back(0);
+  const size_t off_items = tab.size();
+  const int g = p->g, Hkv = p->cfg.n_kv_heads;
+  const int64_t rows = W * g;
+  std::vector<int32_t> warp_items;
+  int32_t n_items = 0;
+  if (p->use_tc) {
+    for (int kv = 0; kv < Hkv; ++kv)
+      for (int64_t r0 = 0; r0 < rows; r0 += 128) {
+        WorkItem w{};
+        w.chunk_off = 0;
+        w.kv = kv;
+        w.group0 = 0;
+        w.row0 = static_cast<int32_t>(r0);
+        w.n_rows = static_cast<int32_t>(std::min<int64_t>(128, rows - r0));
+        const int64_t t_last = (r0 + w.n_rows - 1) / g;
+        w.n_chunks = static_cast<int32_t>(ceil_div(p0 + t_last + 1, p->C));
+        push_item(tab, w);
+        ++n_items;
+      }
+  } else {
+    for (int64_t t = 0; t < W; ++t)
+      for (int kv = 0; kv < Hkv; ++kv) {
+        WorkItem w{};
+        w.chunk_off = 0;
+        w.kv = kv;
+        w.group0 = static_cast<int32_t>(t);
+        w.n_rows = g;
+        w.n_chunks = static_cast<int32_t>(ceil_div(p0 + t + 1, p->C));
+        push_item(tab, w);
+        ++n_items;
+      }
+  }
+  const size_t off_warp = tab.size();
+  int32_t grid = 0, n_warps = 0;
+  if (!p->use_tc) {
+    n_warps = n_items;
+    grid = static_cast<int32_t>(ceil_div(n_warps, p->simt_wpc));
+    for (int32_t x = 0; x <= n_warps; ++x) tab.push_back(x);
+  }
+  st = upload(p, &p->d_pre, &p->pre_cap, tab, s);
+  if (st != PST_OK) return st;
+
+  AttnParams a = base_params(p);
+  a.q = q;
+  a.out = out;
+  a.final_mode = 1;
+  a.causal_p0 = static_cast<int32_t>(p0);
+  a.chunks = p->d_pre;
+  a.items = reinterpret_cast<const WorkItem*>(p->d_pre + off_items);
+  a.n_items = n_items;
+  cudaError_t e;
+  if (p->use_tc) {
+    e = launch_attn_tc(p->cfg.dtype, p->D, a, n_items, s);
+  } else {
+    a.warp_items = p->d_pre + off_warp;
+    a.n_warps = n_warps;
+    e = launch_attn_simt(p->cfg.dtype, p->D, g, a, grid, s);
+  }
+  if (e != cudaSuccess) return fail(PST_ERR_CUDA, "prefill launch: %s", cudaGetErrorString(e));
+  return PST_OK;
+}
+
+pst_status pst_gather_kv(const pst_pool* p, int64_t seq_id, void* k_out, void* v_out, void* stream) {
+  pst_status st = need_device(p);
+  if (st != PST_OK) return st;
+  if (!k_out || !v_out) return fail(PST_ERR_INVALID, "null output");
+  auto it = p->seqs.find(seq_id);
+  if (it == p->seqs.end()) return fail(PST_ERR_NOT_FOUND, "unknown sequence %lld", (long long)seq_id);
+  std::vector<ScatterOp> ops;
+  int32_t pos = 0;
+  for (int32_t id : it->second.path) {
+    const Node& n = p->nodes[id];
+    ops.push_back({n.chunk, pos, 0, n.n_tokens, 0});
+    pos += n.n_tokens;
+  }
+  return run_scatter(const_cast<pst_pool*>(p), ops, k_out, v_out, static_cast<cudaStream_t>(stream), true);
+}
+
+pst_status pst_export_tables(const pst_pool* p, int32_t* shared_rows, int64_t shared_cap, int64_t* n_shared,
+                             int32_t* seq_entries, int64_t entries_cap, int64_t* n_entries, int64_t* seq_offsets,
+                             int64_t offsets_cap, int64_t* B) {
+  if (!p || !n_shared || !n_entries || !B) return fail(PST_ERR_INVALID, "null count pointer");
+  pst_status st = ensure_tables(p);
+  if (st != PST_OK) return st;
+  *n_shared = static_cast<int64_t>(p->canon_shared.size() / 4);
+  *n_entries = static_cast<int64_t>(p->canon_entries.size() / 2);
+  *B = static_cast<int64_t>(p->batch.size());
+  if (shared_cap < *n_shared || entries_cap < *n_entries || offsets_cap < *B + 1) {
+    if (shared_cap == 0 && entries_cap == 0 && offsets_cap == 0) return PST_OK;
+    return fail(PST_ERR_INVALID, "export buffers too small");
+  }
+  if (*n_shared) std::memcpy(shared_rows, p->canon_shared.data(), p->canon_shared.size() * sizeof(int32_t));
+  if (*n_entries) std::memcpy(seq_entries, p->canon_entries.data(), p->canon_entries.size() * sizeof(int32_t));
+  std::memcpy(seq_offsets, p->canon_offsets.data(), p->canon_offsets.size() * sizeof(int64_t));
+  return PST_OK;
+}
+
+pst_status pst_stats(const pst_pool* p, pst_stats_t* o) {
+  if (!p || !o) return fail(PST_ERR_INVALID, "bad argument");
+  std::memset(o, 0, sizeof(*o));
+  o->live_seqs = static_cast<int64_t>(p->seqs.size());
+  o->max_chunks = p->cfg.max_chunks;
+  o->free_chunks = static_cast<int64_t>(p->free_chunks.size());
+  o->used_chunks = o->max_chunks - o->free_chunks;
+  int64_t uniq = 0;
+  for (size_t i = 1; i < p->nodes.size(); ++i)
+    if (p->nodes[i].live) uniq += p->nodes[i].n_tokens;
+  o->unique_tokens = uniq;
+  for (const auto& kv : p->seqs) o->logical_tokens += kv.second.length;
+  o->shared_chunks = p->shared_chunks;
+  o->table_version = p->version;
+  o->rebuild_count = p->rebuild_count;
+  o->last_rebuild_us = p->last_rebuild_us;
+  o->phase1_items = p->n_tc_items;
+  o->phase2_items = p->n_simt_items;
+  o->partial_rows = p->n_part_rows;
+  return PST_OK;
+}
+
+pst_status pst_set_profiling(pst_pool* p, int enable) {
+  pst_status st = need_device(p);
+  if (st != PST_OK) return st;
+  p->profiling = enable != 0;
+  return PST_OK;
+}
+
+pst_status pst_phase_times(pst_pool* p, float* ms3) {
+  pst_status st = need_device(p);
+  if (st != PST_OK) return st;
+  if (!ms3) return fail(PST_ERR_INVALID, "null output");
+  if (!p->profiling) return fail(PST_ERR_STATE, "profiling is off");
+  for (int i = 0; i < 3; ++i) {
+    ms3[i] = 0.f;
+    if (!p->pran[i]) continue;
+    CUDA_TRY(cudaEventSynchronize(p->pev[2 * i + 1]));
+    CUDA_TRY(cudaEventElapsedTime(&ms3[i], p->pev[2 * i], p->pev[2 * i + 1]));
+  }
+  return PST_OK;
+}
+
+pst_status pst_last_launch_count(const pst_pool* p, int32_t* n) {
+  if (!p || !n) return fail(PST_ERR_INVALID, "bad argument");
+  *n = p->last_launches;
+  return PST_OK;
+}
+
+pst_status pst_check_device(pst_pool* p, int32_t* code) {
+  pst_status st = need_device(p);
+  if (st != PST_OK) return st;
+  if (!code) return fail(PST_ERR_INVALID, "null output");
+  CUDA_TRY(cudaDeviceSynchronize());
+  CUDA_TRY(cudaMemcpy(code, p->d_err, sizeof(int32_t), cudaMemcpyDeviceToHost));
+  CUDA_TRY(cudaMemset(p->d_err, 0, sizeof(int32_t)));
+  if (*code) return fail(PST_ERR_DEVICE, "device error word 0x%x", *code);
+  return PST_OK;
+}
+
+}  // extern "C"

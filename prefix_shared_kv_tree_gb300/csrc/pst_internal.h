@@ -1,0 +1,113 @@
+// Internal types shared by the host tree manager (pool.cpp) and the CUDA
+// kernels (*.cu).  Not part of the public ABI.
+#pragma once
+
+#include <stdint.h>
+#include <cuda_runtime.h>
+
+namespace pst {
+
+enum Dtype : int32_t { kF16 = 0, kBF16 = 1, kF32 = 2 };
+
+inline int dtype_size(int dt) { return dt == kF32 ? 4 : 2; }
+
+// ---------------------------------------------------------------------------
+// Pool layout.  The slab holds, per (chunk, KV head), one contiguous tile of
+// 2 * C * D elements: first the K block (C key rows x D), then the transposed
+// V block (D rows x C keys).  Both blocks are stored as 8-row x 16-byte "core
+// matrices", row-group major:
+//   byte(r, j) = ((r / 8) * (row_bytes / 16) + j) * 128 + (r % 8) * 16
+// where r is the row (key for K, feature for V^T) and j the 16-byte column
+// chunk.  This is the K-major, no-swizzle operand image the tcgen05 tensor
+// cores read from shared memory, so one bulk copy stages a tile ready for MMA,
+// and it gives conflict-free 16-byte shared-memory reads to the CUDA-core
+// kernel as well.
+// ---------------------------------------------------------------------------
+__host__ __device__ inline uint32_t cm_off(uint32_t r, uint32_t j, uint32_t chunks_per_row) {
+  return ((r >> 3) * chunks_per_row + j) * 128u + (r & 7u) * 16u;
+}
+
+// One unit of partial-attention work: a list of chunks of one KV head against
+// n_rows query rows.  Query rows are numbered in a "group-row" space: row
+// rr = row0 + r belongs to group group0 + rr / g and query head kv * g + rr % g,
+// where a group is a batch row (decode) or a token of the prefill block.
+struct WorkItem {
+  int32_t chunk_off;  // first entry in the chunk-id list
+  int32_t n_chunks;
+  int32_t kv;
+  int32_t group0;
+  int32_t row0;
+  int32_t n_rows;
+  int32_t part_base;  // partial-result row of r = 0 (partial mode)
+  int32_t pad;
+};
+static_assert(sizeof(WorkItem) == 32, "WorkItem layout");
+
+struct AttnParams {
+  const uint8_t* pool;        // chunk slab
+  const int32_t* chunk_len;   // valid tokens of each physical chunk
+  const int32_t* chunks;      // chunk-id lists
+  const WorkItem* items;
+  const int32_t* warp_items;  // CUDA-core kernel: item range [warp_items[w], warp_items[w+1]) of warp w
+  int32_t n_items;
+  int32_t n_warps;            // CUDA-core kernel: warps in the grid
+  const void* q;              // [groups][Hq][D]
+  void* out;                  // final mode: [groups][Hq][D]
+  float* part_o;              // partial mode: [rows][D]
+  float* part_ml;             // partial mode: [rows][2] = (m, n), m in log2 units
+  int32_t Hq, Hkv, g;
+  int32_t chunk_size;
+  int32_t final_mode;         // 0: write (o, m, n) partials; 1: write o / n to out
+  int32_t causal_p0;          // >= 0: group t sees keys [0, causal_p0 + t]; < 0: no causal limit
+  float scale_log2;           // log2(e) / sqrt(D), computed on the host
+  int32_t stages;             // CUDA-core kernel: half-tile stages per warp
+  int32_t warps_per_cta;      // CUDA-core kernel
+  int32_t* err;               // device error word
+};
+
+struct MergeParams {
+  const int32_t* off;    // [B * Hkv + 1] CSR offsets per (batch row, KV head)
+  const int32_t* ent;    // partial row of query head kv*g + 0; head kv*g + hg is at +hg
+  const float* part_o;
+  const float* part_ml;
+  void* out;             // [B][Hq][D]
+  int32_t B, Hq, Hkv, g;
+  int32_t* err;
+};
+
+// Copies user K/V rows into pool tiles (or back out, for gather).
+struct ScatterOp {
+  int32_t chunk;     // physical chunk
+  int32_t src_row;   // first user row (token) of this op
+  int32_t r0, r1;    // rows [r0, r1) of the chunk are written from src_row...
+  int32_t zero_tail; // 1: rows [r1, C) are zero-filled (freshly allocated chunk)
+};
+constexpr int kScatterMax = 128;
+struct ScatterParams {
+  const uint8_t* k;   // scatter: source [rows][Hkv][D]; gather: destination
+  const uint8_t* v;
+  uint8_t* pool;
+  int32_t* chunk_len;
+  int32_t n_ops;
+  int32_t Hkv;
+  ScatterOp ops[kScatterMax];
+};
+
+// Error codes OR-ed into the device error word.
+enum : int32_t {
+  kErrWaitTimeout = 1,   // a bounded mbarrier wait ran out
+  kErrBadIndex = 2,      // an index check failed
+};
+
+// Launchers (defined in the .cu files).  All return the launch status.
+cudaError_t launch_scatter(int dtype, int D, int C, const ScatterParams& p, cudaStream_t s);
+cudaError_t launch_gather(int dtype, int D, int C, const ScatterParams& p, cudaStream_t s);
+cudaError_t launch_attn_simt(int dtype, int D, int g, const AttnParams& p, int grid, cudaStream_t s);
+size_t attn_simt_smem(int dtype, int D, int C, int g, int stages, int warps_per_cta);
+cudaError_t launch_attn_tc(int dtype, int D, const AttnParams& p, int grid, cudaStream_t s);
+size_t attn_tc_smem(int D);
+cudaError_t launch_merge(int dtype, int D, const MergeParams& p, cudaStream_t s);
+bool simt_supported(int dtype, int D, int g);
+bool tc_supported(int dtype, int D, int C);
+
+}  // namespace pst

@@ -234,3 +234,27 @@ def ragged_sequences(seed: int, n_seqs: int, prefix_len: int, tail_lens: List[in
         vs.append(torch.cat([pv, v]))
     q = _normal(gen, (n_seqs, n_q_heads, head_dim), dt, "cpu")
     return toks, ks, vs, q
+
+
+def insert_all(pool, wl: Workload, stream=None, nan_matched: bool = False, device: str = "cuda"):
+    """Insert every sequence of ``wl`` into ``pool`` (insertion order = leaf DFS order).
+
+    Each call passes the sequence's full K/V rows on ``device``; when
+    ``nan_matched`` is set, the rows the pool will not read (the matched
+    prefix) are overwritten with NaN first.  Returns the sequence ids.
+    """
+    ids = []
+    for s in range(wl.n_sequences):
+        toks = wl.seq_tokens(s).cpu()
+        k = wl.seq_k(s).to(device)
+        v = wl.seq_v(s).to(device)
+        if nan_matched:
+            m = pool.match(toks)
+            if m:
+                k = k.clone()
+                v = v.clone()
+                k[:m] = float("nan")
+                v[:m] = float("nan")
+        sid, _ = pool.insert(toks, k, v, stream)
+        ids.append(sid)
+    return ids
