@@ -51,8 +51,9 @@ typedef enum { PST_F16 = 0, PST_BF16 = 1, PST_F32 = 2 } pst_dtype;
 
 /* pst_config.flags */
 enum {
-  PST_FLAG_NO_TENSOR_CORES = 1, /* run the chunk-first phase on the CUDA-core kernel too */
-  PST_FLAG_SERIAL_PHASES = 2    /* launch both phases on the caller's stream (no fork/join) */
+  PST_FLAG_NO_TENSOR_CORES = 1,  /* run the chunk-first phase on the CUDA-core kernel too */
+  PST_FLAG_CONCURRENT_PHASES = 2 /* run the two phases at once on disjoint SMs (fork/join over an
+                                    internal stream) instead of back to back */
 };
 
 typedef struct {
@@ -181,12 +182,13 @@ pst_status pst_export_tables(const pst_pool* pool, int32_t* shared_rows, int64_t
 /* Pool statistics (Knowl 4 quantities: sharing, fragmentation). */
 pst_status pst_stats(const pst_pool* pool, pst_stats_t* out);
 
-/* Record CUDA events around each decode kernel (phase 1, phase 2, merge). */
+/* Record CUDA events around each decode kernel and around the whole call. */
 pst_status pst_set_profiling(pst_pool* pool, int enable);
 
-/* Durations in ms of the last profiled decode's kernels: ms[0] chunk-first,
- * ms[1] sequence-first, ms[2] merge (0 when the kernel did not run).  Waits
- * for those events. */
+/* Durations in ms of the last profiled decode: ms[0] chunk-first kernel,
+ * ms[1] sequence-first kernel (0 when a kernel did not run), ms[2] the whole
+ * call from its first to its last kernel (the online-softmax merge runs inside
+ * both kernels).  Waits for those events. */
 pst_status pst_phase_times(pst_pool* pool, float* ms3);
 
 /* Kernel launches issued by the last pst_decode_attention call. */

@@ -1,0 +1,135 @@
+// K/V scatter into the chunk pool (and gather back out), plus the dtype
+// dispatch of the CUDA-core attention kernel.  The pool stores each (chunk, KV
+// head) as a K block and a transposed V block in the core-matrix layout of
+// pst_internal.h; the scatter builds that layout from user rows [n][Hkv][D]
+// (ChunkAttention, Knowl 1: K and V slices of h x c x d per chunk), see tile_off.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <type_traits>
+
+#include "attn_simt.cuh"
+
+namespace pst {
+
+namespace {
+
+// ---------------------------------------------------------------------------
+// Scatter user rows [rows][Hkv][D] into pool tiles (K rows and V^T columns).
+// grid = (ops, Hkv).
+// ---------------------------------------------------------------------------
+template <int ES>
+__global__ void __launch_bounds__(256) scatter_kernel(const ScatterParams p, int D, int C) {
+  constexpr int VEC = 16 / ES;
+  const ScatterOp op = p.ops[blockIdx.x];
+  const int kv = blockIdx.y;
+  const int DCH = D / VEC;
+  const size_t half = static_cast<size_t>(C) * D * ES;
+  uint8_t* tile = p.pool + (static_cast<size_t>(op.chunk) * p.Hkv + kv) * 2 * half;
+  const int rend = op.zero_tail ? C : op.r1;
+  const size_t src_row_bytes = static_cast<size_t>(p.Hkv) * D * ES;
+  // K: whole 16-byte chunks of rows [r0, rend)
+  for (int idx = threadIdx.x; idx < (rend - op.r0) * DCH; idx += blockDim.x) {
+    const int r = op.r0 + idx / DCH, j = idx % DCH;
+    uint4 val = make_uint4(0, 0, 0, 0);
+    if (r < op.r1) {
+      val = *reinterpret_cast<const uint4*>(p.k + static_cast<size_t>(op.src_row + r - op.r0) * src_row_bytes +
+                                            static_cast<size_t>(kv) * D * ES + j * 16);
+    }
+    *reinterpret_cast<uint4*>(tile + tile_off(r, j, D * ES, C)) = val;
+  }
+  // V^T: the 16-byte chunks holding keys [r0, rend), patched element by element
+  const int jb = op.r0 / VEC, je = (rend + VEC - 1) / VEC, nj = je - jb;
+  for (int idx = threadIdx.x; idx < D * nj; idx += blockDim.x) {
+    const int dr = idx / nj, j = jb + idx % nj;
+    uint4* dst = reinterpret_cast<uint4*>(tile + half + tile_off(dr, j, C * ES, D));
+    union {
+      uint4 v;
+      uint8_t b[16];
+    } cur;
+    cur.v = *dst;
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) {
+      const int key = j * VEC + e;
+      if (key >= op.r0 && key < op.r1) {
+        const uint8_t* s = p.v + static_cast<size_t>(op.src_row + key - op.r0) * src_row_bytes +
+                           (static_cast<size_t>(kv) * D + dr) * ES;
+#pragma unroll
+        for (int b = 0; b < ES; ++b) cur.b[e * ES + b] = s[b];
+      } else if (key >= op.r1 && op.zero_tail) {
+#pragma unroll
+        for (int b = 0; b < ES; ++b) cur.b[e * ES + b] = 0;
+      }
+    }
+    *dst = cur.v;
+  }
+  if (kv == 0 && threadIdx.x == 0) p.chunk_len[op.chunk] = op.r1;
+}
+
+// Gather pool rows [r0, r1) of each op back to user layout (p.k / p.v are
+// the destinations).
+template <int ES>
+__global__ void __launch_bounds__(256) gather_kernel(const ScatterParams p, int D, int C) {
+  constexpr int VEC = 16 / ES;
+  const ScatterOp op = p.ops[blockIdx.x];
+  const int kv = blockIdx.y;
+  const int DCH = D / VEC;
+  const size_t half = static_cast<size_t>(C) * D * ES;
+  const uint8_t* tile = p.pool + (static_cast<size_t>(op.chunk) * p.Hkv + kv) * 2 * half;
+  const size_t row_bytes = static_cast<size_t>(p.Hkv) * D * ES;
+  uint8_t* kd = const_cast<uint8_t*>(p.k);
+  uint8_t* vd = const_cast<uint8_t*>(p.v);
+  for (int idx = threadIdx.x; idx < (op.r1 - op.r0) * DCH; idx += blockDim.x) {
+    const int r = op.r0 + idx / DCH, j = idx % DCH;
+    *reinterpret_cast<uint4*>(kd + static_cast<size_t>(op.src_row + r - op.r0) * row_bytes +
+                              static_cast<size_t>(kv) * D * ES + j * 16) =
+        *reinterpret_cast<const uint4*>(tile + tile_off(r, j, D * ES, C));
+  }
+  for (int idx = threadIdx.x; idx < (op.r1 - op.r0) * D; idx += blockDim.x) {
+    const int r = op.r0 + idx / D, dr = idx % D;
+    const uint8_t* s = tile + half + tile_off(dr, r / VEC, C * ES, D) + (r % VEC) * ES;
+    uint8_t* d = vd + static_cast<size_t>(op.src_row + r - op.r0) * row_bytes + (static_cast<size_t>(kv) * D + dr) * ES;
+#pragma unroll
+    for (int b = 0; b < ES; ++b) d[b] = s[b];
+  }
+}
+
+}  // namespace
+
+bool simt_supported(int dtype, int D, int g) {
+  return (dtype == kF16 || dtype == kBF16 || dtype == kF32) && (D == 64 || D == 128) &&
+         (g == 1 || g == 2 || g == 4 || g == 8);
+}
+
+size_t attn_simt_smem(int dtype, int D, int C, int g, int stages, int warps_per_cta) {
+  return simt_warp_bytes(C, D, g, stages, dtype_size(dtype)) * warps_per_cta;
+}
+
+cudaError_t launch_attn_simt(int dtype, int D, int C, int g, const AttnParams& p, int grid, cudaStream_t s) {
+  switch (dtype) {
+    case kF16: return launch_attn_simt_f16(D, C, g, p, grid, s);
+    case kBF16: return launch_attn_simt_bf16(D, C, g, p, grid, s);
+    case kF32: return launch_attn_simt_f32(D, C, g, p, grid, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_scatter(int dtype, int D, int C, const ScatterParams& p, cudaStream_t s) {
+  if (p.n_ops <= 0) return cudaSuccess;
+  dim3 grid(p.n_ops, p.Hkv);
+  if (dtype_size(dtype) == 2) scatter_kernel<2><<<grid, 256, 0, s>>>(p, D, C);
+  else scatter_kernel<4><<<grid, 256, 0, s>>>(p, D, C);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather(int dtype, int D, int C, const ScatterParams& p, cudaStream_t s) {
+  if (p.n_ops <= 0) return cudaSuccess;
+  dim3 grid(p.n_ops, p.Hkv);
+  if (dtype_size(dtype) == 2) gather_kernel<2><<<grid, 256, 0, s>>>(p, D, C);
+  else gather_kernel<4><<<grid, 256, 0, s>>>(p, D, C);
+  return cudaGetLastError();
+}
+
+}  // namespace pst

@@ -8,19 +8,25 @@
 // causal key limit and a normalised output, runs a W-row chunked-prefill block
 // (Chunked Prefill, sections 1-2).
 //
-// One CTA handles one work item: up to 128 stacked query rows of one KV head
-// against a list of 64-token chunks.  Warp roles:
-//   warp 0      : producer -- one bulk async copy (TMA engine) per chunk moves
-//                 the 32 KB K + V^T tile image from the pool into a 4-stage
-//                 shared-memory ring; the pool already stores the tile in the
-//                 tensor cores' K-major core-matrix layout.
+// Persistent: each CTA walks its own list of work items (up to 128 stacked
+// query rows of one KV head against a list of 64-token chunks); TMEM and the
+// mbarriers are set up once and the pipelines run across item boundaries.
+// Warp roles:
+//   warp 0      : producer.  Lane 0 moves each chunk's 32 KB K + V^T tile image
+//                 from the pool into a 4-stage shared-memory ring with one bulk
+//                 async copy (TMA engine); the pool already stores tiles in the
+//                 tensor cores' 128-byte-swizzled K-major layout, and Q and P
+//                 are written in the same layout.
+//   warp 6      : gathers the next item's query rows into the other half of a
+//                 double-buffered Q tile while the current item computes.
 //   warp 1      : allocates TMEM; lane 0 issues tcgen05.mma:
 //                 S = Q K^T (M=128, N=64, K=D) and O_k = P V (M=128, N=D, K=64),
 //                 both double-buffered in TMEM, and commits to mbarriers.
 //   warps 2..5  : one thread per query row: read S from TMEM, online softmax in
 //                 log2 units, write the rounded probabilities P to shared
-//                 memory as the A operand of the PV product, and fold each
-//                 chunk's O_k into fp32 registers (o = o * alpha + O_k).
+//                 memory as the A operand of the PV product, fold each chunk's
+//                 O_k into fp32 registers (o = o * alpha + O_k), then write the
+//                 item's partial rows and merge completed rows (attn_common.cuh).
 // Every wait is bounded; on a timeout the CTA records an error, drains its
 // copies and MMAs, frees TMEM and exits.
 #include <cuda_bf16.h>
@@ -31,22 +37,22 @@
 #include <cmath>
 #include <type_traits>
 
+#include "attn_common.cuh"
 #include "ptx.cuh"
-#include "pst_internal.h"
 
 namespace pst {
 
 namespace {
 
 constexpr int kC = 64;     // tokens per chunk
-constexpr int kBM = 128;   // stacked query rows per CTA
+constexpr int kBM = 128;   // stacked query rows per item
 constexpr int kNS = 4;     // K/V tile stages
 
 __host__ __device__ constexpr uint32_t tc_tile_bytes(int D) { return 2u * kC * D * 2u; }
 __host__ __device__ constexpr uint32_t tc_q_bytes(int D) { return kBM * D * 2u; }
 __host__ __device__ constexpr uint32_t tc_p_bytes() { return kBM * kC * 2u; }
 __host__ __device__ constexpr size_t tc_smem_bytes(int D) {
-  return 1024 + tc_q_bytes(D) + kNS * tc_tile_bytes(D) + 2 * tc_p_bytes() + 256;
+  return 1024 + 2 * tc_q_bytes(D) + kNS * tc_tile_bytes(D) + 2 * tc_p_bytes() + 256;
 }
 
 template <typename T>
@@ -76,7 +82,7 @@ __device__ __forceinline__ uint32_t pack2_plain(float a, float b) {
 }
 
 template <typename T, int D>
-__global__ void __launch_bounds__(192, 1) attn_tc_kernel(const AttnParams p) {
+__global__ void __launch_bounds__(224, 1) attn_tc_kernel(const AttnParams p) {
   constexpr uint32_t HALF = kC * D * 2;
   constexpr uint32_t TILE = tc_tile_bytes(D);
   constexpr uint32_t QB = tc_q_bytes(D);
@@ -92,14 +98,15 @@ __global__ void __launch_bounds__(192, 1) attn_tc_kernel(const AttnParams p) {
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* qs = smem;
-  uint8_t* kvs = qs + QB;
-  uint8_t* ps = kvs + kNS * TILE;
+  uint8_t* qs = smem;                 // [2] Q tiles
+  uint8_t* kvs = qs + 2 * QB;         // [kNS] K + V^T tiles
+  uint8_t* ps = kvs + kNS * TILE;     // [2] P tiles
   uint64_t* bars = reinterpret_cast<uint64_t*>(ps + 2 * PB);
   uint64_t* full = bars;             // [kNS] tile landed
   uint64_t* empty = bars + kNS;      // [kNS] tile no longer read by the tensor cores
-  uint64_t* qfull = bars + 2 * kNS;  // Q tile written (128 arrivals)
-  uint64_t* sfull = qfull + 1;       // [2] S ready in TMEM
+  uint64_t* qfull = bars + 2 * kNS;  // [2] Q tile written (32 Q-loader lanes)
+  uint64_t* qfree = qfull + 2;       // [2] Q tile no longer read by the tensor cores
+  uint64_t* sfull = qfree + 2;       // [2] S ready in TMEM
   uint64_t* sfree = sfull + 2;       // [2] S read by the softmax threads (128)
   uint64_t* pfull = sfree + 2;       // [2] P written (128)
   uint64_t* ofull = pfull + 2;       // [2] O_k ready in TMEM
@@ -110,18 +117,20 @@ __global__ void __launch_bounds__(192, 1) attn_tc_kernel(const AttnParams p) {
   volatile int* issued_slot = abort_flag + 1;
   volatile int* consumed_slot = abort_flag + 2;
 
+  ptx::pdl_launch_dependents();  // the sequence-first kernel does not read our results
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const WorkItem w = p.items[blockIdx.x];
-  const int nk = w.n_chunks;
+  const int i0 = p.warp_items[blockIdx.x];
+  const int i1 = p.warp_items[blockIdx.x + 1];
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kNS; ++s) {
       ptx::mbar_init(&full[s], 1);
       ptx::mbar_init(&empty[s], 1);
     }
-    ptx::mbar_init(qfull, 128);
     for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(&qfull[b], 32);
+      ptx::mbar_init(&qfree[b], 1);
       ptx::mbar_init(&sfull[b], 1);
       ptx::mbar_init(&sfree[b], 128);
       ptx::mbar_init(&pfull[b], 128);
@@ -139,20 +148,66 @@ __global__ void __launch_bounds__(192, 1) attn_tc_kernel(const AttnParams p) {
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tbase = *tmem_slot;
+  const T* qbase = static_cast<const T*>(p.q);
 
   if (warp == 0) {
-    // ------------------------------------------------------------ producer
+    // ------------------------------------------------------- tile producer
     if (lane == 0) {
       const uint64_t pol = ptx::policy_evict_last();
-      for (int k = 0; k < nk; ++k) {
-        const int s = k % kNS;
-        if (k >= kNS && !ptx::mbar_wait(&empty[s], ((k / kNS) - 1) & 1, abort_flag, p.err)) break;
-        const int chunk = p.chunks[w.chunk_off + k];
-        const uint8_t* src = p.pool + (static_cast<size_t>(chunk) * p.Hkv + w.kv) * TILE;
-        ptx::mbar_arrive_expect_tx(&full[s], TILE);
-        ptx::bulk_g2s_hint(kvs + s * TILE, src, TILE, &full[s], pol);
-        *issued_slot = k + 1;
+      int t = 0;
+      bool ok = true;
+      for (int ii = i0; ii < i1 && ok; ++ii) {
+        const WorkItem w = p.items[ii];
+        for (int c = 0; c < w.n_chunks; ++c, ++t) {
+          const int s = t % kNS;
+          if (t >= kNS && !ptx::mbar_wait(&empty[s], ((t / kNS) - 1) & 1, abort_flag, p.err)) {
+            ok = false;
+            break;
+          }
+          const int chunk = p.chunks[w.chunk_off + c];
+          const uint8_t* src = p.pool + (static_cast<size_t>(chunk) * p.Hkv + w.kv) * TILE;
+          ptx::mbar_arrive_expect_tx(&full[s], TILE);
+          ptx::bulk_g2s_hint(kvs + s * TILE, src, TILE, &full[s], pol);
+          *issued_slot = t + 1;
+        }
       }
+    }
+  } else if (warp == 6) {
+    // ---------------------------------------------------------- Q loader
+    // Gathers each item's 128 query rows (zero past n_rows) into one half of
+    // the double-buffered Q tile, one item ahead of the tensor cores.
+    for (int ii = i0; ii < i1; ++ii) {
+      const int it = ii - i0, qb = it & 1;
+      bool ok = true;
+      if (it >= 2) ok = ptx::mbar_wait(&qfree[qb], ((it - 2) >> 1) & 1, abort_flag, p.err);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      const WorkItem w = p.items[ii];
+      uint8_t* dst = qs + qb * QB;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint4 v[2][DCH];
+#pragma unroll
+        for (int r2 = 0; r2 < 2; ++r2) {
+          const int r = lane + 32 * (2 * half + r2);
+          if (r < w.n_rows) {
+            const int rr = w.row0 + r;
+            const T* src = qbase + (static_cast<size_t>(w.group0 + rr / p.g) * p.Hq + w.kv * p.g + rr % p.g) * D;
+#pragma unroll
+            for (int j = 0; j < DCH; ++j) v[r2][j] = *reinterpret_cast<const uint4*>(src + 8 * j);
+          } else {
+#pragma unroll
+            for (int j = 0; j < DCH; ++j) v[r2][j] = make_uint4(0, 0, 0, 0);
+          }
+        }
+#pragma unroll
+        for (int r2 = 0; r2 < 2; ++r2) {
+          const int r = lane + 32 * (2 * half + r2);
+#pragma unroll
+          for (int j = 0; j < DCH; ++j) *reinterpret_cast<uint4*>(dst + tile_off(r, j, D * 2, kBM)) = v[r2][j];
+        }
+      }
+      ptx::fence_proxy_async_smem();
+      ptx::mbar_arrive(&qfull[qb]);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -160,179 +215,216 @@ __global__ void __launch_bounds__(192, 1) attn_tc_kernel(const AttnParams p) {
       const uint32_t q_addr = ptx::smem_u32(qs);
       const uint32_t kv_addr = ptx::smem_u32(kvs);
       const uint32_t p_addr = ptx::smem_u32(ps);
-      auto issue_s = [&](int k) -> bool {
-        const int s = k % kNS, b = k & 1;
-        if (!ptx::mbar_wait(&full[s], (k / kNS) & 1, abort_flag, p.err)) return false;
-        *consumed_slot = k + 1;
-        if (k >= 2 && !ptx::mbar_wait(&sfree[b], ((k - 2) >> 1) & 1, abort_flag, p.err)) return false;
+      auto issue_s = [&](int t, int qb) -> bool {
+        const int s = t % kNS, b = t & 1;
+        if (!ptx::mbar_wait(&full[s], (t / kNS) & 1, abort_flag, p.err)) return false;
+        *consumed_slot = t + 1;
+        if (t >= 2 && !ptx::mbar_wait(&sfree[b], ((t - 2) >> 1) & 1, abort_flag, p.err)) return false;
         ptx::tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint64_t a = ptx::smem_desc(q_addr + kk * 256, 128, DCH * 128);
-          const uint64_t bd = ptx::smem_desc(kv_addr + s * TILE + kk * 256, 128, DCH * 128);
+          // K step kk covers features [16kk, 16kk+16): column block kk/4, 32-byte offset (kk%4)
+          const uint32_t koff = (kk & 3) * 32;
+          const uint64_t a = ptx::smem_desc_sw128(q_addr + qb * QB + (kk >> 2) * (kBM * 128) + koff, 1024);
+          const uint64_t bd = ptx::smem_desc_sw128(kv_addr + s * TILE + (kk >> 2) * (kC * 128) + koff, 1024);
           ptx::mma_f16(tbase + S_COL + b * kC, a, bd, ID_S, kk > 0 ? 1u : 0u);
         }
         ptx::mma_commit(&sfull[b]);
         return true;
       };
-      auto issue_pv = [&](int k) -> bool {
-        const int s = k % kNS, b = k & 1;
-        if (!ptx::mbar_wait(&pfull[b], (k >> 1) & 1, abort_flag, p.err)) return false;
-        if (k >= 2 && !ptx::mbar_wait(&ofree[b], ((k - 2) >> 1) & 1, abort_flag, p.err)) return false;
+      auto issue_pv = [&](int t) -> bool {
+        const int s = t % kNS, b = t & 1;
+        if (!ptx::mbar_wait(&pfull[b], (t >> 1) & 1, abort_flag, p.err)) return false;
+        if (t >= 2 && !ptx::mbar_wait(&ofree[b], ((t - 2) >> 1) & 1, abort_flag, p.err)) return false;
         ptx::tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < kC / 16; ++kk) {
-          const uint64_t a = ptx::smem_desc(p_addr + b * PB + kk * 256, 128, CCH * 128);
-          const uint64_t bd = ptx::smem_desc(kv_addr + s * TILE + HALF + kk * 256, 128, CCH * 128);
+          const uint64_t a = ptx::smem_desc_sw128(p_addr + b * PB + kk * 32, 1024);
+          const uint64_t bd = ptx::smem_desc_sw128(kv_addr + s * TILE + HALF + kk * 32, 1024);
           ptx::mma_f16(tbase + O_COL + b * D, a, bd, ID_O, kk > 0 ? 1u : 0u);
         }
         ptx::mma_commit(&ofull[b]);
         ptx::mma_commit(&empty[s]);
         return true;
       };
-      bool ok = ptx::mbar_wait(qfull, 0, abort_flag, p.err);
-      if (ok) {
+      int t = 0;
+      bool ok = true;
+      for (int ii = i0; ii < i1 && ok; ++ii) {
+        const int it = ii - i0, qb = it & 1;
+        const int nk = p.items[ii].n_chunks;
+        ok = ptx::mbar_wait(&qfull[qb], (it >> 1) & 1, abort_flag, p.err);
+        if (!ok) break;
         ptx::tc_fence_after();
-        ok = issue_s(0);
-      }
-      for (int k = 0; k < nk && ok; ++k) {
-        if (k + 1 < nk) ok = issue_s(k + 1);
-        if (ok) ok = issue_pv(k);
+        ok = issue_s(t, qb);
+        for (int c = 0; c < nk && ok; ++c, ++t) {
+          if (c + 1 < nk) {
+            ok = issue_s(t + 1, qb);
+          } else {
+            ptx::mma_commit(&qfree[qb]);  // every S of this item is issued
+          }
+          if (ok) ok = issue_pv(t);
+        }
       }
       // Every MMA of this CTA must have finished before TMEM is released.
       ptx::mma_commit(done);
       ptx::mbar_wait(done, 0, nullptr, p.err);
     }
     __syncwarp();
-  } else {
+  } else if (warp >= 2 && warp <= 5) {
     // ------------------------------------------------- softmax / epilogue
     const int quad = warp & 3;
     const int r = quad * 32 + lane;
-    const bool row_valid = r < w.n_rows;
-    int grp = 0, hg = 0;
-    if (row_valid) {
-      const int rr = w.row0 + r;
-      grp = w.group0 + rr / p.g;
-      hg = rr % p.g;
-    }
-    const T* qrow = static_cast<const T*>(p.q) + (static_cast<size_t>(grp) * p.Hq + w.kv * p.g + hg) * D;
-#pragma unroll
-    for (int j = 0; j < DCH; ++j) {
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (row_valid) v = *reinterpret_cast<const uint4*>(qrow + j * 8);
-      *reinterpret_cast<uint4*>(qs + cm_off(r, j, DCH)) = v;
-    }
-    ptx::fence_proxy_async_smem();
-    ptx::mbar_arrive(qfull);
-
-    const int key_limit = (p.causal_p0 >= 0 && row_valid) ? p.causal_p0 + grp + 1 : INT_MAX;
     const uint32_t tl = tbase + (static_cast<uint32_t>(quad * 32) << 16);
-    float o[D];
-#pragma unroll
-    for (int i = 0; i < D; ++i) o[i] = 0.f;
-    float m = -INFINITY, l = 0.f, alpha_pend = 0.f;
+    int t = 0;
     bool ok = true;
-
-    for (int k = 0; k < nk; ++k) {
-      const int b = k & 1;
-      const int chunk = p.chunks[w.chunk_off + k];
-      const int lim = min(p.chunk_len[chunk], key_limit - k * kC);
-      if (!ptx::mbar_wait(&sfull[b], (k >> 1) & 1, abort_flag, p.err)) {
-        ok = false;
-        break;
+    for (int ii = i0; ii < i1 && ok; ++ii) {
+      const WorkItem w = p.items[ii];
+      const int nk = w.n_chunks;
+      const bool row_valid = r < w.n_rows;
+      int grp = 0, hg = 0;
+      if (row_valid) {
+        const int rr = w.row0 + r;
+        grp = w.group0 + rr / p.g;
+        hg = rr % p.g;
       }
-      ptx::tc_fence_after();
-      uint32_t sv0[32], sv1[32];
-      ptx::tmem_ld32(tl + S_COL + b * kC, sv0);
-      ptx::tmem_ld32(tl + S_COL + b * kC + 32, sv1);
-      ptx::tmem_ld_wait(sv0);
-      ptx::tmem_ld_wait(sv1);
-      ptx::tc_fence_before();
-      ptx::mbar_arrive(&sfree[b]);
-
-      float x[kC];
-      float mx = -INFINITY;
+      const int key_limit = (p.causal_p0 >= 0 && row_valid) ? p.causal_p0 + grp + 1 : INT_MAX;
+      float o[D];
 #pragma unroll
-      for (int t = 0; t < kC; ++t) {
-        const uint32_t raw = t < 32 ? sv0[t] : sv1[t - 32];
-        x[t] = (t < lim) ? __uint_as_float(raw) * p.scale_log2 : -INFINITY;
-        mx = fmaxf(mx, x[t]);
-      }
-      const float m_new = fmaxf(m, mx);
-      const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-      const float alpha = exp2f(m - m_use);
-      float psum = 0.f;
-      uint8_t* prow = ps + b * PB;
-#pragma unroll
-      for (int j = 0; j < CCH; ++j) {
-        uint4 pk;
-        pk.x = pack2<T>(exp2f(x[8 * j + 0] - m_use), exp2f(x[8 * j + 1] - m_use), psum);
-        pk.y = pack2<T>(exp2f(x[8 * j + 2] - m_use), exp2f(x[8 * j + 3] - m_use), psum);
-        pk.z = pack2<T>(exp2f(x[8 * j + 4] - m_use), exp2f(x[8 * j + 5] - m_use), psum);
-        pk.w = pack2<T>(exp2f(x[8 * j + 6] - m_use), exp2f(x[8 * j + 7] - m_use), psum);
-        *reinterpret_cast<uint4*>(prow + cm_off(r, j, CCH)) = pk;
-      }
-      ptx::fence_proxy_async_smem();
-      ptx::mbar_arrive(&pfull[b]);
-      l = l * alpha + psum;
+      for (int i = 0; i < D; ++i) o[i] = 0.f;
+      float m = -INFINITY, l = 0.f, alpha_pend = 0.f;
+      int my_len = 0;
 
-      if (k >= 1) {
-        const int b1 = (k - 1) & 1;
-        if (!ptx::mbar_wait(&ofull[b1], ((k - 1) >> 1) & 1, abort_flag, p.err)) {
+      for (int c = 0; c < nk; ++c, ++t) {
+        if ((c & 31) == 0) {  // valid tokens of chunks c .. c+31, one per lane
+          my_len = 0;
+          if (c + lane < nk) my_len = p.chunk_len[p.chunks[w.chunk_off + c + lane]];
+        }
+        const int lim = min(__shfl_sync(0xffffffffu, my_len, c & 31), key_limit - c * kC);
+        const int b = t & 1;
+        if (!ptx::mbar_wait(&sfull[b], (t >> 1) & 1, abort_flag, p.err)) {
           ok = false;
           break;
         }
         ptx::tc_fence_after();
-#pragma unroll
-        for (int cg = 0; cg < D / 32; ++cg) {
-          uint32_t ov[32];
-          ptx::tmem_ld32(tl + O_COL + b1 * D + 32 * cg, ov);
-          ptx::tmem_ld_wait(ov);
-#pragma unroll
-          for (int e = 0; e < 32; ++e) o[32 * cg + e] = fmaf(o[32 * cg + e], alpha_pend, __uint_as_float(ov[e]));
-        }
+        uint32_t sv0[32], sv1[32];
+        ptx::tmem_ld32(tl + S_COL + b * kC, sv0);
+        ptx::tmem_ld32(tl + S_COL + b * kC + 32, sv1);
+        ptx::tmem_ld_wait(sv0);
+        ptx::tmem_ld_wait(sv1);
         ptx::tc_fence_before();
-        ptx::mbar_arrive(&ofree[b1]);
-      }
-      alpha_pend = alpha;
-      m = m_new;
-    }
+        ptx::mbar_arrive(&sfree[b]);
 
-    if (ok && nk > 0) {
-      const int b1 = (nk - 1) & 1;
-      if (ptx::mbar_wait(&ofull[b1], ((nk - 1) >> 1) & 1, abort_flag, p.err)) {
-        ptx::tc_fence_after();
+        float x[kC];
+        float mx = -INFINITY;
 #pragma unroll
-        for (int cg = 0; cg < D / 32; ++cg) {
-          uint32_t ov[32];
-          ptx::tmem_ld32(tl + O_COL + b1 * D + 32 * cg, ov);
-          ptx::tmem_ld_wait(ov);
-#pragma unroll
-          for (int e = 0; e < 32; ++e) o[32 * cg + e] = fmaf(o[32 * cg + e], alpha_pend, __uint_as_float(ov[e]));
+        for (int k2 = 0; k2 < kC; ++k2) {
+          const uint32_t raw = k2 < 32 ? sv0[k2] : sv1[k2 - 32];
+          x[k2] = (k2 < lim) ? __uint_as_float(raw) * p.scale_log2 : -INFINITY;
+          mx = fmaxf(mx, x[k2]);
         }
-        ptx::tc_fence_before();
-        if (row_valid) {
-          if (p.final_mode) {
-            T* out = static_cast<T*>(p.out) + (static_cast<size_t>(grp) * p.Hq + w.kv * p.g + hg) * D;
-            const float inv = 1.f / l;
+        const float m_new = fmaxf(m, mx);
+        const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+        const float alpha = ptx::ex2(m - m_use);
+        float psum = 0.f;
+        uint8_t* prow = ps + b * PB;
 #pragma unroll
-            for (int j = 0; j < DCH; ++j) {
-              uint4 pk;
-              pk.x = pack2_plain<T>(o[8 * j + 0] * inv, o[8 * j + 1] * inv);
-              pk.y = pack2_plain<T>(o[8 * j + 2] * inv, o[8 * j + 3] * inv);
-              pk.z = pack2_plain<T>(o[8 * j + 4] * inv, o[8 * j + 5] * inv);
-              pk.w = pack2_plain<T>(o[8 * j + 6] * inv, o[8 * j + 7] * inv);
-              *reinterpret_cast<uint4*>(out + 8 * j) = pk;
-            }
-          } else {
-            const size_t prow_i = static_cast<size_t>(w.part_base) + r;
-            float4* po = reinterpret_cast<float4*>(p.part_o + prow_i * D);
+        for (int j = 0; j < CCH; ++j) {
+          uint4 pk;
+          pk.x = pack2<T>(ptx::ex2(x[8 * j + 0] - m_use), ptx::ex2(x[8 * j + 1] - m_use), psum);
+          pk.y = pack2<T>(ptx::ex2(x[8 * j + 2] - m_use), ptx::ex2(x[8 * j + 3] - m_use), psum);
+          pk.z = pack2<T>(ptx::ex2(x[8 * j + 4] - m_use), ptx::ex2(x[8 * j + 5] - m_use), psum);
+          pk.w = pack2<T>(ptx::ex2(x[8 * j + 6] - m_use), ptx::ex2(x[8 * j + 7] - m_use), psum);
+          *reinterpret_cast<uint4*>(prow + r * 128 + ((j ^ (r & 7)) << 4)) = pk;
+        }
+        ptx::fence_proxy_async_smem();
+        ptx::mbar_arrive(&pfull[b]);
+        l = l * alpha + psum;
+
+        if (c >= 1) {
+          const int b1 = (t - 1) & 1;
+          if (!ptx::mbar_wait(&ofull[b1], ((t - 1) >> 1) & 1, abort_flag, p.err)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
 #pragma unroll
-            for (int j = 0; j < D / 4; ++j) po[j] = make_float4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
-            p.part_ml[2 * prow_i] = m;
-            p.part_ml[2 * prow_i + 1] = l;
+          for (int cg = 0; cg < D / 32; ++cg) {
+            uint32_t ov[32];
+            ptx::tmem_ld32(tl + O_COL + b1 * D + 32 * cg, ov);
+            ptx::tmem_ld_wait(ov);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[32 * cg + e] = fmaf(o[32 * cg + e], alpha_pend, __uint_as_float(ov[e]));
+          }
+          ptx::tc_fence_before();
+          ptx::mbar_arrive(&ofree[b1]);
+        }
+        alpha_pend = alpha;
+        m = m_new;
+      }
+      if (!ok) break;
+
+      // last chunk's O of the item
+      {
+        const int b1 = (t - 1) & 1;
+        if (!ptx::mbar_wait(&ofull[b1], ((t - 1) >> 1) & 1, abort_flag, p.err)) ok = false;
+        if (ok) {
+          ptx::tc_fence_after();
+#pragma unroll
+          for (int cg = 0; cg < D / 32; ++cg) {
+            uint32_t ov[32];
+            ptx::tmem_ld32(tl + O_COL + b1 * D + 32 * cg, ov);
+            ptx::tmem_ld_wait(ov);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[32 * cg + e] = fmaf(o[32 * cg + e], alpha_pend, __uint_as_float(ov[e]));
+          }
+          ptx::tc_fence_before();
+          ptx::mbar_arrive(&ofree[b1]);
+        }
+      }
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+
+      if (row_valid) {
+        if (p.final_mode) {
+          T* out = static_cast<T*>(p.out) + (static_cast<size_t>(grp) * p.Hq + w.kv * p.g + hg) * D;
+          const float inv = 1.f / l;
+#pragma unroll
+          for (int j = 0; j < DCH; ++j) {
+            uint4 pk;
+            pk.x = pack2_plain<T>(o[8 * j + 0] * inv, o[8 * j + 1] * inv);
+            pk.y = pack2_plain<T>(o[8 * j + 2] * inv, o[8 * j + 3] * inv);
+            pk.z = pack2_plain<T>(o[8 * j + 4] * inv, o[8 * j + 5] * inv);
+            pk.w = pack2_plain<T>(o[8 * j + 6] * inv, o[8 * j + 7] * inv);
+            *reinterpret_cast<uint4*>(out + 8 * j) = pk;
+          }
+        } else {
+          const size_t prow_i = static_cast<size_t>(w.part_base) + r;
+          float4* po = reinterpret_cast<float4*>(p.part_o + prow_i * D);
+#pragma unroll
+          for (int j = 0; j < D / 4; ++j) po[j] = make_float4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
+          reinterpret_cast<float2*>(p.part_ml)[prow_i] = make_float2(m, l);
+        }
+      }
+      if (!p.final_mode) {
+        // One arrival per (batch row, KV head) group of g rows; g divides 32,
+        // so a group never straddles two warps.  The arrival that completes a
+        // pair merges it (attn_common.cuh).
+        __threadfence();
+        __syncwarp();
+        int last = 0;
+        if (row_valid && hg == 0) {
+          const int key = grp * p.Hkv + w.kv;
+          const int expected = __ldcg(p.m_off + key + 1) - __ldcg(p.m_off + key);
+          const int old = atomicAdd(p.m_cnt + key, 1);
+          last = (old + 1 == expected);
+          if (last) {
+            __threadfence();
+            p.m_cnt[key] = 0;
           }
         }
+        // every row of a completed group merges itself, all lanes in parallel
+        last = __shfl_sync(0xffffffffu, last, lane - hg);
+        if (last && row_valid) merge_row_thread<T, D>(p, grp, w.kv, hg);
       }
     }
   }
@@ -355,7 +447,7 @@ cudaError_t launch_tc_t(const AttnParams& p, int grid, cudaStream_t s) {
   auto fn = attn_tc_kernel<T, D>;
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  fn<<<grid, 192, smem, s>>>(p);
+  fn<<<grid, 224, smem, s>>>(p);
   return cudaGetLastError();
 }
 

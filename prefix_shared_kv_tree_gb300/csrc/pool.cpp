@@ -23,6 +23,7 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <string>
 #include <unordered_map>
@@ -108,9 +109,10 @@ struct pst_pool {
   double last_rebuild_us = 0;
   std::vector<int64_t> batch;  // live ids in batch order
   std::vector<int32_t> h_tab;
-  size_t off_chunks = 0, off_tc = 0, off_simt = 0, off_warp = 0, off_moff = 0, off_ment = 0;
-  int32_t n_tc_items = 0, n_simt_items = 0, n_simt_warps = 0;
-  int32_t simt_grid = 0, simt_stages = 3, simt_wpc = 4;
+  size_t off_chunks = 0, off_tc = 0, off_tc_cta = 0, off_simt = 0, off_warp = 0, off_moff = 0, off_ment = 0;
+  int32_t n_tc_items = 0, n_tc_ctas = 0, n_simt_items = 0, n_simt_warps = 0;
+  double tc_chunk_us = 0.5, simt_tile_us = 0.75;  // cost model for splitting SMs between the phases
+  int32_t simt_grid = 0, simt_stages = 3, simt_wpc = 8;
   int64_t n_part_rows = 0, shared_chunks = 0;
   std::vector<int32_t> canon_shared;   // 4 per row
   std::vector<int32_t> canon_entries;  // 2 per entry
@@ -126,6 +128,7 @@ struct pst_pool {
   float* d_part_ml = nullptr;
   size_t part_cap = 0;  // rows
   int32_t* d_err = nullptr;
+  int32_t* d_cnt = nullptr;  // merge arrival counters, max_seqs * Hkv
   int32_t* d_pre = nullptr;
   size_t pre_cap = 0;
   int32_t* h_stage = nullptr;  // pinned upload staging
@@ -356,8 +359,13 @@ pst_status rebuild(pst_pool* p) {
     const int32_t id0 = r.front();
     const int64_t rows = static_cast<int64_t>(nj[id0] - ni[id0]) * g;
     p1_iters += static_cast<int64_t>(r.size()) * Hkv * (p->use_tc ? ceil_div(rows, 128) : (nj[id0] - ni[id0]));
+    (void)rows;
   }
-  const int64_t split1 = std::min<int64_t>(32, std::max<int64_t>(4, (p1_iters + p->n_sm - 1) / std::max(1, p->n_sm)));
+  // chunk-first items: enough of them to cover every SM when the phases run
+  // back to back; fewer, longer ones when they share the GPU
+  const int64_t split1 = (p->cfg.flags & PST_FLAG_CONCURRENT_PHASES)
+                             ? 8
+                             : std::min<int64_t>(16, std::max<int64_t>(2, ceil_div(p1_iters, std::max(1, p->n_sm))));
   for (const auto& r : runs) {
     const int32_t i = ni[r.front()], j = nj[r.front()];
     const int32_t rows = (j - i) * g;
@@ -407,11 +415,56 @@ pst_status rebuild(pst_pool* p) {
     for (int kv = 0; kv < Hkv; ++kv) streams.push_back({off, n, kv, u});
   }
 
-  // ---- split the CUDA-core tile streams evenly over all warps of the grid
   int64_t T = 0;
   for (const auto& st : streams) T += st.n;
+
+  // ---- tensor-core items -> persistent CTAs.  When both phases run at once,
+  // each kernel's CTA fills an SM, so the GPU is split: k SMs for the
+  // chunk-first kernel, the rest for the sequence-first kernel, k chosen by a
+  // simple cost model so both finish together; items go to CTAs longest first.
+  std::vector<int32_t> tc_cta_off(1, 0);
+  p->n_tc_ctas = 0;
+  if (p->n_tc_items > 0) {
+    const int32_t n = p->n_tc_items;
+    const bool concurrent = T > 0 && (p->cfg.flags & PST_FLAG_CONCURRENT_PHASES);
+    std::vector<double> cost(n);
+    double w_tc = 0;
+    for (int32_t x = 0; x < n; ++x) {
+      cost[x] = tc_items[8 * x + 1] * p->tc_chunk_us + p->tc_chunk_us;  // + one chunk's worth per item
+      w_tc += cost[x];
+    }
+    int32_t k = std::min(p->n_sm, n);
+    if (concurrent && p->n_sm > 1) {
+      const double w_simt = static_cast<double>(T) * p->simt_tile_us;
+      k = static_cast<int32_t>(std::lround(p->n_sm * w_tc / (w_tc + w_simt)));
+      k = std::max(1, std::min({k, n, p->n_sm - 1}));
+    }
+    std::vector<int32_t> order(n);
+    for (int32_t x = 0; x < n; ++x) order[x] = x;
+    std::stable_sort(order.begin(), order.end(), [&](int32_t a, int32_t b) { return cost[a] > cost[b]; });
+    std::vector<double> load(k, 0.0);
+    std::vector<std::vector<int32_t>> per(k);
+    for (int32_t x : order) {
+      const int32_t c = static_cast<int32_t>(std::min_element(load.begin(), load.end()) - load.begin());
+      load[c] += cost[x];
+      per[c].push_back(x);
+    }
+    std::vector<int32_t> sorted;
+    sorted.reserve(tc_items.size());
+    for (int32_t c = 0; c < k; ++c) {
+      for (int32_t x : per[c]) sorted.insert(sorted.end(), tc_items.begin() + 8 * x, tc_items.begin() + 8 * x + 8);
+      tc_cta_off.push_back(static_cast<int32_t>(sorted.size() / 8));
+    }
+    tc_items.swap(sorted);
+    p->n_tc_ctas = k;
+  }
+
+  // ---- split the CUDA-core tile streams evenly over all warps of the grid
   const int64_t warps_needed = std::max<int64_t>(1, ceil_div(T, 2));
-  p->simt_grid = static_cast<int32_t>(std::min<int64_t>(p->n_sm, ceil_div(warps_needed, p->simt_wpc)));
+  const int32_t simt_sms = (p->n_tc_ctas > 0 && (p->cfg.flags & PST_FLAG_CONCURRENT_PHASES))
+                               ? std::max(1, p->n_sm - p->n_tc_ctas)
+                               : p->n_sm;
+  p->simt_grid = static_cast<int32_t>(std::min<int64_t>(simt_sms, ceil_div(warps_needed, p->simt_wpc)));
   p->n_simt_warps = p->simt_grid * p->simt_wpc;
   const int64_t W = p->n_simt_warps;
   warp_items.assign(W + 1, 0);
@@ -471,6 +524,8 @@ pst_status rebuild(pst_pool* p) {
   while (t.size() % 8) t.push_back(0);  // 32-byte alignment of the item arrays
   p->off_tc = t.size();
   t.insert(t.end(), tc_items.begin(), tc_items.end());
+  p->off_tc_cta = t.size();
+  t.insert(t.end(), tc_cta_off.begin(), tc_cta_off.end());
   p->off_simt = t.size();
   t.insert(t.end(), simt_items.begin(), simt_items.end());
   p->off_warp = t.size();
@@ -581,10 +636,12 @@ pst_status pst_pool_create(const pst_config* cfg, int device, pst_pool** out) {
   p->free_chunks.reserve(c.max_chunks);
   for (int64_t x = c.max_chunks - 1; x >= 0; --x) p->free_chunks.push_back(static_cast<int32_t>(x));
 
-  // CUDA-core kernel shape: 4 warps x 3 half-tile stages when it fits
-  p->simt_wpc = 4;
+  if (const char* e = std::getenv("PST_TC_CHUNK_US")) p->tc_chunk_us = std::atof(e);
+  if (const char* e = std::getenv("PST_SIMT_TILE_US")) p->simt_tile_us = std::atof(e);
+  // CUDA-core kernel shape: 8 warps x 3 piece stages when it fits
+  p->simt_wpc = 8;
   p->simt_stages = 3;
-  while (attn_simt_smem(c.dtype, p->D, p->C, g, p->simt_stages, p->simt_wpc) > 200 * 1024) {
+  while (attn_simt_smem(c.dtype, p->D, p->C, g, p->simt_stages, p->simt_wpc) > 220 * 1024) {
     if (p->simt_stages > 2) p->simt_stages--;
     else p->simt_wpc--;
   }
@@ -608,6 +665,9 @@ pst_status pst_pool_create(const pst_config* cfg, int device, pst_pool** out) {
     if ((e = cudaMemset(p->d_chunk_len, 0, sizeof(int32_t) * c.max_chunks)) != cudaSuccess) return bail(e, "cudaMemset");
     if ((e = cudaMalloc(&p->d_err, sizeof(int32_t))) != cudaSuccess) return bail(e, "cudaMalloc");
     if ((e = cudaMemset(p->d_err, 0, sizeof(int32_t))) != cudaSuccess) return bail(e, "cudaMemset");
+    const size_t ncnt = static_cast<size_t>(p->cfg.max_seqs) * c.n_kv_heads;
+    if ((e = cudaMalloc(&p->d_cnt, sizeof(int32_t) * ncnt)) != cudaSuccess) return bail(e, "cudaMalloc");
+    if ((e = cudaMemset(p->d_cnt, 0, sizeof(int32_t) * ncnt)) != cudaSuccess) return bail(e, "cudaMemset");
     if ((e = cudaStreamCreateWithFlags(&p->aux, cudaStreamNonBlocking)) != cudaSuccess) return bail(e, "stream");
     if ((e = cudaEventCreateWithFlags(&p->ev_fork, cudaEventDisableTiming)) != cudaSuccess) return bail(e, "event");
     if ((e = cudaEventCreateWithFlags(&p->ev_join, cudaEventDisableTiming)) != cudaSuccess) return bail(e, "event");
@@ -631,6 +691,7 @@ pst_status pst_pool_free(pst_pool* p) {
     cudaFree(p->d_part_o);
     cudaFree(p->d_part_ml);
     cudaFree(p->d_err);
+    cudaFree(p->d_cnt);
     cudaFree(p->d_pre);
     cudaFree(p->d_q);
     cudaFree(p->d_out);
@@ -781,19 +842,25 @@ pst_status pst_seq_length(const pst_pool* p, int64_t seq_id, int64_t* n_tokens) 
 static pst_status decode_impl(pst_pool* p, const void* q, void* out, cudaStream_t s) {
   pst_status st = ensure_tables(p);
   if (st != PST_OK) return st;
-  st = sync_device_tables(p, s);
-  if (st != PST_OK) return st;
   p->last_launches = 0;
   p->pran[0] = p->pran[1] = p->pran[2] = false;
   const int32_t B = static_cast<int32_t>(p->batch.size());
   if (B == 0) return PST_OK;
+  if (!q || !out) return fail(PST_ERR_INVALID, "null q/out with %d live sequences", B);
+  st = sync_device_tables(p, s);
+  if (st != PST_OK) return st;
   AttnParams a = base_params(p);
   a.q = q;
+  a.out = out;
   a.part_o = p->d_part_o;
   a.part_ml = p->d_part_ml;
   a.chunks = p->d_tab + p->off_chunks;
-  const bool fork = p->n_tc_items > 0 && p->n_simt_items > 0 && !(p->cfg.flags & PST_FLAG_SERIAL_PHASES);
+  a.m_off = p->d_tab + p->off_moff;
+  a.m_ent = p->d_tab + p->off_ment;
+  a.m_cnt = p->d_cnt;
+  const bool fork = p->n_tc_items > 0 && p->n_simt_items > 0 && (p->cfg.flags & PST_FLAG_CONCURRENT_PHASES);
   cudaStream_t s1 = fork ? p->aux : s;
+  if (p->profiling) CUDA_TRY(cudaEventRecord(p->pev[4], s));
   if (fork) {
     CUDA_TRY(cudaEventRecord(p->ev_fork, s));
     CUDA_TRY(cudaStreamWaitEvent(p->aux, p->ev_fork, 0));
@@ -802,8 +869,9 @@ static pst_status decode_impl(pst_pool* p, const void* q, void* out, cudaStream_
     AttnParams a1 = a;
     a1.items = reinterpret_cast<const WorkItem*>(p->d_tab + p->off_tc);
     a1.n_items = p->n_tc_items;
+    a1.warp_items = p->d_tab + p->off_tc_cta;
     if (p->profiling) CUDA_TRY(cudaEventRecord(p->pev[0], s1));
-    cudaError_t e = launch_attn_tc(p->cfg.dtype, p->D, a1, p->n_tc_items, s1);
+    cudaError_t e = launch_attn_tc(p->cfg.dtype, p->D, a1, p->n_tc_ctas, s1);
     if (e != cudaSuccess) return fail(PST_ERR_CUDA, "chunk-first launch: %s", cudaGetErrorString(e));
     if (p->profiling) CUDA_TRY(cudaEventRecord(p->pev[1], s1));
     p->pran[0] = true;
@@ -816,7 +884,8 @@ static pst_status decode_impl(pst_pool* p, const void* q, void* out, cudaStream_
     a2.warp_items = p->d_tab + p->off_warp;
     a2.n_warps = p->n_simt_warps;
     if (p->profiling) CUDA_TRY(cudaEventRecord(p->pev[2], s));
-    cudaError_t e = launch_attn_simt(p->cfg.dtype, p->D, p->g, a2, p->simt_grid, s);
+    a2.pdl = (p->n_tc_items > 0 && !fork) ? 1 : 0;
+    cudaError_t e = launch_attn_simt(p->cfg.dtype, p->D, p->C, p->g, a2, p->simt_grid, s);
     if (e != cudaSuccess) return fail(PST_ERR_CUDA, "sequence-first launch: %s", cudaGetErrorString(e));
     if (p->profiling) CUDA_TRY(cudaEventRecord(p->pev[3], s));
     p->pran[1] = true;
@@ -826,30 +895,16 @@ static pst_status decode_impl(pst_pool* p, const void* q, void* out, cudaStream_
     CUDA_TRY(cudaEventRecord(p->ev_join, p->aux));
     CUDA_TRY(cudaStreamWaitEvent(s, p->ev_join, 0));
   }
-  MergeParams mp{};
-  mp.off = p->d_tab + p->off_moff;
-  mp.ent = p->d_tab + p->off_ment;
-  mp.part_o = p->d_part_o;
-  mp.part_ml = p->d_part_ml;
-  mp.out = out;
-  mp.B = B;
-  mp.Hq = p->cfg.n_q_heads;
-  mp.Hkv = p->cfg.n_kv_heads;
-  mp.g = p->g;
-  mp.err = p->d_err;
-  if (p->profiling) CUDA_TRY(cudaEventRecord(p->pev[4], s));
-  cudaError_t e = launch_merge(p->cfg.dtype, p->D, mp, s);
-  if (e != cudaSuccess) return fail(PST_ERR_CUDA, "merge launch: %s", cudaGetErrorString(e));
-  if (p->profiling) CUDA_TRY(cudaEventRecord(p->pev[5], s));
-  p->pran[2] = true;
-  p->last_launches++;
+  if (p->profiling) {
+    CUDA_TRY(cudaEventRecord(p->pev[5], s));
+    p->pran[2] = true;
+  }
   return PST_OK;
 }
 
 pst_status pst_decode_attention(pst_pool* p, const void* q, void* out, void* stream) {
   pst_status st = need_device(p);
   if (st != PST_OK) return st;
-  if (!q || !out) return fail(PST_ERR_INVALID, "null q/out");
   return decode_impl(p, q, out, static_cast<cudaStream_t>(stream));
 }
 
@@ -964,8 +1019,8 @@ pst_status pst_prefill_attend(pst_pool* p, int64_t seq_id, const int32_t* tokens
   if (!p->use_tc) {
     n_warps = n_items;
     grid = static_cast<int32_t>(ceil_div(n_warps, p->simt_wpc));
-    for (int32_t x = 0; x <= n_warps; ++x) tab.push_back(x);
   }
+  for (int32_t x = 0; x <= n_items; ++x) tab.push_back(x);  // one item per warp (CUDA cores) or CTA (tensor cores)
   st = upload(p, &p->d_pre, &p->pre_cap, tab, s);
   if (st != PST_OK) return st;
 
@@ -978,12 +1033,13 @@ pst_status pst_prefill_attend(pst_pool* p, int64_t seq_id, const int32_t* tokens
   a.items = reinterpret_cast<const WorkItem*>(p->d_pre + off_items);
   a.n_items = n_items;
   cudaError_t e;
+  a.warp_items = p->d_pre + off_warp;
   if (p->use_tc) {
     e = launch_attn_tc(p->cfg.dtype, p->D, a, n_items, s);
   } else {
     a.warp_items = p->d_pre + off_warp;
     a.n_warps = n_warps;
-    e = launch_attn_simt(p->cfg.dtype, p->D, g, a, grid, s);
+    e = launch_attn_simt(p->cfg.dtype, p->D, p->C, g, a, grid, s);
   }
   if (e != cudaSuccess) return fail(PST_ERR_CUDA, "prefill launch: %s", cudaGetErrorString(e));
   return PST_OK;
@@ -1080,6 +1136,10 @@ pst_status pst_check_device(pst_pool* p, int32_t* code) {
   CUDA_TRY(cudaDeviceSynchronize());
   CUDA_TRY(cudaMemcpy(code, p->d_err, sizeof(int32_t), cudaMemcpyDeviceToHost));
   CUDA_TRY(cudaMemset(p->d_err, 0, sizeof(int32_t)));
+  if (*code) {
+    // a kernel gave up part-way: its merge counters may be stale
+    CUDA_TRY(cudaMemset(p->d_cnt, 0, sizeof(int32_t) * static_cast<size_t>(p->cfg.max_seqs) * p->cfg.n_kv_heads));
+  }
   if (*code) return fail(PST_ERR_DEVICE, "device error word 0x%x", *code);
   return PST_OK;
 }

@@ -13,18 +13,27 @@ inline int dtype_size(int dt) { return dt == kF32 ? 4 : 2; }
 
 // ---------------------------------------------------------------------------
 // Pool layout.  The slab holds, per (chunk, KV head), one contiguous tile of
-// 2 * C * D elements: first the K block (C key rows x D), then the transposed
-// V block (D rows x C keys).  Both blocks are stored as 8-row x 16-byte "core
-// matrices", row-group major:
-//   byte(r, j) = ((r / 8) * (row_bytes / 16) + j) * 128 + (r % 8) * 16
-// where r is the row (key for K, feature for V^T) and j the 16-byte column
-// chunk.  This is the K-major, no-swizzle operand image the tcgen05 tensor
-// cores read from shared memory, so one bulk copy stages a tile ready for MMA,
-// and it gives conflict-free 16-byte shared-memory reads to the CUDA-core
-// kernel as well.
+// 2 * C * D elements: first the K block (C key rows of D elements), then the
+// transposed V block (D feature rows of C keys).  A block whose rows are a
+// multiple of 128 bytes is stored as 128-byte column blocks one after another,
+// each [rows][128 B], with the eight 16-byte chunks of row r permuted by XOR
+// with (r mod 8).  That is the 128-byte-swizzled K-major operand image the
+// tcgen05 tensor cores read from shared memory (so one bulk copy stages a
+// tile ready for MMA), and it gives conflict-free 16-byte shared-memory reads
+// to the CUDA-core kernel.  64-byte rows (16-bit V^T with c = 32) use plain
+// 8-row x 16-byte core matrices.
 // ---------------------------------------------------------------------------
 __host__ __device__ inline uint32_t cm_off(uint32_t r, uint32_t j, uint32_t chunks_per_row) {
   return ((r >> 3) * chunks_per_row + j) * 128u + (r & 7u) * 16u;
+}
+
+// Byte offset of 16-byte chunk j of row r in a block of `rows` rows of
+// `row_bytes` bytes.
+__host__ __device__ inline uint32_t tile_off(uint32_t r, uint32_t j, uint32_t row_bytes, uint32_t rows) {
+  if ((row_bytes & 127u) == 0) {
+    return (j >> 3) * rows * 128u + r * 128u + (((j & 7u) ^ (r & 7u)) << 4);
+  }
+  return cm_off(r, j, row_bytes >> 4);
 }
 
 // One unit of partial-attention work: a list of chunks of one KV head against
@@ -60,9 +69,17 @@ struct AttnParams {
   int32_t final_mode;         // 0: write (o, m, n) partials; 1: write o / n to out
   int32_t causal_p0;          // >= 0: group t sees keys [0, causal_p0 + t]; < 0: no causal limit
   float scale_log2;           // log2(e) / sqrt(D), computed on the host
-  int32_t stages;             // CUDA-core kernel: half-tile stages per warp
+  int32_t stages;             // CUDA-core kernel: piece stages per warp
   int32_t warps_per_cta;      // CUDA-core kernel
   int32_t* err;               // device error word
+  // fused merge (partial mode): CSR of partial rows per (batch row, KV head),
+  // and one arrival counter per pair (zero between calls)
+  const int32_t* m_off;       // [B * Hkv + 1]
+  const int32_t* m_ent;       // partial row of head kv*g + 0 for each entry
+  int32_t* m_cnt;             // [B * Hkv]
+  // 1: launched as a programmatic dependent of the previous kernel on the
+  // stream (it may start while that kernel drains; it must not finish first)
+  int32_t pdl;
 };
 
 struct MergeParams {
@@ -102,8 +119,12 @@ enum : int32_t {
 // Launchers (defined in the .cu files).  All return the launch status.
 cudaError_t launch_scatter(int dtype, int D, int C, const ScatterParams& p, cudaStream_t s);
 cudaError_t launch_gather(int dtype, int D, int C, const ScatterParams& p, cudaStream_t s);
-cudaError_t launch_attn_simt(int dtype, int D, int g, const AttnParams& p, int grid, cudaStream_t s);
+cudaError_t launch_attn_simt(int dtype, int D, int C, int g, const AttnParams& p, int grid, cudaStream_t s);
 size_t attn_simt_smem(int dtype, int D, int C, int g, int stages, int warps_per_cta);
+// per-dtype launchers (one translation unit each)
+cudaError_t launch_attn_simt_f16(int D, int C, int g, const AttnParams& p, int grid, cudaStream_t s);
+cudaError_t launch_attn_simt_bf16(int D, int C, int g, const AttnParams& p, int grid, cudaStream_t s);
+cudaError_t launch_attn_simt_f32(int D, int C, int g, const AttnParams& p, int grid, cudaStream_t s);
 cudaError_t launch_attn_tc(int dtype, int D, const AttnParams& p, int grid, cudaStream_t s);
 size_t attn_tc_smem(int D);
 cudaError_t launch_merge(int dtype, int D, const MergeParams& p, cudaStream_t s);

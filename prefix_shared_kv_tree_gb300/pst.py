@@ -15,14 +15,14 @@ from ctypes import POINTER, Structure, byref, c_char_p, c_double, c_float, c_int
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libpst.so")
+LIB_PATH = os.environ.get("PST_LIBRARY") or os.path.join(_HERE, "libpst.so")
 
 PST_OK, PST_ERR_INVALID, PST_ERR_OOM, PST_ERR_NOT_FOUND, PST_ERR_CUDA, PST_ERR_STATE, PST_ERR_DEVICE = range(7)
 STATUS_NAMES = {0: "OK", 1: "INVALID", 2: "OOM", 3: "NOT_FOUND", 4: "CUDA", 5: "STATE", 6: "DEVICE"}
 PST_F16, PST_BF16, PST_F32 = 0, 1, 2
 DTYPE_CODES = {"f16": PST_F16, "bf16": PST_BF16, "f32": PST_F32}
 PST_FLAG_NO_TENSOR_CORES = 1
-PST_FLAG_SERIAL_PHASES = 2
+PST_FLAG_CONCURRENT_PHASES = 2
 MIN_SHARE_NEVER = 2**31 - 1
 
 
