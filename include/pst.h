@@ -151,6 +151,28 @@ pst_status pst_decode_attention(pst_pool* pool, const void* q, void* out, void* 
  * copies inside the CUDA runtime). */
 pst_status pst_decode_attention_host(pst_pool* pool, const void* q_host, void* out_host, void* stream);
 
+/* Decode attention that allocates nothing.  No counterpart in the paper: it
+ * exists for callers that cannot allocate device memory at call time -- for
+ * example a serving runtime that hands all GPU memory to its own allocator up
+ * front, or a latency-critical loop where cudaMalloc / cudaFree would
+ * synchronise the device.  Same inputs, outputs and result as
+ * pst_decode_attention, but the partial rows and merge counters live in a
+ * fixed 32 MiB device area that the library defines at file scope: every GPU
+ * that loads the library holds that area until the process exits.
+ *   - The first call on a device looks up the area's device address (once per
+ *     device); make that first call before any stream capture.
+ *   - Needs the chunk tables already on the device: after a structural change
+ *     (insert, remove, a new chunk on append) call pst_decode_attention once
+ *     first; otherwise returns PST_ERR_STATE.  It never rebuilds or uploads.
+ *   - A batch needing more than 32 MiB of scratch (about
+ *     B*Hkv*4 + partial_rows*(d+2)*4 bytes, see pst_stats) returns
+ *     PST_ERR_INVALID.
+ *   - All calls share the one area (it keeps the last call's contents; the
+ *     call clears its merge counters itself): calls whose GPU work overlaps --
+ *     on different streams or from different pools -- race with each other.
+ * Calls no cudaMalloc, cudaFree or other allocating routine. */
+pst_status pst_decode_attention_noalloc(pst_pool* pool, const void* q, void* out, void* stream);
+
 /* Chunked-prefill attend (Chunked Prefill, sections 1-2): append W tokens
  * (host tokens int32[W], device k_new/v_new [W][Hkv][d]) to sequence seq_id at
  * positions [p0, p0+W), p0 = its current length, then out[t][h] =

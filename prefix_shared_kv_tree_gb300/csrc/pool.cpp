@@ -908,6 +908,65 @@ pst_status pst_decode_attention(pst_pool* p, const void* q, void* out, void* str
   return decode_impl(p, q, out, static_cast<cudaStream_t>(stream));
 }
 
+// Decode attention without any allocation: the partial rows and the merge
+// counters go to the library's fixed device scratch instead of the pool's own
+// buffers.  Only launches kernels and one memset on `stream`.
+pst_status pst_decode_attention_noalloc(pst_pool* p, const void* q, void* out, void* stream) {
+  pst_status st = need_device(p);
+  if (st != PST_OK) return st;
+  if (p->dirty || !p->tab_uploaded)
+    return fail(PST_ERR_STATE,
+                "the chunk tables changed since the last pst_decode_attention; call it once first "
+                "(that call may allocate) before using the allocation-free variant");
+  const int32_t B = static_cast<int32_t>(p->batch.size());
+  if (B == 0) return PST_OK;
+  if (!q || !out) return fail(PST_ERR_INVALID, "null q/out with %d live sequences", B);
+  const int Hkv = p->cfg.n_kv_heads;
+  auto align256 = [](size_t x) { return (x + 255) / 256 * 256; };
+  const size_t cnt_bytes = align256(static_cast<size_t>(B) * Hkv * sizeof(int32_t));
+  const size_t ml_bytes = align256(static_cast<size_t>(p->n_part_rows) * 2 * sizeof(float));
+  const size_t o_bytes = static_cast<size_t>(p->n_part_rows) * p->D * sizeof(float);
+  const size_t need = cnt_bytes + ml_bytes + o_bytes;
+  if (need > kStaticScratchBytes)
+    return fail(PST_ERR_INVALID, "this batch needs %zu bytes of scratch; the fixed area holds %zu", need,
+                kStaticScratchBytes);
+  void* base = nullptr;
+  cudaError_t e = static_scratch_address(p->device, &base);
+  if (e != cudaSuccess) return fail(PST_ERR_CUDA, "cudaGetSymbolAddress(scratch): %s", cudaGetErrorString(e));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* b8 = static_cast<uint8_t*>(base);
+  int32_t* cnt = reinterpret_cast<int32_t*>(b8);
+  CUDA_TRY(cudaMemsetAsync(cnt, 0, static_cast<size_t>(B) * Hkv * sizeof(int32_t), s));
+  AttnParams a = base_params(p);
+  a.q = q;
+  a.out = out;
+  a.part_ml = reinterpret_cast<float*>(b8 + cnt_bytes);
+  a.part_o = reinterpret_cast<float*>(b8 + cnt_bytes + ml_bytes);
+  a.chunks = p->d_tab + p->off_chunks;
+  a.m_off = p->d_tab + p->off_moff;
+  a.m_ent = p->d_tab + p->off_ment;
+  a.m_cnt = cnt;
+  if (p->n_tc_items > 0) {
+    AttnParams a1 = a;
+    a1.items = reinterpret_cast<const WorkItem*>(p->d_tab + p->off_tc);
+    a1.n_items = p->n_tc_items;
+    a1.warp_items = p->d_tab + p->off_tc_cta;
+    e = launch_attn_tc(p->cfg.dtype, p->D, a1, p->n_tc_ctas, s);
+    if (e != cudaSuccess) return fail(PST_ERR_CUDA, "chunk-first launch: %s", cudaGetErrorString(e));
+  }
+  if (p->n_simt_items > 0) {
+    AttnParams a2 = a;
+    a2.items = reinterpret_cast<const WorkItem*>(p->d_tab + p->off_simt);
+    a2.n_items = p->n_simt_items;
+    a2.warp_items = p->d_tab + p->off_warp;
+    a2.n_warps = p->n_simt_warps;
+    a2.pdl = 0;
+    e = launch_attn_simt(p->cfg.dtype, p->D, p->C, p->g, a2, p->simt_grid, s);
+    if (e != cudaSuccess) return fail(PST_ERR_CUDA, "sequence-first launch: %s", cudaGetErrorString(e));
+  }
+  return PST_OK;
+}
+
 pst_status pst_decode_attention_host(pst_pool* p, const void* q_host, void* out_host, void* stream) {
   pst_status st = need_device(p);
   if (st != PST_OK) return st;

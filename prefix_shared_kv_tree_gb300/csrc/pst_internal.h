@@ -116,6 +116,12 @@ enum : int32_t {
   kErrBadIndex = 2,      // an index check failed
 };
 
+// Fixed device scratch used by pst_decode_attention_noalloc (static_scratch.cu).
+constexpr size_t kStaticScratchBytes = size_t(32) << 20;
+// Device address of that area on `device` (looked up once per device, with
+// the device made current for the lookup).
+cudaError_t static_scratch_address(int device, void** ptr);
+
 // Launchers (defined in the .cu files).  All return the launch status.
 cudaError_t launch_scatter(int dtype, int D, int C, const ScatterParams& p, cudaStream_t s);
 cudaError_t launch_gather(int dtype, int D, int C, const ScatterParams& p, cudaStream_t s);

@@ -62,6 +62,7 @@ SIGNATURES = {
     "pst_seq_length": (c_int, [_P, c_int64, _I64P]),
     "pst_decode_attention": (c_int, [_P, _P, _P, _P]),
     "pst_decode_attention_host": (c_int, [_P, _P, _P, _P]),
+    "pst_decode_attention_noalloc": (c_int, [_P, _P, _P, _P]),
     "pst_prefill_attend": (c_int, [_P, c_int64, _P, c_int64, _P, _P, _P, _P, _P]),
     "pst_gather_kv": (c_int, [_P, c_int64, _P, _P, _P]),
     "pst_export_tables": (c_int, [_P, _P, c_int64, _I64P, _P, c_int64, _I64P, _P, c_int64, _I64P]),
@@ -191,6 +192,10 @@ class Pool:
     # ---- attention
     def decode_attention(self, q, out, stream=None) -> None:
         check(lib.pst_decode_attention(self.h, _ptr(q), _ptr(out), _stream(stream)))
+
+    def decode_attention_noalloc(self, q, out, stream=None) -> None:
+        """pst_decode_attention_noalloc: same result, scratch in the library's fixed device area."""
+        check(lib.pst_decode_attention_noalloc(self.h, _ptr(q), _ptr(out), _stream(stream)))
 
     def decode_attention_host(self, q_host, out_host, stream=None) -> None:
         check(lib.pst_decode_attention_host(self.h, _ptr(q_host), _ptr(out_host), _stream(stream)))
