@@ -23,6 +23,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -52,6 +53,23 @@ def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return rank, world, local
+
+
+def max_over_ranks(x: float, device=None) -> float:
+    """Max of a per-rank number over all ranks (identity on one process)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(unique_bytes_per_rank: int, ms_per_step: float, world: int) -> float:
+    """Aggregate unique-KV GB/s of `world` replicas that each process one step
+    of the workload per `ms_per_step` (the max over ranks)."""
+    return world * unique_bytes_per_rank / (ms_per_step * 1e-3) / 1e9
 
 
 def measured_peak():
@@ -105,7 +123,7 @@ class ClockSampler:
     def __init__(self, device_index: int):
         self.dev = device_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+        self.path = os.path.join(tempfile.gettempdir(), f"pst_clocks_{os.getpid()}.csv")
 
     def start(self):
         try:
@@ -299,11 +317,7 @@ def run_ours(args):
     clk = clocks.stop()
     pool.set_profiling(False)
     times = [a.elapsed_time(b) for a, b in ev]
-    ms = sum(times) / len(times)
-    if world > 1:
-        t = torch.tensor([ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(sum(times) / len(times), device="cuda")
     assert pool.check_device() == 0
 
     # ---- e2e through the host-buffer entry point (H2D q, decode, D2H out, sync)
@@ -336,7 +350,7 @@ def run_ours(args):
     if rank != 0:
         return
     unique = spec.unique_kv_bytes()
-    value = world * unique / (ms * 1e-3) / 1e9
+    value = whole_job_gbs(unique, ms, world)
     es = {"f16": 2, "bf16": 2, "f32": 4}[spec.dtype]
     qbytes = spec.n_sequences * spec.n_q_heads * spec.head_dim * es
     line = {
