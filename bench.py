@@ -165,6 +165,15 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows), "samples_under_load": len(loaded)}
 
 
+def source_digest(files) -> str:
+    """sha256 (first 16 hex digits) of the listed kernel sources, concatenated."""
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "prefix_shared_kv_tree_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
 def traffic_for(kernel: str, workload: str):
     """DRAM bytes per launch from a committed ncu summary, if it was taken on the
     current source of that kernel (else None)."""
@@ -173,9 +182,7 @@ def traffic_for(kernel: str, workload: str):
         with open(path) as f:
             d = json.load(f)
         ent = d[workload][kernel]
-        src = os.path.join(ROOT, "prefix_shared_kv_tree_gb300", "csrc", ent["source"])
-        digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-        if digest != ent["source_sha256_16"]:
+        if source_digest(ent["sources"]) != ent["sources_sha256_16"]:
             return None
         return float(ent["bytes_per_launch"])
     except Exception:
@@ -338,14 +345,11 @@ def run_ours(args):
     peak, peak_kind = measured_peak()
     st = pool.stats()
     phase_ms = [sum(p[j] for p in phase) / len(phase) for j in range(3)]
-    names = ["chunk_first_tc", "sequence_first_simt", "merge"]
-    dom = max(range(3), key=lambda j: phase_ms[j])
+    names = ["chunk_first_tc", "sequence_first_simt", "whole_call"]
+    dom = max(range(2), key=lambda j: phase_ms[j])  # the dominant kernel (not the whole call)
     min_share = args.min_share or 2
-    dom_bytes = [shared_bytes(spec, min_share), private_bytes(spec, min_share), None][dom]
-    if dom_bytes is None:
-        dom_bytes = step_bytes(spec)
+    dom_bytes = [shared_bytes(spec, min_share), private_bytes(spec, min_share)][dom]
     achieved = dom_bytes / (phase_ms[dom] * 1e-3) / 1e9
-    kernel_src = {0: "kernels_tc.cu", 1: "kernels_simt.cu", 2: "kernels_simt.cu"}[dom]
 
     if rank != 0:
         return
