@@ -142,7 +142,8 @@ pst_status pst_seq_length(const pst_pool* pool, int64_t seq_id, int64_t* n_token
  * q, out: device [B][Hq][d], B = live count.  Rebuilds and uploads the chunk
  * tables first if the tree changed (Knowl 5).  Chunk-first partials run on the
  * tensor cores (tcgen05) for f16/bf16 with c = 64, sequence-first partials on
- * the CUDA cores, then an online-softmax merge writes out. */
+ * the CUDA cores, then a merge kernel combines the partial rows (attn_reduce)
+ * and writes out. */
 pst_status pst_decode_attention(pst_pool* pool, const void* q, void* out, void* stream);
 
 /* Same as pst_decode_attention with HOST q/out: copies q host->device, runs
@@ -156,20 +157,21 @@ pst_status pst_decode_attention_host(pst_pool* pool, const void* q_host, void* o
  * example a serving runtime that hands all GPU memory to its own allocator up
  * front, or a latency-critical loop where cudaMalloc / cudaFree would
  * synchronise the device.  Same inputs, outputs and result as
- * pst_decode_attention, but the partial rows and merge counters live in a
- * fixed 32 MiB device area that the library defines at file scope: every GPU
- * that loads the library holds that area until the process exits.
+ * pst_decode_attention, but the partial rows live in a fixed 32 MiB device
+ * area that the library defines at file scope: every GPU that loads the
+ * library holds that area until the process exits.
  *   - The first call on a device looks up the area's device address (once per
  *     device); make that first call before any stream capture.
  *   - Needs the chunk tables already on the device: after a structural change
  *     (insert, remove, a new chunk on append) call pst_decode_attention once
  *     first; otherwise returns PST_ERR_STATE.  It never rebuilds or uploads.
  *   - A batch needing more than 32 MiB of scratch (about
- *     B*Hkv*4 + partial_rows*(d+2)*4 bytes, see pst_stats) returns
+ *     partial_rows * (d + 2) * 4 bytes, see pst_stats) returns
  *     PST_ERR_INVALID.
- *   - All calls share the one area (it keeps the last call's contents; the
- *     call clears its merge counters itself): calls whose GPU work overlaps --
- *     on different streams or from different pools -- race with each other.
+ *   - All calls share the one area (it keeps the last call's contents; every
+ *     partial row is written before it is read, so nothing needs clearing):
+ *     calls whose GPU work overlaps -- on different streams or from different
+ *     pools -- race with each other.
  * Calls no cudaMalloc, cudaFree or other allocating routine. */
 pst_status pst_decode_attention_noalloc(pst_pool* pool, const void* q, void* out, void* stream);
 
@@ -209,8 +211,9 @@ pst_status pst_set_profiling(pst_pool* pool, int enable);
 
 /* Durations in ms of the last profiled decode: ms[0] chunk-first kernel,
  * ms[1] sequence-first kernel (0 when a kernel did not run), ms[2] the whole
- * call from its first to its last kernel (the online-softmax merge runs inside
- * both kernels).  Waits for those events. */
+ * call from its first kernel to the end of the merge.  Waits for those
+ * events.  (The per-kernel events sit between the kernels and may keep them
+ * from overlapping; time the whole call without profiling.) */
 pst_status pst_phase_times(pst_pool* pool, float* ms3);
 
 /* Kernel launches issued by the last pst_decode_attention call. */

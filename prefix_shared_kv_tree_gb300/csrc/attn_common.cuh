@@ -1,12 +1,6 @@
 // Device helpers shared by the attention kernels: element conversion, warp
 // reductions, and the online-softmax merge of a row's partial results
 // (ChunkAttention, Knowl 3: attn_reduce, then O = o / n).
-//
-// The merge is fused into the kernels that produce partials: every work item
-// that writes the (o, m, n) rows of a (batch row, KV head) pair bumps that
-// pair's arrival counter after its rows are globally visible; the warp whose
-// arrival completes the count merges the pair's rows and writes the output,
-// then resets the counter for the next call.  No warp ever waits for another.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -69,9 +63,9 @@ __device__ __forceinline__ float warp_sum(float x) {
 
 // Merge all partial rows of query head kv*g + hg of batch row u and write the
 // normalised output row.  Whole warp; lane owns D/32 contiguous features.
-// Partials are read through L2 (they were written by other SMs).  The result
-// is bit-identical to merge_row_thread: same max, then the same weighted sums
-// taken in entry order, then one multiply by 1/n.
+// Partials are read through L2 (they were written by other SMs): first the
+// row max over all entries, then the weighted sums taken in entry order, then
+// one multiply by 1/n.
 template <typename T, int D>
 __device__ __forceinline__ void merge_row(const AttnParams& p, int u, int kv, int hg, int lane) {
   constexpr int DPL = D / 32;
@@ -121,68 +115,6 @@ __device__ __forceinline__ void merge_row(const AttnParams& p, int u, int kv, in
   T* out = static_cast<T*>(p.out) + (static_cast<size_t>(u) * p.Hq + kv * p.g + hg) * D + lane * DPL;
 #pragma unroll
   for (int i = 0; i < DPL; ++i) out[i] = from_float<T>(o[i] * inv);
-}
-
-// Same merge done by a single thread for one full row (used where every lane
-// of a warp finishes a different row at once).
-template <typename T, int D>
-__device__ __forceinline__ void merge_row_thread(const AttnParams& p, int u, int kv, int hg) {
-  const int key = u * p.Hkv + kv;
-  const int e0 = __ldcg(p.m_off + key), e1 = __ldcg(p.m_off + key + 1);
-  float m = -INFINITY;
-  for (int e = e0; e < e1; ++e) {
-    const int pr = __ldcg(p.m_ent + e) + hg;
-    m = fmaxf(m, __ldcg(p.part_ml + 2 * static_cast<size_t>(pr)));
-  }
-  float4 o[D / 4];
-#pragma unroll
-  for (int i = 0; i < D / 4; ++i) o[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-  float n = 0.f;
-  for (int e = e0; e < e1; ++e) {
-    const int pr = __ldcg(p.m_ent + e) + hg;
-    const float2 mn = __ldcg(reinterpret_cast<const float2*>(p.part_ml) + pr);
-    if (mn.x == -INFINITY) continue;
-    const float w = ptx::ex2(mn.x - m);
-    n = fmaf(w, mn.y, n);
-    const float4* src = reinterpret_cast<const float4*>(p.part_o + static_cast<size_t>(pr) * D);
-#pragma unroll
-    for (int i = 0; i < D / 4; ++i) {
-      const float4 t = __ldcg(src + i);
-      o[i].x = fmaf(w, t.x, o[i].x);
-      o[i].y = fmaf(w, t.y, o[i].y);
-      o[i].z = fmaf(w, t.z, o[i].z);
-      o[i].w = fmaf(w, t.w, o[i].w);
-    }
-  }
-  const float inv = 1.f / n;
-  T* out = static_cast<T*>(p.out) + (static_cast<size_t>(u) * p.Hq + kv * p.g + hg) * D;
-#pragma unroll
-  for (int i = 0; i < D / 4; ++i) {
-    out[4 * i + 0] = from_float<T>(o[i].x * inv);
-    out[4 * i + 1] = from_float<T>(o[i].y * inv);
-    out[4 * i + 2] = from_float<T>(o[i].z * inv);
-    out[4 * i + 3] = from_float<T>(o[i].w * inv);
-  }
-}
-
-// Arrival of one work item at (u, kv) after this warp's partial rows were
-// stored.  Every lane must call it (the stores of all lanes are fenced);
-// `expected` (lane 0) is the pair's number of partial entries.  Returns true
-// on the lane-uniform "this arrival completed the pair".
-__device__ __forceinline__ bool arrive_pair(const AttnParams& p, int u, int kv, int lane, int expected) {
-  __syncwarp();  // orders the other lanes' stores before lane 0's release fence
-  int last = 0;
-  if (lane == 0) {
-    __threadfence();
-    const int key = u * p.Hkv + kv;
-    const int old = atomicAdd(p.m_cnt + key, 1);
-    last = (old + 1 == expected);
-    if (last) {
-      __threadfence();
-      p.m_cnt[key] = 0;  // every arrival of this call has happened: reset for the next call
-    }
-  }
-  return __shfl_sync(0xffffffffu, last, 0) != 0;
 }
 
 }  // namespace pst

@@ -12,8 +12,8 @@
 // ring.  Scores: lane = key, 128-bit shared loads, fp32 FMAs split over 4
 // accumulators; tile max by warp shuffles; row sums stay lane-local until the
 // item ends.  Values: lane = output feature row of V^T, 2 accumulators per row.
-// The item's (o, m, n) rows then go to the partial buffer and the last
-// arriving item of a (batch row, KV head) merges them (attn_common.cuh).
+// The item's (o, m, n) rows then go to the partial buffer; the merge kernel
+// that follows combines the rows of every (batch row, KV head).
 #pragma once
 
 #include "attn_common.cuh"
@@ -66,6 +66,7 @@ __global__ void __launch_bounds__(256, 1) attn_simt_kernel(const AttnParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  ptx::pdl_launch_dependents();  // the merge kernel may become resident; it waits for us
   const int gw = blockIdx.x * p.warps_per_cta + warp;
   const int it0 = gw < p.n_warps ? p.warp_items[gw] : 0;
   const int it1 = gw < p.n_warps ? p.warp_items[gw + 1] : 0;
@@ -123,11 +124,14 @@ __global__ void __launch_bounds__(256, 1) attn_simt_kernel(const AttnParams p) {
   bool aborted = false;
   const T* qptr = static_cast<const T*>(p.q);
 
-  // The next item's query rows are fetched into registers one item ahead.
+  // The next item's query rows and chunk lengths (lane c: chunk c, first 32
+  // chunks) are fetched into registers one item ahead.
   constexpr int NQ = (G * DCH + 31) / 32;
   uint4 qnext[NQ];
+  int len_next = 0;
   auto fetch_q = [&](int it_idx) {
     const WorkItem wn = p.items[it_idx];
+    len_next = lane < wn.n_chunks ? p.chunk_len[p.chunks[wn.chunk_off + lane]] : 0;
 #pragma unroll
     for (int k = 0; k < NQ; ++k) {
       const int idx = lane + 32 * k;
@@ -156,13 +160,8 @@ __global__ void __launch_bounds__(256, 1) attn_simt_kernel(const AttnParams p) {
       }
     }
     __syncwarp();
+    int my_len = len_next;
     if (it + 1 < it1) fetch_q(it + 1);
-    // arrivals this pair expects (read early, used at the end of the item)
-    int expected = 0;
-    if (!p.final_mode && lane == 0) {
-      const int key = grp * p.Hkv + w.kv;
-      expected = p.m_off[key + 1] - p.m_off[key];
-    }
 
     float m[G], nl[G], o[G][DPL][2];
 #pragma unroll
@@ -173,9 +172,8 @@ __global__ void __launch_bounds__(256, 1) attn_simt_kernel(const AttnParams p) {
       for (int i = 0; i < DPL; ++i) o[h][i][0] = o[h][i][1] = 0.f;
     }
 
-    int my_len = 0;
     for (int c = 0; c < w.n_chunks && !aborted; ++c) {
-      if ((c & 31) == 0) {  // valid tokens of chunks c .. c+31 of this item, one per lane
+      if ((c & 31) == 0 && c > 0) {  // valid tokens of chunks c .. c+31 of this item, one per lane
         my_len = 0;
         if (c + lane < w.n_chunks) my_len = p.chunk_len[p.chunks[w.chunk_off + c + lane]];
       }
@@ -323,9 +321,6 @@ __global__ void __launch_bounds__(256, 1) attn_simt_kernel(const AttnParams p) {
 #pragma unroll
         for (int i = 0; i < DPL; ++i) po[lane + 32 * i] = o[h][i][0] + o[h][i][1];
         if (lane == 0) reinterpret_cast<float2*>(p.part_ml)[row] = make_float2(m[h], n);
-      }
-      if (arrive_pair(p, grp, w.kv, lane, expected)) {
-        for (int h = 0; h < G; ++h) merge_row<T, D>(p, grp, w.kv, h, lane);
       }
     }
     __syncwarp();

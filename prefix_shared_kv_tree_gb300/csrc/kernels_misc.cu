@@ -1,5 +1,5 @@
-// K/V scatter into the chunk pool (and gather back out), plus the dtype
-// dispatch of the CUDA-core attention kernel.  The pool stores each (chunk, KV
+// K/V scatter into the chunk pool (and gather back out), the merge kernel,
+// and the dtype dispatch of the CUDA-core attention kernel.  The pool stores each (chunk, KV
 // head) as a K block and a transposed V block in the core-matrix layout of
 // pst_internal.h; the scatter builds that layout from user rows [n][Hkv][D]
 // (ChunkAttention, Knowl 1: K and V slices of h x c x d per chunk), see tile_off.
@@ -96,7 +96,51 @@ __global__ void __launch_bounds__(256) gather_kernel(const ScatterParams p, int 
   }
 }
 
+// ---------------------------------------------------------------------------
+// Merge (ChunkAttention, Knowl 3: attn_reduce over all partial rows of a
+// query row, then O = o / n).  One warp per (batch row, KV head) pair; the
+// partials come from the chunk-first and sequence-first kernels that precede
+// it on the stream.  Launched as a programmatic dependent: it becomes
+// resident while they run and waits for their completion before reading.
+// ---------------------------------------------------------------------------
+template <typename T, int D>
+__global__ void __launch_bounds__(128) merge_kernel(const AttnParams p, int B) {
+  if (p.pdl) ptx::pdl_wait();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int pair = blockIdx.x * 4 + warp;
+  if (pair >= B * p.Hkv) return;
+  const int u = pair / p.Hkv, kv = pair % p.Hkv;
+  for (int hg = 0; hg < p.g; ++hg) merge_row<T, D>(p, u, kv, hg, lane);
+}
+
+template <typename T>
+cudaError_t launch_merge_t(int D, const AttnParams& p, int B, cudaStream_t s) {
+  const int pairs = B * p.Hkv;
+  if (pairs == 0) return cudaSuccess;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((pairs + 3) / 4);
+  cfg.blockDim = dim3(128);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = p.pdl ? 1 : 0;
+  if (D == 64) return cudaLaunchKernelEx(&cfg, merge_kernel<T, 64>, p, B);
+  if (D == 128) return cudaLaunchKernelEx(&cfg, merge_kernel<T, 128>, p, B);
+  return cudaErrorInvalidValue;
+}
+
 }  // namespace
+
+cudaError_t launch_merge(int dtype, int D, const AttnParams& p, int B, cudaStream_t s) {
+  switch (dtype) {
+    case kF16: return launch_merge_t<__half>(D, p, B, s);
+    case kBF16: return launch_merge_t<__nv_bfloat16>(D, p, B, s);
+    case kF32: return launch_merge_t<float>(D, p, B, s);
+  }
+  return cudaErrorInvalidValue;
+}
 
 bool simt_supported(int dtype, int D, int g) {
   return (dtype == kF16 || dtype == kBF16 || dtype == kF32) && (D == 64 || D == 128) &&

@@ -26,7 +26,8 @@
 //                 log2 units, write the rounded probabilities P to shared
 //                 memory as the A operand of the PV product, fold each chunk's
 //                 O_k into fp32 registers (o = o * alpha + O_k), then write the
-//                 item's partial rows and merge completed rows (attn_common.cuh).
+//                 item's partial rows (the merge kernel combines them) or, for a
+//                 prefill block, the normalised output rows.
 // Every wait is bounded; on a timeout the CTA records an error, drains its
 // copies and MMAs, frees TMEM and exits.
 #include <cuda_bf16.h>
@@ -117,7 +118,7 @@ __global__ void __launch_bounds__(224, 1) attn_tc_kernel(const AttnParams p) {
   volatile int* issued_slot = abort_flag + 1;
   volatile int* consumed_slot = abort_flag + 2;
 
-  ptx::pdl_launch_dependents();  // the sequence-first kernel does not read our results
+  ptx::pdl_launch_dependents();  // the kernels that follow wait for our results themselves
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int i0 = p.warp_items[blockIdx.x];
@@ -404,27 +405,6 @@ __global__ void __launch_bounds__(224, 1) attn_tc_kernel(const AttnParams p) {
           for (int j = 0; j < D / 4; ++j) po[j] = make_float4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
           reinterpret_cast<float2*>(p.part_ml)[prow_i] = make_float2(m, l);
         }
-      }
-      if (!p.final_mode) {
-        // One arrival per (batch row, KV head) group of g rows; g divides 32,
-        // so a group never straddles two warps.  The arrival that completes a
-        // pair merges it (attn_common.cuh).
-        __threadfence();
-        __syncwarp();
-        int last = 0;
-        if (row_valid && hg == 0) {
-          const int key = grp * p.Hkv + w.kv;
-          const int expected = __ldcg(p.m_off + key + 1) - __ldcg(p.m_off + key);
-          const int old = atomicAdd(p.m_cnt + key, 1);
-          last = (old + 1 == expected);
-          if (last) {
-            __threadfence();
-            p.m_cnt[key] = 0;
-          }
-        }
-        // every row of a completed group merges itself, all lanes in parallel
-        last = __shfl_sync(0xffffffffu, last, lane - hg);
-        if (last && row_valid) merge_row_thread<T, D>(p, grp, w.kv, hg);
       }
     }
   }

@@ -128,7 +128,6 @@ struct pst_pool {
   float* d_part_ml = nullptr;
   size_t part_cap = 0;  // rows
   int32_t* d_err = nullptr;
-  int32_t* d_cnt = nullptr;  // merge arrival counters, max_seqs * Hkv
   int32_t* d_pre = nullptr;
   size_t pre_cap = 0;
   int32_t* h_stage = nullptr;  // pinned upload staging
@@ -665,9 +664,6 @@ pst_status pst_pool_create(const pst_config* cfg, int device, pst_pool** out) {
     if ((e = cudaMemset(p->d_chunk_len, 0, sizeof(int32_t) * c.max_chunks)) != cudaSuccess) return bail(e, "cudaMemset");
     if ((e = cudaMalloc(&p->d_err, sizeof(int32_t))) != cudaSuccess) return bail(e, "cudaMalloc");
     if ((e = cudaMemset(p->d_err, 0, sizeof(int32_t))) != cudaSuccess) return bail(e, "cudaMemset");
-    const size_t ncnt = static_cast<size_t>(p->cfg.max_seqs) * c.n_kv_heads;
-    if ((e = cudaMalloc(&p->d_cnt, sizeof(int32_t) * ncnt)) != cudaSuccess) return bail(e, "cudaMalloc");
-    if ((e = cudaMemset(p->d_cnt, 0, sizeof(int32_t) * ncnt)) != cudaSuccess) return bail(e, "cudaMemset");
     if ((e = cudaStreamCreateWithFlags(&p->aux, cudaStreamNonBlocking)) != cudaSuccess) return bail(e, "stream");
     if ((e = cudaEventCreateWithFlags(&p->ev_fork, cudaEventDisableTiming)) != cudaSuccess) return bail(e, "event");
     if ((e = cudaEventCreateWithFlags(&p->ev_join, cudaEventDisableTiming)) != cudaSuccess) return bail(e, "event");
@@ -691,7 +687,6 @@ pst_status pst_pool_free(pst_pool* p) {
     cudaFree(p->d_part_o);
     cudaFree(p->d_part_ml);
     cudaFree(p->d_err);
-    cudaFree(p->d_cnt);
     cudaFree(p->d_pre);
     cudaFree(p->d_q);
     cudaFree(p->d_out);
@@ -857,7 +852,6 @@ static pst_status decode_impl(pst_pool* p, const void* q, void* out, cudaStream_
   a.chunks = p->d_tab + p->off_chunks;
   a.m_off = p->d_tab + p->off_moff;
   a.m_ent = p->d_tab + p->off_ment;
-  a.m_cnt = p->d_cnt;
   const bool fork = p->n_tc_items > 0 && p->n_simt_items > 0 && (p->cfg.flags & PST_FLAG_CONCURRENT_PHASES);
   cudaStream_t s1 = fork ? p->aux : s;
   if (p->profiling) CUDA_TRY(cudaEventRecord(p->pev[4], s));
@@ -895,6 +889,13 @@ static pst_status decode_impl(pst_pool* p, const void* q, void* out, cudaStream_
     CUDA_TRY(cudaEventRecord(p->ev_join, p->aux));
     CUDA_TRY(cudaStreamWaitEvent(s, p->ev_join, 0));
   }
+  {
+    AttnParams am = a;
+    am.pdl = fork ? 0 : 1;  // right behind the attention kernel(s) on this stream
+    cudaError_t e = launch_merge(p->cfg.dtype, p->D, am, B, s);
+    if (e != cudaSuccess) return fail(PST_ERR_CUDA, "merge launch: %s", cudaGetErrorString(e));
+    p->last_launches++;
+  }
   if (p->profiling) {
     CUDA_TRY(cudaEventRecord(p->pev[5], s));
     p->pran[2] = true;
@@ -908,9 +909,9 @@ pst_status pst_decode_attention(pst_pool* p, const void* q, void* out, void* str
   return decode_impl(p, q, out, static_cast<cudaStream_t>(stream));
 }
 
-// Decode attention without any allocation: the partial rows and the merge
-// counters go to the library's fixed device scratch instead of the pool's own
-// buffers.  Only launches kernels and one memset on `stream`.
+// Decode attention without any allocation: the partial rows go to the
+// library's fixed device scratch instead of the pool's own buffers.  Only
+// launches kernels on `stream`.
 pst_status pst_decode_attention_noalloc(pst_pool* p, const void* q, void* out, void* stream) {
   pst_status st = need_device(p);
   if (st != PST_OK) return st;
@@ -921,12 +922,10 @@ pst_status pst_decode_attention_noalloc(pst_pool* p, const void* q, void* out, v
   const int32_t B = static_cast<int32_t>(p->batch.size());
   if (B == 0) return PST_OK;
   if (!q || !out) return fail(PST_ERR_INVALID, "null q/out with %d live sequences", B);
-  const int Hkv = p->cfg.n_kv_heads;
   auto align256 = [](size_t x) { return (x + 255) / 256 * 256; };
-  const size_t cnt_bytes = align256(static_cast<size_t>(B) * Hkv * sizeof(int32_t));
   const size_t ml_bytes = align256(static_cast<size_t>(p->n_part_rows) * 2 * sizeof(float));
   const size_t o_bytes = static_cast<size_t>(p->n_part_rows) * p->D * sizeof(float);
-  const size_t need = cnt_bytes + ml_bytes + o_bytes;
+  const size_t need = ml_bytes + o_bytes;
   if (need > kStaticScratchBytes)
     return fail(PST_ERR_INVALID, "this batch needs %zu bytes of scratch; the fixed area holds %zu", need,
                 kStaticScratchBytes);
@@ -935,17 +934,14 @@ pst_status pst_decode_attention_noalloc(pst_pool* p, const void* q, void* out, v
   if (e != cudaSuccess) return fail(PST_ERR_CUDA, "cudaGetSymbolAddress(scratch): %s", cudaGetErrorString(e));
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* b8 = static_cast<uint8_t*>(base);
-  int32_t* cnt = reinterpret_cast<int32_t*>(b8);
-  CUDA_TRY(cudaMemsetAsync(cnt, 0, static_cast<size_t>(B) * Hkv * sizeof(int32_t), s));
   AttnParams a = base_params(p);
   a.q = q;
   a.out = out;
-  a.part_ml = reinterpret_cast<float*>(b8 + cnt_bytes);
-  a.part_o = reinterpret_cast<float*>(b8 + cnt_bytes + ml_bytes);
+  a.part_ml = reinterpret_cast<float*>(b8);
+  a.part_o = reinterpret_cast<float*>(b8 + ml_bytes);
   a.chunks = p->d_tab + p->off_chunks;
   a.m_off = p->d_tab + p->off_moff;
   a.m_ent = p->d_tab + p->off_ment;
-  a.m_cnt = cnt;
   if (p->n_tc_items > 0) {
     AttnParams a1 = a;
     a1.items = reinterpret_cast<const WorkItem*>(p->d_tab + p->off_tc);
@@ -960,10 +956,14 @@ pst_status pst_decode_attention_noalloc(pst_pool* p, const void* q, void* out, v
     a2.n_items = p->n_simt_items;
     a2.warp_items = p->d_tab + p->off_warp;
     a2.n_warps = p->n_simt_warps;
-    a2.pdl = 0;
+    a2.pdl = p->n_tc_items > 0 ? 1 : 0;
     e = launch_attn_simt(p->cfg.dtype, p->D, p->C, p->g, a2, p->simt_grid, s);
     if (e != cudaSuccess) return fail(PST_ERR_CUDA, "sequence-first launch: %s", cudaGetErrorString(e));
   }
+  AttnParams am = a;
+  am.pdl = 1;
+  e = launch_merge(p->cfg.dtype, p->D, am, B, s);
+  if (e != cudaSuccess) return fail(PST_ERR_CUDA, "merge launch: %s", cudaGetErrorString(e));
   return PST_OK;
 }
 
@@ -1195,10 +1195,6 @@ pst_status pst_check_device(pst_pool* p, int32_t* code) {
   CUDA_TRY(cudaDeviceSynchronize());
   CUDA_TRY(cudaMemcpy(code, p->d_err, sizeof(int32_t), cudaMemcpyDeviceToHost));
   CUDA_TRY(cudaMemset(p->d_err, 0, sizeof(int32_t)));
-  if (*code) {
-    // a kernel gave up part-way: its merge counters may be stale
-    CUDA_TRY(cudaMemset(p->d_cnt, 0, sizeof(int32_t) * static_cast<size_t>(p->cfg.max_seqs) * p->cfg.n_kv_heads));
-  }
   if (*code) return fail(PST_ERR_DEVICE, "device error word 0x%x", *code);
   return PST_OK;
 }

@@ -72,25 +72,15 @@ struct AttnParams {
   int32_t stages;             // CUDA-core kernel: piece stages per warp
   int32_t warps_per_cta;      // CUDA-core kernel
   int32_t* err;               // device error word
-  // fused merge (partial mode): CSR of partial rows per (batch row, KV head),
-  // and one arrival counter per pair (zero between calls)
+  // merge CSR of partial rows per (batch row, KV head) (read by the merge)
   const int32_t* m_off;       // [B * Hkv + 1]
   const int32_t* m_ent;       // partial row of head kv*g + 0 for each entry
-  int32_t* m_cnt;             // [B * Hkv]
   // 1: launched as a programmatic dependent of the previous kernel on the
   // stream (it may start while that kernel drains; it must not finish first)
   int32_t pdl;
 };
 
-struct MergeParams {
-  const int32_t* off;    // [B * Hkv + 1] CSR offsets per (batch row, KV head)
-  const int32_t* ent;    // partial row of query head kv*g + 0; head kv*g + hg is at +hg
-  const float* part_o;
-  const float* part_ml;
-  void* out;             // [B][Hq][D]
-  int32_t B, Hq, Hkv, g;
-  int32_t* err;
-};
+
 
 // Copies user K/V rows into pool tiles (or back out, for gather).
 struct ScatterOp {
@@ -133,7 +123,10 @@ cudaError_t launch_attn_simt_bf16(int D, int C, int g, const AttnParams& p, int 
 cudaError_t launch_attn_simt_f32(int D, int C, int g, const AttnParams& p, int grid, cudaStream_t s);
 cudaError_t launch_attn_tc(int dtype, int D, const AttnParams& p, int grid, cudaStream_t s);
 size_t attn_tc_smem(int D);
-cudaError_t launch_merge(int dtype, int D, const MergeParams& p, cudaStream_t s);
+// Merge of the partial rows of every (batch row, KV head) pair into `out`
+// (one warp per pair); a programmatic dependent of the previous kernel when
+// p.pdl is set.
+cudaError_t launch_merge(int dtype, int D, const AttnParams& p, int B, cudaStream_t s);
 bool simt_supported(int dtype, int D, int g);
 bool tc_supported(int dtype, int D, int C);
 
