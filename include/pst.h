@@ -140,7 +140,8 @@ pst_status pst_seq_length(const pst_pool* pool, int64_t seq_id, int64_t* n_token
 /* Decode attention (Knowl 2 + 3): out[u][h] = softmax(q[u][h] K_u^T / sqrt(d)) V_u
  * for every live sequence u in batch order, over all of its cached tokens.
  * q, out: device [B][Hq][d], B = live count.  Rebuilds and uploads the chunk
- * tables first if the tree changed (Knowl 5).  Chunk-first partials run on the
+ * tables first if the tree changed (Knowl 5).  q and out must start on a
+ * 16-byte boundary (PST_ERR_INVALID otherwise).  Chunk-first partials run on the
  * tensor cores (tcgen05) for f16/bf16 with c = 64, sequence-first partials on
  * the CUDA cores, then a merge kernel combines the partial rows (attn_reduce)
  * and writes out. */
@@ -179,7 +180,7 @@ pst_status pst_decode_attention_noalloc(pst_pool* pool, const void* q, void* out
  * (host tokens int32[W], device k_new/v_new [W][Hkv][d]) to sequence seq_id at
  * positions [p0, p0+W), p0 = its current length, then out[t][h] =
  * softmax(q[t][h] K^T / sqrt(d)) V over keys [0, p0+t] of the sequence.
- * q, out: device [W][Hq][d].  Appended tokens are never merged with other
+ * q, out: device [W][Hq][d], 16-byte aligned.  Appended tokens are never merged with other
  * sequences' chunks.  Atomic on PST_ERR_OOM. */
 pst_status pst_prefill_attend(pst_pool* pool, int64_t seq_id, const int32_t* tokens, int64_t W,
                               const void* q, const void* k_new, const void* v_new, void* out,

@@ -61,43 +61,84 @@ __device__ __forceinline__ float warp_sum(float x) {
   return x;
 }
 
-// Merge all partial rows of query head kv*g + hg of batch row u and write the
-// normalised output row.  Whole warp; lane owns D/32 contiguous features.
-// Partials are read through L2 (they were written by other SMs): first the
-// row max over all entries, then the weighted sums taken in entry order, then
-// one multiply by 1/n.
+// Merge the partial rows of one output row -- query head kv*g + hg of batch
+// row u, task = (u * Hkv + kv) * g + hg -- whose pair owns entries [e0, e1)
+// (entry e: partial row e*g + hg), and write the normalised output row.
+// Whole warp; lane owns D/32 contiguous features.  Partials are read through
+// L2 (other SMs wrote them): the (m, n) of every entry at once (lane = entry)
+// for the row max, then the weighted sums taken in entry order, then one
+// multiply by 1/n (ChunkAttention, Knowl 3: attn_reduce, then O = o / n).
 template <typename T, int D>
-__device__ __forceinline__ void merge_row(const AttnParams& p, int u, int kv, int hg, int lane) {
+__device__ __forceinline__ void merge_row(const AttnParams& p, int task, int e0, int e1, int lane) {
   constexpr int DPL = D / 32;
-  const int key = u * p.Hkv + kv;
-  const int e0 = __ldcg(p.m_off + key), e1 = __ldcg(p.m_off + key + 1);
+  constexpr int kFast = 16;  // entries merged from registers after one round of loads
+  const int g = p.g, hg = task % g;
+  const int cnt = e1 - e0;
+  const float2* ml = reinterpret_cast<const float2*>(p.part_ml);
+  if (cnt <= kFast) {
+    // Every load first -- each entry's (m, n) (lane = entry) and this lane's
+    // features of every entry's o row -- then the same arithmetic, in the same
+    // entry order, as the general path below.
+    using VecT = typename std::conditional<DPL == 4, float4, float2>::type;
+    VecT ov[kFast];
+#pragma unroll
+    for (int j = 0; j < kFast; ++j)
+      if (j < cnt)
+        ov[j] = __ldcg(reinterpret_cast<const VecT*>(p.part_o + (static_cast<size_t>(e0 + j) * g + hg) * D + lane * DPL));
+    const float2 mn = lane < cnt ? __ldcg(ml + static_cast<size_t>(e0 + lane) * g + hg) : make_float2(-INFINITY, 0.f);
+    const float m = warp_max(mn.x);
+    float o[DPL];
+#pragma unroll
+    for (int i = 0; i < DPL; ++i) o[i] = 0.f;
+    float n = 0.f;
+#pragma unroll
+    for (int j = 0; j < kFast; ++j) {
+      if (j < cnt) {
+        const float mj = __shfl_sync(0xffffffffu, mn.x, j);
+        const float nj = __shfl_sync(0xffffffffu, mn.y, j);
+        const float wj = mj == -INFINITY ? 0.f : ptx::ex2(mj - m);
+        n = fmaf(wj, nj, n);
+        if constexpr (DPL == 4) {
+          o[0] = fmaf(wj, ov[j].x, o[0]);
+          o[1] = fmaf(wj, ov[j].y, o[1]);
+          o[2] = fmaf(wj, ov[j].z, o[2]);
+          o[3] = fmaf(wj, ov[j].w, o[3]);
+        } else {
+          o[0] = fmaf(wj, ov[j].x, o[0]);
+          o[1] = fmaf(wj, ov[j].y, o[1]);
+        }
+      }
+    }
+    const float inv = 1.f / n;
+    T* out = static_cast<T*>(p.out) + static_cast<size_t>(task) * D + lane * DPL;
+#pragma unroll
+    for (int i = 0; i < DPL; ++i) out[i] = from_float<T>(o[i] * inv);
+    return;
+  }
+  float2 first = make_float2(-INFINITY, 0.f);  // entry `lane` of the first 32
   float m = -INFINITY;
-  for (int e = e0 + lane; e < e1; e += 32) {
-    const int pr = __ldcg(p.m_ent + e) + hg;
-    m = fmaxf(m, __ldcg(p.part_ml + 2 * static_cast<size_t>(pr)));
+  for (int e = lane; e < cnt; e += 32) {
+    const float2 t = __ldcg(ml + static_cast<size_t>(e0 + e) * g + hg);
+    if (e < 32) first = t;
+    m = fmaxf(m, t.x);
   }
   m = warp_max(m);
   float o[DPL];
 #pragma unroll
   for (int i = 0; i < DPL; ++i) o[i] = 0.f;
   float n = 0.f;
-  for (int base = e0; base < e1; base += 32) {
-    const int cnt = min(32, e1 - base);
-    int pr = 0;
-    float2 mn = make_float2(-INFINITY, 0.f);
-    if (lane < cnt) {
-      pr = __ldcg(p.m_ent + base + lane) + hg;
-      mn = __ldcg(reinterpret_cast<const float2*>(p.part_ml) + pr);
-    }
-#pragma unroll 4
-    for (int j = 0; j < cnt; ++j) {
-      const int prj = __shfl_sync(0xffffffffu, pr, j);
+  for (int base = 0; base < cnt; base += 32) {
+    float2 mn = first;
+    if (base > 0) mn = lane < cnt - base ? __ldcg(ml + static_cast<size_t>(e0 + base + lane) * g + hg)
+                                         : make_float2(-INFINITY, 0.f);
+    const int c = min(32, cnt - base);
+#pragma unroll 8
+    for (int j = 0; j < c; ++j) {
       const float mj = __shfl_sync(0xffffffffu, mn.x, j);
       const float nj = __shfl_sync(0xffffffffu, mn.y, j);
-      if (mj == -INFINITY) continue;
-      const float wj = ptx::ex2(mj - m);
+      const float wj = mj == -INFINITY ? 0.f : ptx::ex2(mj - m);  // an entry with no valid key adds nothing
       n = fmaf(wj, nj, n);
-      const float* src = p.part_o + static_cast<size_t>(prj) * D + lane * DPL;
+      const float* src = p.part_o + (static_cast<size_t>(e0 + base + j) * g + hg) * D + lane * DPL;
       if constexpr (DPL == 4) {
         const float4 t = __ldcg(reinterpret_cast<const float4*>(src));
         o[0] = fmaf(wj, t.x, o[0]);
@@ -112,7 +153,7 @@ __device__ __forceinline__ void merge_row(const AttnParams& p, int u, int kv, in
     }
   }
   const float inv = 1.f / n;
-  T* out = static_cast<T*>(p.out) + (static_cast<size_t>(u) * p.Hq + kv * p.g + hg) * D + lane * DPL;
+  T* out = static_cast<T*>(p.out) + static_cast<size_t>(task) * D + lane * DPL;
 #pragma unroll
   for (int i = 0; i < DPL; ++i) out[i] = from_float<T>(o[i] * inv);
 }

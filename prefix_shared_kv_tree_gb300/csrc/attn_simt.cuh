@@ -3,17 +3,28 @@
 // chunk-first phase when the tensor-core kernel does not apply (fp32, c = 32),
 // and causal prefill blocks in that case.
 //
-// Warp-per-stream design.  Each warp owns a contiguous share of the grid's
-// (chunk, KV head) tiles, split on the host into work items of one
-// (group, KV head) each.  A tile is consumed as pieces -- each 128-byte column
-// block of K (all C keys), then each 64-row group of V^T -- each a contiguous
-// block of the pool's tile image; lane 0 of the warp keeps `stages` pieces in
-// flight with bulk async copies (TMA engine) into the warp's shared-memory
-// ring.  Scores: lane = key, 128-bit shared loads, fp32 FMAs split over 4
-// accumulators; tile max by warp shuffles; row sums stay lane-local until the
-// item ends.  Values: lane = output feature row of V^T, 2 accumulators per row.
-// The item's (o, m, n) rows then go to the partial buffer; the merge kernel
-// that follows combines the rows of every (batch row, KV head).
+// Warp-specialised, warp-per-stream design.  A CTA holds NW consumer warps and
+// one producer warp; lane c of the producer serves consumer c:
+//   * it claims work items (a run of up to four chunks of one (group, KV
+//     head), chunk ids inline) one at a time from a global counter, largest
+//     first, so consumers whose SM came free late (an earlier kernel held it)
+//     simply get fewer;
+//   * it fills the consumer's two item slots: the item header by shared
+//     stores, the chunks' valid-token counts by 4-byte async copies, the
+//     query rows by one bulk async copy;
+//   * it keeps the consumer's ring of `stages` pieces full with bulk async
+//     copies (TMA engine): a tile is consumed as 32-row pieces -- each 32-key
+//     half of every 128-byte column block of K, then each 32-row group of
+//     V^T -- each a contiguous block of the pool's tile image.
+// The consumer warps issue no global load and no atomic at all: every latency
+// of the item pipeline (claim, descriptor, chunk lengths, query rows, tiles)
+// sits in the producer, which waits for none of them in the step that issued
+// it.  Consumers wait on mbarriers only.  Scores: lane = key, 128-bit shared
+// loads, fp32 FMAs split over 4 accumulators; tile max by warp shuffles; row
+// sums stay lane-local until the item ends.  Values: lane = output feature row
+// of V^T, 2 accumulators per row.  The item's (o, m, n) rows then go to the
+// partial buffer; the merge kernel that follows combines the rows of every
+// (batch row, KV head).
 #pragma once
 
 #include "attn_common.cuh"
@@ -23,325 +34,574 @@ namespace pst {
 
 __host__ __device__ inline size_t simt_align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Pieces of a tile (see tile_off): each 128-byte column block of K (C rows),
-// then each 64-row group of every column block of V^T.
+// Rows per piece of a tile (see tile_off): each run of kSimtPieceRows keys of
+// every 128-byte column block of K, then each run of kSimtPieceRows rows of
+// every column block of V^T -- each a contiguous block of the tile image.
+#ifndef PST_SIMT_PIECE_ROWS
+#define PST_SIMT_PIECE_ROWS 64
+#endif
+constexpr int kSimtPieceRows = PST_SIMT_PIECE_ROWS;
+static_assert(kSimtPieceRows == 32 || kSimtPieceRows == 64, "piece rows");
+
 __host__ __device__ inline size_t simt_stage_bytes(int C, int D, int es) {
-  const size_t kpb = static_cast<size_t>(C) * 128;
-  const size_t vpb = ((C * es) % 128 == 0) ? static_cast<size_t>(64) * 128 : static_cast<size_t>(64) * C * es;
+  const int kr = C < kSimtPieceRows ? C : kSimtPieceRows;
+  const int vr = D < kSimtPieceRows ? D : kSimtPieceRows;
+  const size_t kpb = static_cast<size_t>(kr) * 128;
+  const size_t vpb = ((C * es) % 128 == 0) ? static_cast<size_t>(vr) * 128 : static_cast<size_t>(vr) * C * es;
   return kpb > vpb ? kpb : vpb;
 }
 
-// Shared memory of one warp: [stages x piece][q rows fp32][p fp32][barriers].
+// Consumer warps per CTA at most (one more warp produces).  With nine warps
+// one SM sub-partition holds three, which caps registers at 168 per thread:
+// query groups of four and more take seven consumers (255 registers).
+#ifndef PST_SIMT_G4_WARPS
+#define PST_SIMT_G4_WARPS 7
+#endif
+__host__ __device__ constexpr int simt_max_warps(int G) { return G >= 8 ? 7 : G >= 4 ? PST_SIMT_G4_WARPS : 8; }
+
+// Item slot: a 64-byte header -- [0] n_chunks (0: no more work), [1] kv,
+// [2] group0, [3] part_base, [4..7] valid tokens of the first four chunks,
+// [8] chunk-list offset of a longer run, [12..15] the chunk ids of a run of
+// at most four -- then the item's G query rows as stored (G * D elements).
+constexpr int kSlotHeader = 64;
+
+// Shared memory of one consumer warp, all offsets from the warp's base:
+// [stages x piece][q rows fp32][p fp32][2 item slots][barriers: full[S],
+// empty[S], slot_full[2], slot_empty[2]].
+struct SimtLayout {
+  uint32_t stage, q, p, slot, slot_bytes, bars, total;
+};
+
+__host__ __device__ inline SimtLayout simt_layout(int C, int D, int G, int S, int es) {
+  SimtLayout L;
+  L.stage = static_cast<uint32_t>(simt_stage_bytes(C, D, es));
+  size_t off = static_cast<size_t>(S) * L.stage;
+  L.q = static_cast<uint32_t>(off);
+  off += static_cast<size_t>(G) * D * 4;
+  L.p = static_cast<uint32_t>(off);
+  off += static_cast<size_t>(G) * C * 4;
+  off = simt_align_up(off, 128);
+  L.slot = static_cast<uint32_t>(off);
+  L.slot_bytes = static_cast<uint32_t>(kSlotHeader + static_cast<size_t>(G) * D * es);
+  off += 2 * static_cast<size_t>(L.slot_bytes);
+  off = simt_align_up(off, 8);
+  L.bars = static_cast<uint32_t>(off);
+  off += static_cast<size_t>(2 * S + 4) * 8;
+  L.total = static_cast<uint32_t>(simt_align_up(off, 128));
+  return L;
+}
+
 __host__ __device__ inline size_t simt_warp_bytes(int C, int D, int G, int S, int es) {
-  size_t b = S * simt_stage_bytes(C, D, es);
-  b += static_cast<size_t>(G) * D * 4;
-  b += static_cast<size_t>(G) * C * 4;
-  b = simt_align_up(b, 8) + S * 8;
-  return simt_align_up(b, 128);
+  return simt_layout(C, D, G, S, es).total;
+}
+
+// A work item as loaded: the two raw 16-byte halves of the SimtItem and
+// whether the claimed index was a real item.  The producer lets a loaded item
+// sit for a whole item before touching it, so the load's latency never stalls.
+struct SimtMeta {
+  int4 a;  // chunk[0..3]
+  int4 b;  // n_chunks, kv, group0, part_base
+  int valid;
+  __device__ __forceinline__ int n_chunks() const { return valid ? b.x : 0; }
+  __device__ __forceinline__ int kv() const { return b.y; }
+  __device__ __forceinline__ int group0() const { return b.z; }
+  __device__ __forceinline__ int part_base() const { return b.w; }
+};
+
+// Loads item idx (a claimed index; past the end it reads the last item and
+// marks the result invalid).  n_items >= 1.
+__device__ __forceinline__ SimtMeta simt_load_item(const SimtItem* items, int idx, int n_items) {
+  SimtMeta m;
+  const int4* src = reinterpret_cast<const int4*>(items + min(idx, n_items - 1));
+  m.a = __ldg(src);
+  m.b = __ldg(src + 1);
+  m.valid = idx < n_items;
+  return m;
+}
+
+// Chunk id c of an item (inline ids, or the id list for long runs); c < n.
+__device__ __forceinline__ int simt_chunk_id(const SimtMeta& m, int c, const int32_t* chunks) {
+  if (m.b.x > kSimtInline) return chunks[m.a.x + c];
+  return c == 0 ? m.a.x : c == 1 ? m.a.y : c == 2 ? m.a.z : m.a.w;
 }
 
 template <typename T, int D, int G, int C>
-__global__ void __launch_bounds__(256, 1) attn_simt_kernel(const AttnParams p) {
+__global__ void __launch_bounds__(32 * (simt_max_warps(G) + 1), 1) attn_simt_kernel(const AttnParams p) {
   constexpr int ES = sizeof(T);
   constexpr int VEC = 16 / ES;
-  constexpr int DCH = D / VEC;    // 16-byte chunks per K row
-  constexpr int CCH = C / VEC;    // 16-byte chunks per V^T row
-  constexpr int KPL = C / 32;     // keys per lane
-  constexpr int KB = D * ES / 128;                 // K pieces: 128-byte column blocks, C rows each
-  constexpr bool VSW = (C * ES) % 128 == 0;         // V^T rows in 128-byte swizzled blocks
-  constexpr int VB = VSW ? C * ES / 128 : 1;        // V^T column blocks
-  constexpr int VR = D / 64;                        // 64-row groups per V^T block
-  constexpr int VP = VB * VR;                       // V^T pieces
-  constexpr int NP = KB + VP;
-  constexpr int DPL = D / 32;     // output features per lane
-  constexpr int KCH = 128 / 16;   // 16-byte chunks per K piece row
-  constexpr int VCH = VSW ? 8 : C * ES / 16;        // 16-byte chunks per V^T piece row
-  constexpr uint32_t KPB = static_cast<uint32_t>(C) * 128u;
-  constexpr uint32_t VPB = VSW ? 64u * 128u : 64u * C * ES;
+  constexpr int DCH = D / VEC;     // 16-byte chunks per query row
+  constexpr int KB = D * ES / 128;                       // K: 128-byte column blocks of C rows
+  constexpr int KPR = C < kSimtPieceRows ? C : kSimtPieceRows;  // keys per K piece
+  constexpr int KPC = C / KPR;                           // K pieces per column block
+  constexpr int KT = KPR / 32;                           // keys per lane per K piece
+  constexpr int KPL = C / 32;      // keys per lane per chunk
+  constexpr bool VSW = (C * ES) % 128 == 0;              // V^T rows in 128-byte swizzled blocks
+  constexpr int VB = VSW ? C * ES / 128 : 1;             // V^T column blocks
+  constexpr int VPR = D < kSimtPieceRows ? D : kSimtPieceRows;  // feature rows per V^T piece
+  constexpr int VG = D / VPR;                            // V^T pieces per column block
+  constexpr int VT = VPR / 32;                           // feature rows per lane per V^T piece
+  constexpr int NP = KB * KPC + VB * VG;                 // pieces per tile
+  constexpr int DPL = D / 32;      // output features per lane
+  constexpr int KCH = 128 / 16;    // 16-byte chunks per K piece row
+  constexpr int VCH = VSW ? 8 : C * ES / 16;             // 16-byte chunks per V^T piece row
+  constexpr uint32_t KPB = static_cast<uint32_t>(KPR) * 128u;
+  constexpr uint32_t VPB = VSW ? static_cast<uint32_t>(VPR) * 128u : static_cast<uint32_t>(VPR) * C * ES;
   constexpr uint32_t HALF = static_cast<uint32_t>(C) * D * ES;
   constexpr size_t TILE = 2 * static_cast<size_t>(HALF);
+  constexpr uint32_t QBYTES = static_cast<uint32_t>(G) * D * ES;
+  constexpr int NQ = (G * DCH + 31) / 32;  // 16-byte query pieces per lane
   const int S = p.stages;
-  const uint32_t SB = static_cast<uint32_t>(simt_stage_bytes(C, D, ES));
+  const int NW = p.warps_per_cta;  // consumer warps; warp NW produces
+  const SimtLayout L = simt_layout(C, D, G, S, ES);
 
   extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ int s_abort;
+  __shared__ __align__(16) SimtItem s_batch[2][8];  // claimed item descriptors, two batches of NW
+  __shared__ uint64_t s_bbar[2];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   ptx::pdl_launch_dependents();  // the merge kernel may become resident; it waits for us
-  const int gw = blockIdx.x * p.warps_per_cta + warp;
-  const int it0 = gw < p.n_warps ? p.warp_items[gw] : 0;
-  const int it1 = gw < p.n_warps ? p.warp_items[gw + 1] : 0;
-  if (it0 >= it1) {
-    if (p.pdl) ptx::pdl_wait();  // never complete before the kernel we overlap
-    return;
+  const int n_items = p.n_items;
+  const SimtItem* items = reinterpret_cast<const SimtItem*>(p.items);
+
+  if (threadIdx.x == 0) {
+    s_abort = 0;
+    ptx::mbar_init(&s_bbar[0], 1);
+    ptx::mbar_init(&s_bbar[1], 1);
   }
-
-  uint8_t* wb = smem + static_cast<size_t>(warp) * simt_warp_bytes(C, D, G, S, ES);
-  uint8_t* stages = wb;
-  float* qbuf = reinterpret_cast<float*>(wb + static_cast<size_t>(S) * SB);
-  float* pbuf = qbuf + G * D;
-  uint64_t* full = reinterpret_cast<uint64_t*>(simt_align_up(reinterpret_cast<size_t>(pbuf + G * C), 8));
-
-  if (lane == 0) {
-    for (int s = 0; s < S; ++s) ptx::mbar_init(&full[s], 1);
+  if (warp < NW && lane == 0) {
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(warp) * L.total + L.bars);
+    for (int s = 0; s < 2 * S + 4; ++s) ptx::mbar_init(&bars[s], 1);
     ptx::fence_mbar_init();
   }
-  __syncwarp();
+  __syncthreads();
+  volatile int* abort_flag = &s_abort;
 
-  // Producer cursor (lane 0 only): next piece to stage.
-  int pi = it0, pc = 0, pp = 0;
-  uint32_t issued = 0;
-  WorkItem pw = p.items[it0];
-  auto issue_next = [&]() {
-    if (pi >= it1) return;
-    const int chunk = p.chunks[pw.chunk_off + pc];
-    const uint8_t* tile = p.pool + (static_cast<size_t>(chunk) * p.Hkv + pw.kv) * TILE;
-    const uint8_t* src;
-    if (pp < KB) {
-      src = tile + pp * KPB;
-    } else {
-      const int vb = (pp - KB) / VR, vr = (pp - KB) % VR;
-      src = tile + HALF + (VSW ? (static_cast<size_t>(vb) * D * 128 + vr * 64 * 128) : static_cast<size_t>(vr) * VPB);
-    }
-    const uint32_t bytes = pp < KB ? KPB : VPB;
-    const int s = issued % S;
-    ptx::mbar_arrive_expect_tx(&full[s], bytes);
-    ptx::bulk_g2s(stages + static_cast<size_t>(s) * SB, src, bytes, &full[s]);
-    ++issued;
-    if (++pp == NP) {
-      pp = 0;
-      if (++pc == pw.n_chunks) {
-        pc = 0;
-        if (++pi < it1) pw = p.items[pi];
+  if (warp == NW) {
+    // ================================================================ producer
+    // Fills lane c's consumer's two item slots (c < NW).  Items are claimed
+    // for the whole CTA, NW consecutive indices per atomic; a batch's
+    // descriptors land in s_batch by one bulk copy.  Two batches are in hand
+    // and the claim of a third is in flight, so this warp never reads a
+    // register that a global load or atomic of the current step still fills
+    // (its lanes share one scoreboard: such a read would stall every lane).
+    const bool mine = lane < NW;
+    uint8_t* rb = smem + static_cast<size_t>(mine ? lane : 0) * L.total;
+    uint8_t* slots = rb + L.slot;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(rb + L.bars);
+    uint64_t* sfull = bars + 2 * S;
+    uint64_t* sempty = bars + 2 * S + 2;
+    const T* qptr = static_cast<const T*>(p.q);
+    auto fill_batch = [&](int buf, int base) {  // lane 0
+      const int valid = max(0, min(n_items - base, NW));
+      if (valid > 0) {
+        ptx::mbar_arrive_expect_tx(&s_bbar[buf], valid * static_cast<uint32_t>(sizeof(SimtItem)));
+        ptx::bulk_g2s(&s_batch[buf][0], items + base, valid * static_cast<uint32_t>(sizeof(SimtItem)), &s_bbar[buf]);
+      } else {
+        ptx::mbar_arrive(&s_bbar[buf]);
       }
+    };
+    int base0 = 0, base1 = 0, pend = 0;
+    if (lane == 0) {
+      base0 = atomicAdd(p.sched, NW);
+      base1 = atomicAdd(p.sched, NW);
     }
-  };
-  if (lane == 0) {
-    for (int s = 0; s < S; ++s) issue_next();
-  }
-  __syncwarp();
-
-  uint32_t consumed = 0;
-  bool aborted = false;
-  const T* qptr = static_cast<const T*>(p.q);
-
-  // The next item's query rows and chunk lengths (lane c: chunk c, first 32
-  // chunks) are fetched into registers one item ahead.
-  constexpr int NQ = (G * DCH + 31) / 32;
-  uint4 qnext[NQ];
-  int len_next = 0;
-  auto fetch_q = [&](int it_idx) {
-    const WorkItem wn = p.items[it_idx];
-    len_next = lane < wn.n_chunks ? p.chunk_len[p.chunks[wn.chunk_off + lane]] : 0;
-#pragma unroll
-    for (int k = 0; k < NQ; ++k) {
-      const int idx = lane + 32 * k;
-      if (idx < G * DCH) {
-        const int h = idx / DCH, j = idx % DCH;
-        qnext[k] = *reinterpret_cast<const uint4*>(qptr + (static_cast<size_t>(wn.group0) * p.Hq + wn.kv * p.g + h) * D +
-                                                  j * VEC);
-      }
+    base0 = __shfl_sync(0xffffffffu, base0, 0);
+    base1 = __shfl_sync(0xffffffffu, base1, 0);
+    if (lane == 0) {
+      fill_batch(0, base0);
+      fill_batch(1, base1);
+      pend = base1 + NW < n_items ? atomicAdd(p.sched, NW) : n_items;
     }
-  };
-  fetch_q(it0);
-
-  for (int it = it0; it < it1 && !aborted; ++it) {
-    const WorkItem w = p.items[it];
-    const int grp = w.group0;
-    // Query rows of this group, pre-scaled into log2 units.
-#pragma unroll
-    for (int k = 0; k < NQ; ++k) {
-      const int idx = lane + 32 * k;
-      if (idx < G * DCH) {
-        const int h = idx / DCH, j = idx % DCH;
-        float f[VEC];
-        unpack16<T>(qnext[k], f);
-#pragma unroll
-        for (int e = 0; e < VEC; ++e) qbuf[h * D + j * VEC + e] = f[e] * p.scale_log2;
-      }
-    }
-    __syncwarp();
-    int my_len = len_next;
-    if (it + 1 < it1) fetch_q(it + 1);
-
-    float m[G], nl[G], o[G][DPL][2];
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-      m[h] = -INFINITY;
-      nl[h] = 0.f;
-#pragma unroll
-      for (int i = 0; i < DPL; ++i) o[h][i][0] = o[h][i][1] = 0.f;
-    }
-
-    for (int c = 0; c < w.n_chunks && !aborted; ++c) {
-      if ((c & 31) == 0 && c > 0) {  // valid tokens of chunks c .. c+31 of this item, one per lane
-        my_len = 0;
-        if (c + lane < w.n_chunks) my_len = p.chunk_len[p.chunks[w.chunk_off + c + lane]];
-      }
-      int lim = __shfl_sync(0xffffffffu, my_len, c & 31);
-      if (p.causal_p0 >= 0) lim = min(lim, p.causal_p0 + grp + 1 - c * C);
-
-      // ---- scores over the K pieces (one 128-byte column block of all keys each)
-      float acc[G][KPL][4];
-#pragma unroll
-      for (int h = 0; h < G; ++h)
-#pragma unroll
-        for (int kk = 0; kk < KPL; ++kk) acc[h][kk][0] = acc[h][kk][1] = acc[h][kk][2] = acc[h][kk][3] = 0.f;
-#pragma unroll
-      for (int kb = 0; kb < KB; ++kb) {
-        const int s = consumed % S;
-        if (!ptx::mbar_wait(&full[s], (consumed / S) & 1, nullptr, p.err)) {
-          aborted = true;
-          break;
+    uint32_t fills0 = 1, fills1 = 1;
+    int bcur = 0, bpos = 0;
+    bool finished = !mine;
+    int qs = 0;
+    uint32_t written = 0, idle = 0;
+    uint64_t idle_since = 0;
+    while (true) {
+      // ---- next item into the consumer's next slot, once it has released it
+      const bool want = !finished && (written < 2 || ptx::mbar_test_wait(&sempty[qs], ((written >> 1) - 1) & 1));
+      const unsigned wm = __ballot_sync(0xffffffffu, want);
+      if (wm != 0u) {
+        const int cnt = __popc(wm);
+        // the current batch (and, past its end, the next) must have landed
+        bool ok = ptx::mbar_wait(&s_bbar[bcur], ((bcur ? fills1 : fills0) - 1) & 1, abort_flag, p.err);
+        if (bpos + cnt > NW)
+          ok = ok && ptx::mbar_wait(&s_bbar[bcur ^ 1], ((bcur ? fills0 : fills1) - 1) & 1, abort_flag, p.err);
+        if (!__all_sync(0xffffffffu, ok)) break;
+        if (want) {
+          const int pos = bpos + __popc(wm & ((1u << lane) - 1u));
+          const int buf = pos < NW ? bcur : (bcur ^ 1);
+          const int i = pos < NW ? pos : pos - NW;
+          const int idx = (buf ? base1 : base0) + i;
+          const int4* d = reinterpret_cast<const int4*>(&s_batch[buf][i]);
+          SimtMeta cur;
+          cur.a = d[0];
+          cur.b = d[1];
+          cur.valid = idx < n_items;
+          uint8_t* sl = slots + static_cast<size_t>(qs) * L.slot_bytes;
+          int* hdr = reinterpret_cast<int*>(sl);
+          const int n = cur.n_chunks();
+          hdr[0] = n;
+          if (n > 0) {
+            hdr[1] = cur.kv();
+            hdr[2] = cur.group0();
+            hdr[3] = cur.part_base();
+            hdr[8] = cur.a.x;
+            *reinterpret_cast<int4*>(hdr + 12) = cur.a;  // chunk ids of a short run (words 12..15)
+            if (n <= kSimtInline) {
+              for (int c = 0; c < n; ++c) ptx::cp_async_4(hdr + 4 + c, p.chunk_len + simt_chunk_id(cur, c, p.chunks));
+              ptx::cp_async_mbar_arrive(&sfull[qs]);  // the slot completes only once they landed
+            }
+            ptx::mbar_arrive_expect_tx(&sfull[qs], QBYTES);  // release: the header stores above
+            ptx::bulk_g2s(sl + kSlotHeader, qptr + (static_cast<size_t>(cur.group0()) * p.Hq + cur.kv() * p.g) * D,
+                          QBYTES, &sfull[qs]);
+          } else {
+            ptx::mbar_arrive(&sfull[qs]);  // end marker
+            finished = true;
+          }
+          ++written;
+          if (++qs == 2) qs = 0;
         }
-        const uint8_t* kt = stages + static_cast<size_t>(s) * SB;
+        bpos += cnt;
+        if (bpos >= NW) {
+          // The current batch is used up (every read of it above fed a store
+          // that has issued): refill its buffer with the batch claimed last time.
+          const int nb = __shfl_sync(0xffffffffu, pend, 0);
+          if (bcur == 0) {
+            base0 = nb;
+            ++fills0;
+          } else {
+            base1 = nb;
+            ++fills1;
+          }
+          if (lane == 0) {
+            fill_batch(bcur, nb);
+            pend = nb + NW < n_items ? atomicAdd(p.sched, NW) : n_items;
+          }
+          bcur ^= 1;
+          bpos -= NW;
+        }
+      }
+      if (__all_sync(0xffffffffu, finished)) break;
+      if (*abort_flag) break;
+      if (wm != 0u) {
+        idle = 0;
+      } else if ((++idle & 255u) == 0) {  // the timer is read now and then only
+        const uint64_t t = ptx::globaltimer();
+        if (idle == 256) {
+          idle_since = t;
+        } else if (t - idle_since > ptx::kWaitLimitNs) {
+          if (lane == 0) atomicOr(p.err, kErrWaitTimeout);
+          *abort_flag = 1;
+        }
+      }
+    }
+    // Every bulk copy this warp started must land before the CTA exits: the
+    // last fill of each batch buffer and of each of this lane's slots.
+    ptx::mbar_wait(&s_bbar[0], (fills0 - 1) & 1, nullptr, p.err);
+    ptx::mbar_wait(&s_bbar[1], (fills1 - 1) & 1, nullptr, p.err);
+    if (mine)
+      for (int q = 0; q < 2; ++q)
+        if (written > static_cast<uint32_t>(q)) {
+          const uint32_t last = q + ((written - 1 - q) / 2) * 2;
+          ptx::mbar_wait(&sfull[q], (last >> 1) & 1, nullptr, p.err);
+        }
+  } else {
+    // ================================================================ consumer
+    uint8_t* rb = smem + static_cast<size_t>(warp) * L.total;
+    uint8_t* stages = rb;
+    float* qbuf = reinterpret_cast<float*>(rb + L.q);
+    float* pbuf = reinterpret_cast<float*>(rb + L.p);
+    const uint8_t* slots = rb + L.slot;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(rb + L.bars);
+    uint64_t* full = bars;
+    uint64_t* sfull = bars + 2 * S;
+    uint64_t* sempty = bars + 2 * S + 2;
+
+    // Staging (lane 0): the tiles of item si (this item or the next) go into
+    // the warp's ring of S pieces; an item's chunk ids come from its slot
+    // header, which the producer wrote before that slot completed.
+    uint32_t k = 0;  // items started
+    uint32_t si = 0;          // item being staged
+    bool s_ready = false;     // its header is in s_* below
+    bool s_done = false;      // no more items to stage
+    int s_n = 0, s_kv = 0, s_list = 0, pc = 0, pp = 0, ps = 0;
+    int4 s_ids = make_int4(0, 0, 0, 0);
+    uint32_t issued = 0;
+    auto issue_next = [&]() -> bool {  // false: nothing can be issued now
+      if (s_done || si > k + 1) return false;
+      if (!s_ready) {
+        if (!ptx::mbar_test_wait(&sfull[si & 1], (si >> 1) & 1)) return false;
+        const int* h = reinterpret_cast<const int*>(slots + static_cast<size_t>(si & 1) * L.slot_bytes);
+        s_n = h[0];
+        if (s_n == 0) {
+          s_done = true;
+          return false;
+        }
+        s_kv = h[1];
+        s_list = h[8];
+        s_ids = *reinterpret_cast<const int4*>(h + 12);
+        s_ready = true;
+        pc = 0;
+        pp = 0;
+      }
+      const int chunk = s_n > kSimtInline ? p.chunks[s_list + pc]
+                                          : (pc == 0 ? s_ids.x : pc == 1 ? s_ids.y : pc == 2 ? s_ids.z : s_ids.w);
+      const uint8_t* tile = p.pool + (static_cast<size_t>(chunk) * p.Hkv + s_kv) * TILE;
+      const uint8_t* src;
+      uint32_t bytes;
+      if (pp < KB * KPC) {
+        src = tile + (pp / KPC) * (C * 128) + (pp % KPC) * KPB;
+        bytes = KPB;
+      } else {
+        const int vb = (pp - KB * KPC) / VG, vg = (pp - KB * KPC) % VG;
+        src = tile + HALF + (VSW ? (static_cast<size_t>(vb) * D * 128 + vg * VPB) : static_cast<size_t>(vg) * VPB);
+        bytes = VPB;
+      }
+      ptx::mbar_arrive_expect_tx_relaxed(&full[ps], bytes);
+      ptx::bulk_g2s(stages + static_cast<size_t>(ps) * L.stage, src, bytes, &full[ps]);
+      ++issued;
+      if (++ps == S) ps = 0;
+      if (++pp == NP) {
+        pp = 0;
+        if (++pc == s_n) {
+          ++si;
+          s_ready = false;
+        }
+      }
+      return true;
+    };
+    uint32_t consumed = 0;
+    int cs = 0;          // stage of the next piece
+    uint32_t cph = 0;    // its mbarrier phase parity
+    bool aborted = false;
+
+    for (; !aborted; ++k) {
+      const int qs = k & 1;
+      if (!ptx::mbar_wait(&sfull[qs], (k >> 1) & 1, abort_flag, p.err)) break;
+      const uint8_t* sl = slots + static_cast<size_t>(qs) * L.slot_bytes;
+      const int* hdr = reinterpret_cast<const int*>(sl);
+      const int n_chunks = hdr[0];
+      if (n_chunks == 0) break;  // end marker
+      const int kv = hdr[1], grp = hdr[2], part_base = hdr[3], list_off = hdr[8];
+      // valid tokens of chunks 0 .. 31 of this item, one per lane (long runs,
+      // from prefill only, read them from the chunk-length array)
+      int my_len = lane < n_chunks ? hdr[4 + min(lane, kSimtInline - 1)] : 0;
+      if (n_chunks > kSimtInline) my_len = lane < n_chunks ? p.chunk_len[p.chunks[list_off + lane]] : 0;
+      // query rows of this item, pre-scaled into log2 units
+#pragma unroll
+      for (int kq = 0; kq < NQ; ++kq) {
+        const int idx = lane + 32 * kq;
+        if (idx < G * DCH) {
+          const int h = idx / DCH, j = idx % DCH;
+          float f[VEC];
+          unpack16<T>(*reinterpret_cast<const uint4*>(sl + kSlotHeader + (static_cast<size_t>(h) * D + j * VEC) * ES),
+                      f);
+#pragma unroll
+          for (int e = 0; e < VEC; ++e) qbuf[h * D + j * VEC + e] = f[e] * p.scale_log2;
+        }
+      }
+      if (lane == 0) {  // stage ahead: the rest of this item and the start of the next
+        while (issued < consumed + S && issue_next()) {
+        }
+      }
+      __syncwarp();
+      // The slot is free once the header and rows are in registers / qbuf;
+      // staging (lane 0, above) read item k+1's slot, never item k's after this.
+      if (lane == 0) ptx::mbar_arrive_relaxed(&sempty[qs]);
+
+      // o[h][i]: two partial sums (even / odd keys of each 16-byte run) of
+      // output feature lane + 32 i, added at the end; packed fp32x2 FMAs
+      float m[G], nl[G];
+      float2 o[G][DPL];
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        m[h] = -INFINITY;
+        nl[h] = 0.f;
+#pragma unroll
+        for (int i = 0; i < DPL; ++i) o[h][i] = make_float2(0.f, 0.f);
+      }
+
+      for (int c = 0; c < n_chunks && !aborted; ++c) {
+        if ((c & 31) == 0 && c > 0) {  // valid tokens of chunks c .. c+31 (long runs only)
+          my_len = c + lane < n_chunks ? p.chunk_len[p.chunks[list_off + c + lane]] : 0;
+        }
+        int lim = __shfl_sync(0xffffffffu, my_len, c & 31);
+        if (p.causal_p0 >= 0) lim = min(lim, p.causal_p0 + grp + 1 - c * C);
+
+        // ---- scores over the K pieces
+        float2 acc[G][KPL][2];  // per key: four partial sums (feature i mod 4), as two pairs
+#pragma unroll
+        for (int h = 0; h < G; ++h)
+#pragma unroll
+          for (int kk = 0; kk < KPL; ++kk) acc[h][kk][0] = acc[h][kk][1] = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int kp = 0; kp < KB * KPC; ++kp) {
+          const int kb = kp / KPC, kh = kp % KPC;  // column block, key run: keys kh*KPR + lane + 32 t
+          if (!ptx::mbar_wait(&full[cs], cph, abort_flag, p.err)) {
+            aborted = true;
+            break;
+          }
+          const uint8_t* kt = stages + static_cast<size_t>(cs) * L.stage;
 #pragma unroll 4
-        for (int jj = 0; jj < KCH; ++jj) {
+          for (int jj = 0; jj < KCH; ++jj) {
 #pragma unroll
-          for (int kk = 0; kk < KPL; ++kk) {
-            const int r = lane + 32 * kk;
-            float kf[VEC];
-            unpack16<T>(*reinterpret_cast<const uint4*>(kt + r * 128 + ((jj ^ (r & 7)) << 4)), kf);
+            for (int t = 0; t < KT; ++t) {
+              const int r = lane + 32 * t;
+              float kf[VEC];
+              unpack16<T>(*reinterpret_cast<const uint4*>(kt + r * 128 + ((jj ^ (r & 7)) << 4)), kf);
 #pragma unroll
-            for (int h = 0; h < G; ++h) {
-              const float4* qv = reinterpret_cast<const float4*>(qbuf + h * D + kb * (128 / ES) + jj * VEC);
+              for (int h = 0; h < G; ++h) {
+                const float4* qv = reinterpret_cast<const float4*>(qbuf + h * D + kb * (128 / ES) + jj * VEC);
 #pragma unroll
-              for (int e4 = 0; e4 < VEC / 4; ++e4) {
-                const float4 qq = qv[e4];
-                acc[h][kk][0] = fmaf(qq.x, kf[4 * e4 + 0], acc[h][kk][0]);
-                acc[h][kk][1] = fmaf(qq.y, kf[4 * e4 + 1], acc[h][kk][1]);
-                acc[h][kk][2] = fmaf(qq.z, kf[4 * e4 + 2], acc[h][kk][2]);
-                acc[h][kk][3] = fmaf(qq.w, kf[4 * e4 + 3], acc[h][kk][3]);
+                for (int e4 = 0; e4 < VEC / 4; ++e4) {
+                  const float4 qq = qv[e4];
+                  acc[h][kh * KT + t][0] =
+                      __ffma2_rn(make_float2(qq.x, qq.y), make_float2(kf[4 * e4 + 0], kf[4 * e4 + 1]), acc[h][kh * KT + t][0]);
+                  acc[h][kh * KT + t][1] =
+                      __ffma2_rn(make_float2(qq.z, qq.w), make_float2(kf[4 * e4 + 2], kf[4 * e4 + 3]), acc[h][kh * KT + t][1]);
+                }
               }
             }
           }
+          __syncwarp();  // every lane is done with the stage
+          ++consumed;
+          if (++cs == S) {
+            cs = 0;
+            cph ^= 1u;
+          }
+          if (lane == 0) issue_next();
+        }
+        if (aborted) break;
+        float sc[G][KPL];
+#pragma unroll
+        for (int h = 0; h < G; ++h)
+#pragma unroll
+          for (int kk = 0; kk < KPL; ++kk)
+            sc[h][kk] = (acc[h][kk][0].x + acc[h][kk][0].y) + (acc[h][kk][1].x + acc[h][kk][1].y);
+
+        // ---- online softmax over the chunk's C keys (Knowl 3, log2 units)
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          float mx = -INFINITY;
+#pragma unroll
+          for (int kk = 0; kk < KPL; ++kk) {
+            if (kk * 32 + lane >= lim) sc[h][kk] = -INFINITY;
+            mx = fmaxf(mx, sc[h][kk]);
+          }
+          const float m_new = fmaxf(m[h], warp_max(mx));
+          const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+          const float alpha = ptx::ex2(m[h] - m_use);
+          float ps_ = 0.f;
+#pragma unroll
+          for (int kk = 0; kk < KPL; ++kk) {
+            const float pr = ptx::ex2(sc[h][kk] - m_use);
+            ps_ += pr;
+            pbuf[h * C + kk * 32 + lane] = pr;
+          }
+          nl[h] = nl[h] * alpha + ps_;
+#pragma unroll
+          for (int i = 0; i < DPL; ++i) o[h][i] = __fmul2_rn(o[h][i], make_float2(alpha, alpha));
+          m[h] = m_new;
         }
         __syncwarp();
-        ++consumed;
-        if (lane == 0) issue_next();
-      }
-      if (aborted) break;
-      float sc[G][KPL];
-#pragma unroll
-      for (int h = 0; h < G; ++h)
-#pragma unroll
-        for (int kk = 0; kk < KPL; ++kk)
-          sc[h][kk] = (acc[h][kk][0] + acc[h][kk][1]) + (acc[h][kk][2] + acc[h][kk][3]);
 
-      // ---- online softmax over the chunk's C keys (Knowl 3, log2 units)
+        // ---- o += p V over the V^T pieces (VPR feature rows of one key block each)
 #pragma unroll
-      for (int h = 0; h < G; ++h) {
-        float mx = -INFINITY;
-#pragma unroll
-        for (int kp = 0; kp < KPL; ++kp) {
-          if (kp * 32 + lane >= lim) sc[h][kp] = -INFINITY;
-          mx = fmaxf(mx, sc[h][kp]);
-        }
-        const float m_new = fmaxf(m[h], warp_max(mx));
-        const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-        const float alpha = ptx::ex2(m[h] - m_use);
-        float ps = 0.f;
-#pragma unroll
-        for (int kp = 0; kp < KPL; ++kp) {
-          const float pr = ptx::ex2(sc[h][kp] - m_use);
-          ps += pr;
-          pbuf[h * C + kp * 32 + lane] = pr;
-        }
-        nl[h] = nl[h] * alpha + ps;
-#pragma unroll
-        for (int i = 0; i < DPL; ++i) {
-          o[h][i][0] *= alpha;
-          o[h][i][1] *= alpha;
-        }
-        m[h] = m_new;
-      }
-      __syncwarp();
-
-      // ---- o += p V over the V^T pieces (64 feature rows of one key block each)
-#pragma unroll
-      for (int vp = 0; vp < VP; ++vp) {
-        const int vb = vp / VR, vr = vp % VR;
-        const int s = consumed % S;
-        if (!ptx::mbar_wait(&full[s], (consumed / S) & 1, nullptr, p.err)) {
-          aborted = true;
-          break;
-        }
-        const uint8_t* vt = stages + static_cast<size_t>(s) * SB;
-#pragma unroll 2
-        for (int j = 0; j < VCH; ++j) {
-          const int key0 = (VSW ? vb * (128 / ES) : 0) + j * VEC;
-          float pv[G][VEC];
-#pragma unroll
-          for (int h = 0; h < G; ++h) {
-            const float4* pp4 = reinterpret_cast<const float4*>(pbuf + h * C + key0);
-#pragma unroll
-            for (int e4 = 0; e4 < VEC / 4; ++e4) {
-              const float4 t = pp4[e4];
-              pv[h][4 * e4 + 0] = t.x;
-              pv[h][4 * e4 + 1] = t.y;
-              pv[h][4 * e4 + 2] = t.z;
-              pv[h][4 * e4 + 3] = t.w;
-            }
+        for (int vp = 0; vp < VB * VG; ++vp) {
+          const int vb = vp / VG, vg = vp % VG;  // key block, feature rows vg*VPR + lane + 32 t
+          if (!ptx::mbar_wait(&full[cs], cph, abort_flag, p.err)) {
+            aborted = true;
+            break;
           }
-#pragma unroll
-          for (int r2 = 0; r2 < 2; ++r2) {
-            const int r = lane + 32 * r2;
-            float vf[VEC];
-            const uint32_t off = VSW ? r * 128 + ((j ^ (r & 7)) << 4) : cm_off(r, j, VCH);
-            unpack16<T>(*reinterpret_cast<const uint4*>(vt + off), vf);
+          const uint8_t* vt = stages + static_cast<size_t>(cs) * L.stage;
+#pragma unroll 2
+          for (int j = 0; j < VCH; ++j) {
+            const int key0 = (VSW ? vb * (128 / ES) : 0) + j * VEC;
+            float pv[G][VEC];
 #pragma unroll
             for (int h = 0; h < G; ++h) {
+              const float4* pp4 = reinterpret_cast<const float4*>(pbuf + h * C + key0);
 #pragma unroll
-              for (int e = 0; e < VEC; ++e)
-                o[h][2 * vr + r2][e & 1] = fmaf(pv[h][e], vf[e], o[h][2 * vr + r2][e & 1]);
+              for (int e4 = 0; e4 < VEC / 4; ++e4) {
+                const float4 t4 = pp4[e4];
+                pv[h][4 * e4 + 0] = t4.x;
+                pv[h][4 * e4 + 1] = t4.y;
+                pv[h][4 * e4 + 2] = t4.z;
+                pv[h][4 * e4 + 3] = t4.w;
+              }
+            }
+#pragma unroll
+            for (int t = 0; t < VT; ++t) {
+              const int r = lane + 32 * t;
+              float vf[VEC];
+              const uint32_t off = VSW ? r * 128 + ((j ^ (r & 7)) << 4) : cm_off(r, j, VCH);
+              unpack16<T>(*reinterpret_cast<const uint4*>(vt + off), vf);
+#pragma unroll
+              for (int h = 0; h < G; ++h) {
+#pragma unroll
+                for (int e = 0; e < VEC; e += 2)
+                  o[h][vg * VT + t] = __ffma2_rn(make_float2(pv[h][e], pv[h][e + 1]), make_float2(vf[e], vf[e + 1]),
+                                                 o[h][vg * VT + t]);
+              }
             }
           }
+          __syncwarp();  // every lane is done with the stage, and with pbuf before the next chunk rewrites it
+          ++consumed;
+          if (++cs == S) {
+            cs = 0;
+            cph ^= 1u;
+          }
+          if (lane == 0) issue_next();
         }
-        __syncwarp();
-        ++consumed;
-        if (lane == 0) issue_next();
+      }
+      if (aborted) break;
+
+      // ---- item result
+      if (p.final_mode) {
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          const float inv = 1.f / warp_sum(nl[h]);
+          T* out = static_cast<T*>(p.out) + (static_cast<size_t>(grp) * p.Hq + kv * p.g + h) * D;
+#pragma unroll
+          for (int i = 0; i < DPL; ++i) out[lane + 32 * i] = from_float<T>((o[h][i].x + o[h][i].y) * inv);
+        }
+      } else {
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          const float n = warp_sum(nl[h]);
+          const size_t row = static_cast<size_t>(part_base) + h;
+          float* po = p.part_o + row * D;
+#pragma unroll
+          for (int i = 0; i < DPL; ++i) po[lane + 32 * i] = o[h][i].x + o[h][i].y;
+          if (lane == 0) reinterpret_cast<float2*>(p.part_ml)[row] = make_float2(m[h], n);
+        }
       }
     }
-    if (aborted) break;
-
-    // ---- item result
-    if (p.final_mode) {
-#pragma unroll
-      for (int h = 0; h < G; ++h) {
-        const float inv = 1.f / warp_sum(nl[h]);
-        T* out = static_cast<T*>(p.out) + (static_cast<size_t>(grp) * p.Hq + w.kv * p.g + h) * D;
-#pragma unroll
-        for (int i = 0; i < DPL; ++i) out[lane + 32 * i] = from_float<T>((o[h][i][0] + o[h][i][1]) * inv);
-      }
-    } else {
-#pragma unroll
-      for (int h = 0; h < G; ++h) {
-        const float n = warp_sum(nl[h]);
-        const size_t row = static_cast<size_t>(w.part_base) + h;
-        float* po = p.part_o + row * D;
-#pragma unroll
-        for (int i = 0; i < DPL; ++i) po[lane + 32 * i] = o[h][i][0] + o[h][i][1];
-        if (lane == 0) reinterpret_cast<float2*>(p.part_ml)[row] = make_float2(m[h], n);
+    if (lane == 0) {
+      // Let every copy still in flight land before the warp leaves (only
+      // after an abort are there any).
+      for (uint32_t x = consumed; x < issued; ++x) {
+        const int s = static_cast<int>(x % S);
+        ptx::mbar_wait(&full[s], (x / S) & 1, nullptr, p.err);
       }
     }
-    __syncwarp();
-  }
-
-  if (aborted && lane == 0) {
-    // Let every copy still in flight land before the warp leaves.
-    for (uint32_t k = consumed; k < issued; ++k) ptx::mbar_wait(&full[k % S], (k / S) & 1, nullptr, p.err);
   }
   if (p.pdl) ptx::pdl_wait();  // never complete before the kernel we overlap
 }
 
 template <typename T, int D, int G, int C>
 cudaError_t launch_simt_t(const AttnParams& p, int grid, cudaStream_t s) {
+  if (p.warps_per_cta < 1 || p.warps_per_cta > simt_max_warps(G)) return cudaErrorInvalidValue;
   const size_t smem = simt_warp_bytes(C, D, G, p.stages, sizeof(T)) * p.warps_per_cta;
   auto fn = attn_simt_kernel<T, D, G, C>;
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(p.warps_per_cta * 32);
+  cfg.blockDim = dim3((p.warps_per_cta + 1) * 32);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];

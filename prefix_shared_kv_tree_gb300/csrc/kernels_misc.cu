@@ -105,20 +105,25 @@ __global__ void __launch_bounds__(256) gather_kernel(const ScatterParams p, int 
 // ---------------------------------------------------------------------------
 template <typename T, int D>
 __global__ void __launch_bounds__(128) merge_kernel(const AttnParams p, int B) {
-  if (p.pdl) ptx::pdl_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int pair = blockIdx.x * 4 + warp;
-  if (pair >= B * p.Hkv) return;
-  const int u = pair / p.Hkv, kv = pair % p.Hkv;
-  for (int hg = 0; hg < p.g; ++hg) merge_row<T, D>(p, u, kv, hg, lane);
+  const int task = blockIdx.x * 4 + warp;  // output row: (u * Hkv + kv) * g + hg
+  const bool live = task < B * p.Hq;
+  int e0 = 0, e1 = 0;
+  if (live) {  // the merge table was uploaded before the attention kernels ran
+    const int key = task / p.g;
+    e0 = __ldg(p.m_off + key);
+    e1 = __ldg(p.m_off + key + 1);
+  }
+  if (p.pdl) ptx::pdl_wait();
+  if (live) merge_row<T, D>(p, task, e0, e1, lane);
 }
 
 template <typename T>
 cudaError_t launch_merge_t(int D, const AttnParams& p, int B, cudaStream_t s) {
-  const int pairs = B * p.Hkv;
-  if (pairs == 0) return cudaSuccess;
+  const int tasks = B * p.Hq;
+  if (tasks == 0) return cudaSuccess;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((pairs + 3) / 4);
+  cfg.gridDim = dim3((tasks + 3) / 4);
   cfg.blockDim = dim3(128);
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
@@ -146,6 +151,8 @@ bool simt_supported(int dtype, int D, int g) {
   return (dtype == kF16 || dtype == kBF16 || dtype == kF32) && (D == 64 || D == 128) &&
          (g == 1 || g == 2 || g == 4 || g == 8);
 }
+
+int attn_simt_max_warps(int g) { return simt_max_warps(g); }
 
 size_t attn_simt_smem(int dtype, int D, int C, int g, int stages, int warps_per_cta) {
   return simt_warp_bytes(C, D, g, stages, dtype_size(dtype)) * warps_per_cta;

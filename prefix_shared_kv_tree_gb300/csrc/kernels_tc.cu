@@ -289,6 +289,7 @@ __global__ void __launch_bounds__(224, 1) attn_tc_kernel(const AttnParams p) {
         hg = rr % p.g;
       }
       const int key_limit = (p.causal_p0 >= 0 && row_valid) ? p.causal_p0 + grp + 1 : INT_MAX;
+      const int part_row = (row_valid && !p.final_mode) ? __ldg(p.row_idx + w.part_base + r) : 0;
       float o[D];
 #pragma unroll
       for (int i = 0; i < D; ++i) o[i] = 0.f;
@@ -399,7 +400,7 @@ __global__ void __launch_bounds__(224, 1) attn_tc_kernel(const AttnParams p) {
             *reinterpret_cast<uint4*>(out + 8 * j) = pk;
           }
         } else {
-          const size_t prow_i = static_cast<size_t>(w.part_base) + r;
+          const size_t prow_i = static_cast<size_t>(part_row);
           float4* po = reinterpret_cast<float4*>(p.part_o + prow_i * D);
 #pragma unroll
           for (int j = 0; j < D / 4; ++j) po[j] = make_float4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);

@@ -109,9 +109,15 @@ struct pst_pool {
   double last_rebuild_us = 0;
   std::vector<int64_t> batch;  // live ids in batch order
   std::vector<int32_t> h_tab;
-  size_t off_chunks = 0, off_tc = 0, off_tc_cta = 0, off_simt = 0, off_warp = 0, off_moff = 0, off_ment = 0;
+  size_t off_chunks = 0, off_tc = 0, off_tc_cta = 0, off_simt = 0, off_warp = 0, off_moff = 0, off_rows = 0;
   int32_t n_tc_items = 0, n_tc_ctas = 0, n_simt_items = 0, n_simt_warps = 0;
-  double tc_chunk_us = 0.5, simt_tile_us = 0.75;  // cost model for splitting SMs between the phases
+  // Cost model for splitting the SMs between the phases (GB300, 64-token
+  // chunks, head size 128): one chunk of one tensor-core item, the fixed cost
+  // of an item, one CUDA-core tile when the phases run on split SMs, the
+  // DRAM rate one SM of the CUDA-core kernel sustains, and the whole GPU's.
+  double tc_chunk_us = 1.4, tc_item_us = 1.0, simt_tile_us = 0.75, simt_sm_gbs = 60.0, hbm_gbs = 6500.0;
+  int32_t simt_unit = 0;      // CUDA-core work-item size in chunks; 0 = automatic
+  int32_t simt_max_ctas = 0;  // cap on the CUDA-core grid; 0 = one CTA per SM
   int32_t simt_grid = 0, simt_stages = 3, simt_wpc = 8;
   int64_t n_part_rows = 0, shared_chunks = 0;
   std::vector<int32_t> canon_shared;   // 4 per row
@@ -128,6 +134,7 @@ struct pst_pool {
   float* d_part_ml = nullptr;
   size_t part_cap = 0;  // rows
   int32_t* d_err = nullptr;
+  int32_t* d_sched = nullptr;  // work-claim counter of the CUDA-core kernel
   int32_t* d_pre = nullptr;
   size_t pre_cap = 0;
   int32_t* h_stage = nullptr;  // pinned upload staging
@@ -271,6 +278,24 @@ pst_status upload(pst_pool* p, int32_t** dbuf, size_t* dcap, const std::vector<i
   return PST_OK;
 }
 
+// Query rows are fetched with bulk async copies and outputs written with
+// 16-byte stores: both buffers must start on a 16-byte boundary.
+bool misaligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) != 0; }
+
+// CUDA-core work item (SimtItem): chunk ids inline for runs of up to
+// kSimtInline chunks, else the run's offset in the chunk-id list.
+void push_simt_item(std::vector<int32_t>& v, const std::vector<int32_t>& ids, int32_t off, int32_t n, int32_t kv,
+                    int32_t group0, int32_t part_base) {
+  static_assert(kSimtInline == 4, "inline chunk slots");
+  int32_t c[kSimtInline] = {0, 0, 0, 0};
+  if (n <= kSimtInline) {
+    for (int32_t x = 0; x < n; ++x) c[x] = ids[off + x];
+  } else {
+    c[0] = off;
+  }
+  v.insert(v.end(), {c[0], c[1], c[2], c[3], n, kv, group0, part_base});
+}
+
 void push_item(std::vector<int32_t>& v, const WorkItem& w) {
   const int32_t* x = reinterpret_cast<const int32_t*>(&w);
   v.insert(v.end(), x, x + 8);
@@ -348,9 +373,19 @@ pst_status rebuild(pst_pool* p) {
 
   std::vector<int32_t> chunks;
   std::vector<int32_t> tc_items, simt_items, warp_items;
-  std::vector<std::pair<int32_t, int32_t>> ment;  // (u*Hkv + kv, partial row base)
+  // Partial results, one entry per (batch row, KV head) pair and item that
+  // covers it.  The rows of one pair end up contiguous in entry order (slot
+  // e of the pair holds heads kv*g .. kv*g+g-1 at rows e*g ..), so the merge
+  // reads one contiguous block per pair.  An entry points back at its
+  // producer: a tensor-core row-index slot (rows of head 0 at tc_rows[pos]) or
+  // a CUDA-core item (x).
+  struct Entry {
+    int32_t key;  // u * Hkv + kv
+    int32_t pos;  // >= 0: index into tc_rows of head 0; < 0: -1 - CUDA-core item index
+  };
+  std::vector<Entry> ents;
+  std::vector<int32_t> tc_rows;  // tensor-core item row -> partial row
   std::vector<Stream> streams;
-  int64_t prow = 0;
 
   // ---- phase 1: chunk-first over the runs
   int64_t p1_iters = 0;
@@ -385,11 +420,11 @@ pst_status rebuild(pst_pool* p) {
             w.group0 = i;
             w.row0 = r0;
             w.n_rows = std::min(128, rows - r0);
-            w.part_base = static_cast<int32_t>(prow);
+            w.part_base = static_cast<int32_t>(tc_rows.size());
             push_item(tc_items, w);
             for (int32_t u = i + r0 / g; u < i + (r0 + w.n_rows) / g; ++u)
-              ment.emplace_back(u * Hkv + kv, static_cast<int32_t>(prow + (u - i) * g - r0));
-            prow += w.n_rows;
+              ents.push_back({u * Hkv + kv, static_cast<int32_t>(tc_rows.size()) + (u - i) * g - r0});
+            tc_rows.resize(tc_rows.size() + w.n_rows, 0);
           }
         }
       } else {
@@ -429,10 +464,33 @@ pst_status rebuild(pst_pool* p) {
     std::vector<double> cost(n);
     double w_tc = 0;
     for (int32_t x = 0; x < n; ++x) {
-      cost[x] = tc_items[8 * x + 1] * p->tc_chunk_us + p->tc_chunk_us;  // + one chunk's worth per item
+      cost[x] = tc_items[8 * x + 1] * p->tc_chunk_us + p->tc_item_us;
       w_tc += cost[x];
     }
+    const double max_cost = *std::max_element(cost.begin(), cost.end());
     int32_t k = std::min(p->n_sm, n);
+    if (!concurrent && T > 0 && p->n_sm > 1) {
+      // The sequence-first kernel is launched right behind this one
+      // (programmatic dependent launch) and starts on the SMs this kernel
+      // leaves free; its CTAs claim work dynamically, so those that start
+      // late, on SMs this kernel releases, just take less.  The chunk-first
+      // phase is compute-bound, the sequence-first phase DRAM-bound: pick the
+      // k that minimises the modelled end time of both (with 20% margin on the
+      // chunk-first estimate, fewer SMs on ties).
+      const double simt_bytes = static_cast<double>(T) * p->tile_bytes;
+      const double hbm = p->hbm_gbs * 1e3, per_sm = p->simt_sm_gbs * 1e3;  // bytes per microsecond
+      double best = 1e300;
+      for (int32_t kk = 1; kk <= std::min(p->n_sm, n); ++kk) {
+        const double t_tc = 1.2 * std::max(w_tc / kk, max_cost);
+        const double r = std::min(hbm, (p->n_sm - kk) * per_sm);
+        const double done = r * t_tc;
+        const double t = done >= simt_bytes ? std::max(t_tc, simt_bytes / r) : t_tc + (simt_bytes - done) / hbm;
+        if (t < best * (1.0 - 1e-9)) {
+          best = t;
+          k = kk;
+        }
+      }
+    }
     if (concurrent && p->n_sm > 1) {
       const double w_simt = static_cast<double>(T) * p->simt_tile_us;
       k = static_cast<int32_t>(std::lround(p->n_sm * w_tc / (w_tc + w_simt)));
@@ -458,61 +516,54 @@ pst_status rebuild(pst_pool* p) {
     p->n_tc_ctas = k;
   }
 
-  // ---- split the CUDA-core tile streams evenly over all warps of the grid
-  const int64_t warps_needed = std::max<int64_t>(1, ceil_div(T, 2));
+  // ---- cut the CUDA-core tile streams into work items that warps claim at
+  // run time: items of about T / (8 W) chunks (W = warps in the grid), the
+  // largest claimed first, and the last ~2W chunks as single-chunk items so the
+  // kernel ends evenly.
   const int32_t simt_sms = (p->n_tc_ctas > 0 && (p->cfg.flags & PST_FLAG_CONCURRENT_PHASES))
                                ? std::max(1, p->n_sm - p->n_tc_ctas)
                                : p->n_sm;
-  p->simt_grid = static_cast<int32_t>(std::min<int64_t>(simt_sms, ceil_div(warps_needed, p->simt_wpc)));
+  p->simt_grid = static_cast<int32_t>(std::min<int64_t>(simt_sms, std::max<int64_t>(1, ceil_div(T, p->simt_wpc))));
+  if (p->simt_max_ctas > 0) p->simt_grid = std::min(p->simt_grid, p->simt_max_ctas);
   p->n_simt_warps = p->simt_grid * p->simt_wpc;
-  const int64_t W = p->n_simt_warps;
-  warp_items.assign(W + 1, 0);
   {
-    int64_t t_base = 0;  // global index of the current stream's first tile
-    size_t si = 0;
-    int64_t wcur = 0;
-    int32_t item_count = 0;
-    for (int64_t w = 0; w < W; ++w) {
-      warp_items[w] = item_count;
-      const int64_t lo = w * T / W, hi = (w + 1) * T / W;
-      int64_t t = lo;
-      while (t < hi) {
-        while (si < streams.size() && t_base + streams[si].n <= t) {
-          t_base += streams[si].n;
-          ++si;
-        }
-        const Stream& st = streams[si];
-        const int64_t a = t - t_base;
-        const int64_t b = std::min<int64_t>(st.n, hi - t_base);
-        WorkItem it{};
-        it.chunk_off = st.chunk_off + static_cast<int32_t>(a);
-        it.n_chunks = static_cast<int32_t>(b - a);
-        it.kv = st.kv;
-        it.group0 = st.group;
-        it.row0 = 0;
-        it.n_rows = g;
-        it.part_base = static_cast<int32_t>(prow);
-        push_item(simt_items, it);
-        ment.emplace_back(st.group * Hkv + st.kv, static_cast<int32_t>(prow));
-        prow += g;
-        ++item_count;
-        t = t_base + b;
-      }
-      wcur = w;
+    const int64_t W = p->n_simt_warps;
+    const int32_t unit = std::min<int32_t>(
+        kSimtInline, p->simt_unit > 0 ? p->simt_unit : static_cast<int32_t>(std::max<int64_t>(1, T / (8 * W))));
+    std::vector<Stream> units;
+    for (const auto& st : streams)
+      for (int32_t a = 0; a < st.n; a += unit) units.push_back({st.chunk_off + a, std::min(unit, st.n - a), st.kv, st.group});
+    std::stable_sort(units.begin(), units.end(), [](const Stream& x, const Stream& y) { return x.n > y.n; });
+    int64_t tail = 0;
+    size_t cut = units.size();
+    while (cut > 0 && tail < 2 * W) tail += units[--cut].n;
+    std::vector<Stream> ordered(units.begin(), units.begin() + cut);
+    for (size_t x = cut; x < units.size(); ++x)
+      for (int32_t a = 0; a < units[x].n; ++a) ordered.push_back({units[x].chunk_off + a, 1, units[x].kv, units[x].group});
+    for (const auto& un : ordered) {
+      ents.push_back({un.group * Hkv + un.kv, -1 - static_cast<int32_t>(simt_items.size() / 8)});
+      push_simt_item(simt_items, chunks, un.chunk_off, un.n, un.kv, un.group, 0);
     }
-    (void)wcur;
-    warp_items[W] = item_count;
+    warp_items.assign(1, 0);
   }
   p->n_simt_items = static_cast<int32_t>(simt_items.size() / 8);
-  p->n_part_rows = prow;
+  p->n_part_rows = static_cast<int64_t>(ents.size()) * g;
 
-  // ---- merge CSR per (batch row, KV head), emission order kept
-  std::vector<int32_t> moff(static_cast<size_t>(B) * Hkv + 1, 0), ments(ment.size());
-  for (const auto& e : ment) moff[e.first + 1]++;
+  // ---- merge CSR per (batch row, KV head): entry slots in emission order,
+  // and each producer told its rows
+  std::vector<int32_t> moff(static_cast<size_t>(B) * Hkv + 1, 0);
+  for (const auto& e : ents) moff[e.key + 1]++;
   for (size_t x = 1; x < moff.size(); ++x) moff[x] += moff[x - 1];
   {
     std::vector<int32_t> fill(moff.begin(), moff.end() - 1);
-    for (const auto& e : ment) ments[fill[e.first]++] = e.second;
+    for (const auto& e : ents) {
+      const int32_t slot = fill[e.key]++;
+      if (e.pos >= 0) {
+        for (int hg = 0; hg < g; ++hg) tc_rows[e.pos + hg] = slot * g + hg;
+      } else {
+        simt_items[8 * static_cast<size_t>(-1 - e.pos) + 7] = slot * g;
+      }
+    }
   }
 
   // ---- pack the table image
@@ -525,14 +576,15 @@ pst_status rebuild(pst_pool* p) {
   t.insert(t.end(), tc_items.begin(), tc_items.end());
   p->off_tc_cta = t.size();
   t.insert(t.end(), tc_cta_off.begin(), tc_cta_off.end());
+  while (t.size() % 4) t.push_back(0);  // SimtItem: 16-byte alignment
   p->off_simt = t.size();
   t.insert(t.end(), simt_items.begin(), simt_items.end());
   p->off_warp = t.size();
   t.insert(t.end(), warp_items.begin(), warp_items.end());
   p->off_moff = t.size();
   t.insert(t.end(), moff.begin(), moff.end());
-  p->off_ment = t.size();
-  t.insert(t.end(), ments.begin(), ments.end());
+  p->off_rows = t.size();
+  t.insert(t.end(), tc_rows.begin(), tc_rows.end());
   if (t.empty()) t.push_back(0);
 
   p->rebuild_count++;
@@ -590,6 +642,7 @@ AttnParams base_params(const pst_pool* p) {
   a.stages = p->simt_stages;
   a.warps_per_cta = p->simt_wpc;
   a.err = p->d_err;
+  a.sched = p->d_sched;
   return a;
 }
 
@@ -637,9 +690,18 @@ pst_status pst_pool_create(const pst_config* cfg, int device, pst_pool** out) {
 
   if (const char* e = std::getenv("PST_TC_CHUNK_US")) p->tc_chunk_us = std::atof(e);
   if (const char* e = std::getenv("PST_SIMT_TILE_US")) p->simt_tile_us = std::atof(e);
-  // CUDA-core kernel shape: 8 warps x 3 piece stages when it fits
-  p->simt_wpc = 8;
-  p->simt_stages = 3;
+  if (const char* e = std::getenv("PST_TC_ITEM_US")) p->tc_item_us = std::atof(e);
+  if (const char* e = std::getenv("PST_SIMT_SM_GBS")) p->simt_sm_gbs = std::atof(e);
+  if (const char* e = std::getenv("PST_HBM_GBS")) p->hbm_gbs = std::atof(e);
+  if (const char* e = std::getenv("PST_SIMT_UNIT")) p->simt_unit = std::atoi(e);
+  // CUDA-core kernel shape: up to 8 consumer warps (plus the producer warp)
+  // x 6 stages of 4 KB pieces, as far as shared memory allows
+  p->simt_wpc = attn_simt_max_warps(g);
+  p->simt_stages = 6;
+  if (const char* e = std::getenv("PST_SIMT_WPC"))
+    p->simt_wpc = std::max(1, std::min(attn_simt_max_warps(g), std::atoi(e)));
+  if (const char* e = std::getenv("PST_SIMT_STAGES")) p->simt_stages = std::max(2, std::min(16, std::atoi(e)));
+  if (const char* e = std::getenv("PST_SIMT_SMS")) p->simt_max_ctas = std::max(1, std::atoi(e));
   while (attn_simt_smem(c.dtype, p->D, p->C, g, p->simt_stages, p->simt_wpc) > 220 * 1024) {
     if (p->simt_stages > 2) p->simt_stages--;
     else p->simt_wpc--;
@@ -664,6 +726,7 @@ pst_status pst_pool_create(const pst_config* cfg, int device, pst_pool** out) {
     if ((e = cudaMemset(p->d_chunk_len, 0, sizeof(int32_t) * c.max_chunks)) != cudaSuccess) return bail(e, "cudaMemset");
     if ((e = cudaMalloc(&p->d_err, sizeof(int32_t))) != cudaSuccess) return bail(e, "cudaMalloc");
     if ((e = cudaMemset(p->d_err, 0, sizeof(int32_t))) != cudaSuccess) return bail(e, "cudaMemset");
+    if ((e = cudaMalloc(&p->d_sched, 256)) != cudaSuccess) return bail(e, "cudaMalloc");
     if ((e = cudaStreamCreateWithFlags(&p->aux, cudaStreamNonBlocking)) != cudaSuccess) return bail(e, "stream");
     if ((e = cudaEventCreateWithFlags(&p->ev_fork, cudaEventDisableTiming)) != cudaSuccess) return bail(e, "event");
     if ((e = cudaEventCreateWithFlags(&p->ev_join, cudaEventDisableTiming)) != cudaSuccess) return bail(e, "event");
@@ -687,6 +750,7 @@ pst_status pst_pool_free(pst_pool* p) {
     cudaFree(p->d_part_o);
     cudaFree(p->d_part_ml);
     cudaFree(p->d_err);
+    cudaFree(p->d_sched);
     cudaFree(p->d_pre);
     cudaFree(p->d_q);
     cudaFree(p->d_out);
@@ -842,6 +906,7 @@ static pst_status decode_impl(pst_pool* p, const void* q, void* out, cudaStream_
   const int32_t B = static_cast<int32_t>(p->batch.size());
   if (B == 0) return PST_OK;
   if (!q || !out) return fail(PST_ERR_INVALID, "null q/out with %d live sequences", B);
+  if (misaligned16(q) || misaligned16(out)) return fail(PST_ERR_INVALID, "q and out must be 16-byte aligned");
   st = sync_device_tables(p, s);
   if (st != PST_OK) return st;
   AttnParams a = base_params(p);
@@ -851,10 +916,11 @@ static pst_status decode_impl(pst_pool* p, const void* q, void* out, cudaStream_
   a.part_ml = p->d_part_ml;
   a.chunks = p->d_tab + p->off_chunks;
   a.m_off = p->d_tab + p->off_moff;
-  a.m_ent = p->d_tab + p->off_ment;
+  a.row_idx = p->d_tab + p->off_rows;
   const bool fork = p->n_tc_items > 0 && p->n_simt_items > 0 && (p->cfg.flags & PST_FLAG_CONCURRENT_PHASES);
   cudaStream_t s1 = fork ? p->aux : s;
   if (p->profiling) CUDA_TRY(cudaEventRecord(p->pev[4], s));
+  if (p->n_simt_items > 0) CUDA_TRY(cudaMemsetAsync(p->d_sched, 0, sizeof(int32_t), s));
   if (fork) {
     CUDA_TRY(cudaEventRecord(p->ev_fork, s));
     CUDA_TRY(cudaStreamWaitEvent(p->aux, p->ev_fork, 0));
@@ -875,8 +941,6 @@ static pst_status decode_impl(pst_pool* p, const void* q, void* out, cudaStream_
     AttnParams a2 = a;
     a2.items = reinterpret_cast<const WorkItem*>(p->d_tab + p->off_simt);
     a2.n_items = p->n_simt_items;
-    a2.warp_items = p->d_tab + p->off_warp;
-    a2.n_warps = p->n_simt_warps;
     if (p->profiling) CUDA_TRY(cudaEventRecord(p->pev[2], s));
     a2.pdl = (p->n_tc_items > 0 && !fork) ? 1 : 0;
     cudaError_t e = launch_attn_simt(p->cfg.dtype, p->D, p->C, p->g, a2, p->simt_grid, s);
@@ -909,9 +973,9 @@ pst_status pst_decode_attention(pst_pool* p, const void* q, void* out, void* str
   return decode_impl(p, q, out, static_cast<cudaStream_t>(stream));
 }
 
-// Decode attention without any allocation: the partial rows go to the
-// library's fixed device scratch instead of the pool's own buffers.  Only
-// launches kernels on `stream`.
+// Decode attention without any allocation: the partial rows and the work
+// counter go to the library's fixed device scratch instead of the pool's own
+// buffers.  Only a 4-byte memset and kernel launches on `stream`.
 pst_status pst_decode_attention_noalloc(pst_pool* p, const void* q, void* out, void* stream) {
   pst_status st = need_device(p);
   if (st != PST_OK) return st;
@@ -922,10 +986,12 @@ pst_status pst_decode_attention_noalloc(pst_pool* p, const void* q, void* out, v
   const int32_t B = static_cast<int32_t>(p->batch.size());
   if (B == 0) return PST_OK;
   if (!q || !out) return fail(PST_ERR_INVALID, "null q/out with %d live sequences", B);
+  if (misaligned16(q) || misaligned16(out)) return fail(PST_ERR_INVALID, "q and out must be 16-byte aligned");
   auto align256 = [](size_t x) { return (x + 255) / 256 * 256; };
+  const size_t sched_bytes = 256;  // the CUDA-core kernel's work-claim counter
   const size_t ml_bytes = align256(static_cast<size_t>(p->n_part_rows) * 2 * sizeof(float));
   const size_t o_bytes = static_cast<size_t>(p->n_part_rows) * p->D * sizeof(float);
-  const size_t need = ml_bytes + o_bytes;
+  const size_t need = sched_bytes + ml_bytes + o_bytes;
   if (need > kStaticScratchBytes)
     return fail(PST_ERR_INVALID, "this batch needs %zu bytes of scratch; the fixed area holds %zu", need,
                 kStaticScratchBytes);
@@ -937,11 +1003,13 @@ pst_status pst_decode_attention_noalloc(pst_pool* p, const void* q, void* out, v
   AttnParams a = base_params(p);
   a.q = q;
   a.out = out;
-  a.part_ml = reinterpret_cast<float*>(b8);
-  a.part_o = reinterpret_cast<float*>(b8 + ml_bytes);
+  a.sched = reinterpret_cast<int32_t*>(b8);  // must start at zero: cleared below
+  a.part_ml = reinterpret_cast<float*>(b8 + sched_bytes);
+  a.part_o = reinterpret_cast<float*>(b8 + sched_bytes + ml_bytes);
+  CUDA_TRY(cudaMemsetAsync(a.sched, 0, sizeof(int32_t), s));
   a.chunks = p->d_tab + p->off_chunks;
   a.m_off = p->d_tab + p->off_moff;
-  a.m_ent = p->d_tab + p->off_ment;
+  a.row_idx = p->d_tab + p->off_rows;
   if (p->n_tc_items > 0) {
     AttnParams a1 = a;
     a1.items = reinterpret_cast<const WorkItem*>(p->d_tab + p->off_tc);
@@ -954,8 +1022,6 @@ pst_status pst_decode_attention_noalloc(pst_pool* p, const void* q, void* out, v
     AttnParams a2 = a;
     a2.items = reinterpret_cast<const WorkItem*>(p->d_tab + p->off_simt);
     a2.n_items = p->n_simt_items;
-    a2.warp_items = p->d_tab + p->off_warp;
-    a2.n_warps = p->n_simt_warps;
     a2.pdl = p->n_tc_items > 0 ? 1 : 0;
     e = launch_attn_simt(p->cfg.dtype, p->D, p->C, p->g, a2, p->simt_grid, s);
     if (e != cudaSuccess) return fail(PST_ERR_CUDA, "sequence-first launch: %s", cudaGetErrorString(e));
@@ -998,6 +1064,7 @@ pst_status pst_prefill_attend(pst_pool* p, int64_t seq_id, const int32_t* tokens
   pst_status st = need_device(p);
   if (st != PST_OK) return st;
   if (!tokens || W < 1 || !q || !k_new || !v_new || !out) return fail(PST_ERR_INVALID, "bad argument");
+  if (misaligned16(q) || misaligned16(out)) return fail(PST_ERR_INVALID, "q and out must be 16-byte aligned");
   auto it = p->seqs.find(seq_id);
   if (it == p->seqs.end()) return fail(PST_ERR_NOT_FOUND, "unknown sequence %lld", (long long)seq_id);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -1061,15 +1128,10 @@ pst_status pst_prefill_attend(pst_pool* p, int64_t seq_id, const int32_t* tokens
         ++n_items;
       }
   } else {
+    const std::vector<int32_t> ids(tab.begin(), tab.begin() + off_items);
     for (int64_t t = 0; t < W; ++t)
       for (int kv = 0; kv < Hkv; ++kv) {
-        WorkItem w{};
-        w.chunk_off = 0;
-        w.kv = kv;
-        w.group0 = static_cast<int32_t>(t);
-        w.n_rows = g;
-        w.n_chunks = static_cast<int32_t>(ceil_div(p0 + t + 1, p->C));
-        push_item(tab, w);
+        push_simt_item(tab, ids, 0, static_cast<int32_t>(ceil_div(p0 + t + 1, p->C)), kv, static_cast<int32_t>(t), 0);
         ++n_items;
       }
   }
@@ -1096,9 +1158,9 @@ pst_status pst_prefill_attend(pst_pool* p, int64_t seq_id, const int32_t* tokens
   if (p->use_tc) {
     e = launch_attn_tc(p->cfg.dtype, p->D, a, n_items, s);
   } else {
-    a.warp_items = p->d_pre + off_warp;
-    a.n_warps = n_warps;
-    e = launch_attn_simt(p->cfg.dtype, p->D, p->C, g, a, grid, s);
+    CUDA_TRY(cudaMemsetAsync(p->d_sched, 0, sizeof(int32_t), s));
+    (void)n_warps;
+    e = launch_attn_simt(p->cfg.dtype, p->D, p->C, g, a, std::min<int32_t>(grid, p->n_sm), s);
   }
   if (e != cudaSuccess) return fail(PST_ERR_CUDA, "prefill launch: %s", cudaGetErrorString(e));
   return PST_OK;

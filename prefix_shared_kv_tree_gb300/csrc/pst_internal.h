@@ -47,19 +47,34 @@ struct WorkItem {
   int32_t group0;
   int32_t row0;
   int32_t n_rows;
-  int32_t part_base;  // partial-result row of r = 0 (partial mode)
+  int32_t part_base;  // partial mode: row r's partial row is row_idx[part_base + r]
   int32_t pad;
 };
 static_assert(sizeof(WorkItem) == 32, "WorkItem layout");
+
+// Work item of the CUDA-core kernel: a run of chunks of one (batch row, KV
+// head).  Runs of up to kSimtInline chunks carry their pool chunk ids in the
+// item itself, so one 32-byte load tells a warp everything it needs to stage
+// the run; longer runs (prefill) keep their ids in the chunk-id list.
+constexpr int kSimtInline = 4;
+struct alignas(16) SimtItem {
+  int32_t chunk[kSimtInline];  // n_chunks <= kSimtInline: chunk ids; else chunk[0] = first entry in the id list
+  int32_t n_chunks;            // 0 only in the kernel's "no more work" sentinel
+  int32_t kv;
+  int32_t group0;              // batch row (decode) or query position (prefill)
+  int32_t part_base;           // partial-result row of head 0 (partial mode)
+};
+static_assert(sizeof(SimtItem) == 32, "SimtItem layout");
 
 struct AttnParams {
   const uint8_t* pool;        // chunk slab
   const int32_t* chunk_len;   // valid tokens of each physical chunk
   const int32_t* chunks;      // chunk-id lists
-  const WorkItem* items;
-  const int32_t* warp_items;  // CUDA-core kernel: item range [warp_items[w], warp_items[w+1]) of warp w
+  const WorkItem* items;      // tensor-core kernel items, or the CUDA-core kernel's SimtItem array
+  const int32_t* warp_items;  // tensor-core kernel: item range [warp_items[c], warp_items[c+1]) of CTA c
+  int32_t* sched;             // CUDA-core kernel: next unclaimed item (zero at launch)
   int32_t n_items;
-  int32_t n_warps;            // CUDA-core kernel: warps in the grid
+  int32_t n_warps;            // unused
   const void* q;              // [groups][Hq][D]
   void* out;                  // final mode: [groups][Hq][D]
   float* part_o;              // partial mode: [rows][D]
@@ -72,9 +87,11 @@ struct AttnParams {
   int32_t stages;             // CUDA-core kernel: piece stages per warp
   int32_t warps_per_cta;      // CUDA-core kernel
   int32_t* err;               // device error word
-  // merge CSR of partial rows per (batch row, KV head) (read by the merge)
+  // Partial rows are grouped per (batch row, KV head) pair: entry e of the
+  // pair (m_off[key] <= e < m_off[key + 1], key = u * Hkv + kv) holds head
+  // kv*g + hg at row e*g + hg.
   const int32_t* m_off;       // [B * Hkv + 1]
-  const int32_t* m_ent;       // partial row of head kv*g + 0 for each entry
+  const int32_t* row_idx;     // tensor-core kernel: partial row of item row r at row_idx[item.part_base + r]
   // 1: launched as a programmatic dependent of the previous kernel on the
   // stream (it may start while that kernel drains; it must not finish first)
   int32_t pdl;
@@ -117,6 +134,7 @@ cudaError_t launch_scatter(int dtype, int D, int C, const ScatterParams& p, cuda
 cudaError_t launch_gather(int dtype, int D, int C, const ScatterParams& p, cudaStream_t s);
 cudaError_t launch_attn_simt(int dtype, int D, int C, int g, const AttnParams& p, int grid, cudaStream_t s);
 size_t attn_simt_smem(int dtype, int D, int C, int g, int stages, int warps_per_cta);
+int attn_simt_max_warps(int g);  // consumer warps per CTA of the CUDA-core kernel, at most
 // per-dtype launchers (one translation unit each)
 cudaError_t launch_attn_simt_f16(int D, int C, int g, const AttnParams& p, int grid, cudaStream_t s);
 cudaError_t launch_attn_simt_bf16(int D, int C, int g, const AttnParams& p, int grid, cudaStream_t s);
