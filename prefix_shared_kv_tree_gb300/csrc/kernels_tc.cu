@@ -212,40 +212,47 @@ __global__ void __launch_bounds__(224, 1) attn_tc_kernel(const AttnParams p) {
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // The whole warp runs this loop (operands stay warp-uniform); one
+    // elected lane issues each tcgen05 instruction.
+    {
       const uint32_t q_addr = ptx::smem_u32(qs);
       const uint32_t kv_addr = ptx::smem_u32(kvs);
       const uint32_t p_addr = ptx::smem_u32(ps);
+      auto wait_all = [&](uint64_t* bar, uint32_t parity) {
+        return __all_sync(0xffffffffu, ptx::mbar_wait(bar, parity, abort_flag, p.err));
+      };
       auto issue_s = [&](int t, int qb) -> bool {
         const int s = t % kNS, b = t & 1;
-        if (!ptx::mbar_wait(&full[s], (t / kNS) & 1, abort_flag, p.err)) return false;
-        *consumed_slot = t + 1;
-        if (t >= 2 && !ptx::mbar_wait(&sfree[b], ((t - 2) >> 1) & 1, abort_flag, p.err)) return false;
+        if (!wait_all(&full[s], (t / kNS) & 1)) return false;
+        if (lane == 0) *consumed_slot = t + 1;
+        if (t >= 2 && !wait_all(&sfree[b], ((t - 2) >> 1) & 1)) return false;
         ptx::tc_fence_after();
+        // Descriptors of each K step = the tile's base descriptor + the step's
+        // byte offset / 16 (the 14-bit start-address field never carries).
+        const uint64_t a0 = ptx::smem_desc_sw128(q_addr + qb * QB, 1024);
+        const uint64_t b0 = ptx::smem_desc_sw128(kv_addr + s * TILE, 1024);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           // K step kk covers features [16kk, 16kk+16): column block kk/4, 32-byte offset (kk%4)
-          const uint32_t koff = (kk & 3) * 32;
-          const uint64_t a = ptx::smem_desc_sw128(q_addr + qb * QB + (kk >> 2) * (kBM * 128) + koff, 1024);
-          const uint64_t bd = ptx::smem_desc_sw128(kv_addr + s * TILE + (kk >> 2) * (kC * 128) + koff, 1024);
-          ptx::mma_f16(tbase + S_COL + b * kC, a, bd, ID_S, kk > 0 ? 1u : 0u);
+          constexpr uint32_t kA = kBM * 128 / 16, kB = kC * 128 / 16;
+          const uint64_t da = (kk >> 2) * kA + (kk & 3) * 2, db = (kk >> 2) * kB + (kk & 3) * 2;
+          ptx::mma_f16_warp(tbase + S_COL + b * kC, a0 + da, b0 + db, ID_S, kk > 0 ? 1u : 0u);
         }
-        ptx::mma_commit(&sfull[b]);
+        ptx::mma_commit_warp(&sfull[b]);
         return true;
       };
       auto issue_pv = [&](int t) -> bool {
         const int s = t % kNS, b = t & 1;
-        if (!ptx::mbar_wait(&pfull[b], (t >> 1) & 1, abort_flag, p.err)) return false;
-        if (t >= 2 && !ptx::mbar_wait(&ofree[b], ((t - 2) >> 1) & 1, abort_flag, p.err)) return false;
+        if (!wait_all(&pfull[b], (t >> 1) & 1)) return false;
+        if (t >= 2 && !wait_all(&ofree[b], ((t - 2) >> 1) & 1)) return false;
         ptx::tc_fence_after();
+        const uint64_t a0 = ptx::smem_desc_sw128(p_addr + b * PB, 1024);
+        const uint64_t b0 = ptx::smem_desc_sw128(kv_addr + s * TILE + HALF, 1024);
 #pragma unroll
-        for (int kk = 0; kk < kC / 16; ++kk) {
-          const uint64_t a = ptx::smem_desc_sw128(p_addr + b * PB + kk * 32, 1024);
-          const uint64_t bd = ptx::smem_desc_sw128(kv_addr + s * TILE + HALF + kk * 32, 1024);
-          ptx::mma_f16(tbase + O_COL + b * D, a, bd, ID_O, kk > 0 ? 1u : 0u);
-        }
-        ptx::mma_commit(&ofull[b]);
-        ptx::mma_commit(&empty[s]);
+        for (int kk = 0; kk < kC / 16; ++kk)
+          ptx::mma_f16_warp(tbase + O_COL + b * D, a0 + kk * 2, b0 + kk * 2, ID_O, kk > 0 ? 1u : 0u);
+        ptx::mma_commit_warp(&ofull[b]);
+        ptx::mma_commit_warp(&empty[s]);
         return true;
       };
       int t = 0;
@@ -253,7 +260,7 @@ __global__ void __launch_bounds__(224, 1) attn_tc_kernel(const AttnParams p) {
       for (int ii = i0; ii < i1 && ok; ++ii) {
         const int it = ii - i0, qb = it & 1;
         const int nk = p.items[ii].n_chunks;
-        ok = ptx::mbar_wait(&qfull[qb], (it >> 1) & 1, abort_flag, p.err);
+        ok = wait_all(&qfull[qb], (it >> 1) & 1);
         if (!ok) break;
         ptx::tc_fence_after();
         ok = issue_s(t, qb);
@@ -261,13 +268,13 @@ __global__ void __launch_bounds__(224, 1) attn_tc_kernel(const AttnParams p) {
           if (c + 1 < nk) {
             ok = issue_s(t + 1, qb);
           } else {
-            ptx::mma_commit(&qfree[qb]);  // every S of this item is issued
+            ptx::mma_commit_warp(&qfree[qb]);  // every S of this item is issued
           }
           if (ok) ok = issue_pv(t);
         }
       }
       // Every MMA of this CTA must have finished before TMEM is released.
-      ptx::mma_commit(done);
+      ptx::mma_commit_warp(done);
       ptx::mbar_wait(done, 0, nullptr, p.err);
     }
     __syncwarp();
