@@ -92,7 +92,7 @@ __global__ void __launch_bounds__(224, 1) attn_tc_kernel(const AttnParams p) {
   constexpr int CCH = kC / 8;   // 16-byte chunks per row when the reduction runs over keys
   constexpr uint32_t TMEM_COLS = (128 + 2 * D) <= 256 ? 256u : 512u;
   constexpr uint32_t S_COL = 0;    // S double buffer: columns [0, 64), [64, 128)
-  constexpr uint32_t O_COL = 128;  // O double buffer: [128, 128 + D), [128 + D, 128 + 2D)
+  constexpr uint32_t O_COL = 128;  // O of an item, double-buffered by item: [128, 128 + D), [128 + D, 128 + 2D)
   constexpr bool BF = std::is_same<T, __nv_bfloat16>::value;
   constexpr uint32_t ID_S = ptx::idesc_f16(kBM, kC, BF);
   constexpr uint32_t ID_O = ptx::idesc_f16(kBM, D, BF);
@@ -109,10 +109,11 @@ __global__ void __launch_bounds__(224, 1) attn_tc_kernel(const AttnParams p) {
   uint64_t* qfree = qfull + 2;       // [2] Q tile no longer read by the tensor cores
   uint64_t* sfull = qfree + 2;       // [2] S ready in TMEM
   uint64_t* sfree = sfull + 2;       // [2] S read by the softmax threads (128)
-  uint64_t* pfull = sfree + 2;       // [2] P written (128)
-  uint64_t* ofull = pfull + 2;       // [2] O_k ready in TMEM
-  uint64_t* ofree = ofull + 2;       // [2] O_k read (128)
-  uint64_t* done = ofree + 2;        // all MMAs of this CTA completed
+  uint64_t* pfull = sfree + 2;       // [2] P written, O rescaled if needed (128)
+  uint64_t* pfree = pfull + 2;       // [2] the PV product that read P buffer b has completed
+  uint64_t* ofull = pfree + 2;       // [2] every PV product of an item has completed (O buffer by item)
+  uint64_t* oempty = ofull + 2;      // [2] the item's O was read out (128)
+  uint64_t* done = oempty + 2;       // all MMAs of this CTA completed
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* issued_slot = abort_flag + 1;
@@ -135,8 +136,9 @@ __global__ void __launch_bounds__(224, 1) attn_tc_kernel(const AttnParams p) {
       ptx::mbar_init(&sfull[b], 1);
       ptx::mbar_init(&sfree[b], 128);
       ptx::mbar_init(&pfull[b], 128);
+      ptx::mbar_init(&pfree[b], 1);
       ptx::mbar_init(&ofull[b], 1);
-      ptx::mbar_init(&ofree[b], 128);
+      ptx::mbar_init(&oempty[b], 128);
     }
     ptx::mbar_init(done, 1);
     *abort_flag = 0;
@@ -241,18 +243,22 @@ __global__ void __launch_bounds__(224, 1) attn_tc_kernel(const AttnParams p) {
         ptx::mma_commit_warp(&sfull[b]);
         return true;
       };
-      auto issue_pv = [&](int t) -> bool {
-        const int s = t % kNS, b = t & 1;
+      // O += P V for chunk c of item it: accumulates in the item's TMEM buffer
+      // across its chunks (the softmax threads rescale it when their
+      // reference max moves); the first chunk overwrites.
+      auto issue_pv = [&](int t, int it, int c, bool last) -> bool {
+        const int s = t % kNS, b = t & 1, ob = it & 1;
         if (!wait_all(&pfull[b], (t >> 1) & 1)) return false;
-        if (t >= 2 && !wait_all(&ofree[b], ((t - 2) >> 1) & 1)) return false;
+        if (c == 0 && it >= 2 && !wait_all(&oempty[ob], ((it - 2) >> 1) & 1)) return false;
         ptx::tc_fence_after();
         const uint64_t a0 = ptx::smem_desc_sw128(p_addr + b * PB, 1024);
         const uint64_t b0 = ptx::smem_desc_sw128(kv_addr + s * TILE + HALF, 1024);
 #pragma unroll
         for (int kk = 0; kk < kC / 16; ++kk)
-          ptx::mma_f16_warp(tbase + O_COL + b * D, a0 + kk * 2, b0 + kk * 2, ID_O, kk > 0 ? 1u : 0u);
-        ptx::mma_commit_warp(&ofull[b]);
+          ptx::mma_f16_warp(tbase + O_COL + ob * D, a0 + kk * 2, b0 + kk * 2, ID_O, (c > 0 || kk > 0) ? 1u : 0u);
+        ptx::mma_commit_warp(&pfree[b]);
         ptx::mma_commit_warp(&empty[s]);
+        if (last) ptx::mma_commit_warp(&ofull[ob]);
         return true;
       };
       int t = 0;
@@ -270,7 +276,7 @@ __global__ void __launch_bounds__(224, 1) attn_tc_kernel(const AttnParams p) {
           } else {
             ptx::mma_commit_warp(&qfree[qb]);  // every S of this item is issued
           }
-          if (ok) ok = issue_pv(t);
+          if (ok) ok = issue_pv(t, it, c, c + 1 == nk);
         }
       }
       // Every MMA of this CTA must have finished before TMEM is released.
@@ -280,12 +286,18 @@ __global__ void __launch_bounds__(224, 1) attn_tc_kernel(const AttnParams p) {
     __syncwarp();
   } else if (warp >= 2 && warp <= 5) {
     // ------------------------------------------------- softmax / epilogue
+    // One thread per query row.  The item's O accumulates in TMEM; scores
+    // are exponentiated against a per-row reference max that only moves when
+    // a chunk's max exceeds it by more than kRescale (log2 units), so P stays
+    // below 2^kRescale and O (with the row sum) is rescaled rarely.
+    constexpr float kRescale = 8.f;
     const int quad = warp & 3;
     const int r = quad * 32 + lane;
     const uint32_t tl = tbase + (static_cast<uint32_t>(quad * 32) << 16);
     int t = 0;
     bool ok = true;
     for (int ii = i0; ii < i1 && ok; ++ii) {
+      const int it = ii - i0, ob = it & 1;
       const WorkItem w = p.items[ii];
       const int nk = w.n_chunks;
       const bool row_valid = r < w.n_rows;
@@ -297,10 +309,7 @@ __global__ void __launch_bounds__(224, 1) attn_tc_kernel(const AttnParams p) {
       }
       const int key_limit = (p.causal_p0 >= 0 && row_valid) ? p.causal_p0 + grp + 1 : INT_MAX;
       const int part_row = (row_valid && !p.final_mode) ? __ldg(p.row_idx + w.part_base + r) : 0;
-      float o[D];
-#pragma unroll
-      for (int i = 0; i < D; ++i) o[i] = 0.f;
-      float m = -INFINITY, l = 0.f, alpha_pend = 0.f;
+      float m = -INFINITY, l = 0.f;  // reference max, row sum relative to it
       int my_len = 0;
 
       for (int c = 0; c < nk; ++c, ++t) {
@@ -331,9 +340,38 @@ __global__ void __launch_bounds__(224, 1) attn_tc_kernel(const AttnParams p) {
           x[k2] = (k2 < lim) ? __uint_as_float(raw) * p.scale_log2 : -INFINITY;
           mx = fmaxf(mx, x[k2]);
         }
-        const float m_new = fmaxf(m, mx);
-        const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-        const float alpha = ptx::ex2(m - m_use);
+        // Move the reference max: always on the item's first chunk (nothing
+        // accumulated yet); later only when this chunk's max runs past it.
+        const bool move = (c == 0) || (mx > m + kRescale);
+        const float m_old_use = (m == -INFINITY) ? 0.f : m;
+        if (move) m = fmaxf(m, mx);
+        const float m_use = (m == -INFINITY) ? 0.f : m;
+        if (c > 0 && __any_sync(0xffffffffu, move)) {
+          // O so far (through chunk c-1) and l get the factor 2^(old - new):
+          // wait for that chunk's PV product, then rescale in place.
+          const float alpha = move ? ptx::ex2(m_old_use - m_use) : 1.f;
+          if (!ptx::mbar_wait(&pfree[(t - 1) & 1], ((t - 1) >> 1) & 1, abort_flag, p.err)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+#pragma unroll
+          for (int cg = 0; cg < D / 32; ++cg) {
+            uint32_t ov[32];
+            ptx::tmem_ld32(tl + O_COL + ob * D + 32 * cg, ov);
+            ptx::tmem_ld_wait(ov);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+            ptx::tmem_st32(tl + O_COL + ob * D + 32 * cg, ov);
+          }
+          ptx::tmem_st_wait();
+          l *= alpha;
+        }
+        // P buffer b is free once the PV product of chunk t-2 has completed.
+        if (t >= 2 && !ptx::mbar_wait(&pfree[b], ((t - 2) >> 1) & 1, abort_flag, p.err)) {
+          ok = false;
+          break;
+        }
         float psum = 0.f;
         uint8_t* prow = ps + b * PB;
 #pragma unroll
@@ -346,74 +384,48 @@ __global__ void __launch_bounds__(224, 1) attn_tc_kernel(const AttnParams p) {
           *reinterpret_cast<uint4*>(prow + r * 128 + ((j ^ (r & 7)) << 4)) = pk;
         }
         ptx::fence_proxy_async_smem();
+        ptx::tc_fence_before();  // orders any TMEM stores above before the PV product
         ptx::mbar_arrive(&pfull[b]);
-        l = l * alpha + psum;
-
-        if (c >= 1) {
-          const int b1 = (t - 1) & 1;
-          if (!ptx::mbar_wait(&ofull[b1], ((t - 1) >> 1) & 1, abort_flag, p.err)) {
-            ok = false;
-            break;
-          }
-          ptx::tc_fence_after();
-#pragma unroll
-          for (int cg = 0; cg < D / 32; ++cg) {
-            uint32_t ov[32];
-            ptx::tmem_ld32(tl + O_COL + b1 * D + 32 * cg, ov);
-            ptx::tmem_ld_wait(ov);
-#pragma unroll
-            for (int e = 0; e < 32; ++e) o[32 * cg + e] = fmaf(o[32 * cg + e], alpha_pend, __uint_as_float(ov[e]));
-          }
-          ptx::tc_fence_before();
-          ptx::mbar_arrive(&ofree[b1]);
-        }
-        alpha_pend = alpha;
-        m = m_new;
+        l += psum;
       }
       if (!ok) break;
 
-      // last chunk's O of the item
-      {
-        const int b1 = (t - 1) & 1;
-        if (!ptx::mbar_wait(&ofull[b1], ((t - 1) >> 1) & 1, abort_flag, p.err)) ok = false;
-        if (ok) {
-          ptx::tc_fence_after();
-#pragma unroll
-          for (int cg = 0; cg < D / 32; ++cg) {
-            uint32_t ov[32];
-            ptx::tmem_ld32(tl + O_COL + b1 * D + 32 * cg, ov);
-            ptx::tmem_ld_wait(ov);
-#pragma unroll
-            for (int e = 0; e < 32; ++e) o[32 * cg + e] = fmaf(o[32 * cg + e], alpha_pend, __uint_as_float(ov[e]));
-          }
-          ptx::tc_fence_before();
-          ptx::mbar_arrive(&ofree[b1]);
-        }
-      }
+      // ---- the item's O: wait for its last PV product, then write out
+      if (!ptx::mbar_wait(&ofull[ob], (it >> 1) & 1, abort_flag, p.err)) ok = false;
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
-
-      if (row_valid) {
-        if (p.final_mode) {
-          T* out = static_cast<T*>(p.out) + (static_cast<size_t>(grp) * p.Hq + w.kv * p.g + hg) * D;
-          const float inv = 1.f / l;
+      ptx::tc_fence_after();
+      const float inv = 1.f / l;
+      T* out = static_cast<T*>(p.out) + (static_cast<size_t>(grp) * p.Hq + w.kv * p.g + hg) * D;
+      float4* po = reinterpret_cast<float4*>(p.part_o + static_cast<size_t>(part_row) * D);
 #pragma unroll
-          for (int j = 0; j < DCH; ++j) {
-            uint4 pk;
-            pk.x = pack2_plain<T>(o[8 * j + 0] * inv, o[8 * j + 1] * inv);
-            pk.y = pack2_plain<T>(o[8 * j + 2] * inv, o[8 * j + 3] * inv);
-            pk.z = pack2_plain<T>(o[8 * j + 4] * inv, o[8 * j + 5] * inv);
-            pk.w = pack2_plain<T>(o[8 * j + 6] * inv, o[8 * j + 7] * inv);
-            *reinterpret_cast<uint4*>(out + 8 * j) = pk;
+      for (int cg = 0; cg < D / 32; ++cg) {
+        uint32_t ov[32];
+        ptx::tmem_ld32(tl + O_COL + ob * D + 32 * cg, ov);
+        ptx::tmem_ld_wait(ov);
+        if (row_valid) {
+          if (p.final_mode) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const float* o8 = reinterpret_cast<const float*>(ov) + 8 * j;
+              uint4 pk;
+              pk.x = pack2_plain<T>(o8[0] * inv, o8[1] * inv);
+              pk.y = pack2_plain<T>(o8[2] * inv, o8[3] * inv);
+              pk.z = pack2_plain<T>(o8[4] * inv, o8[5] * inv);
+              pk.w = pack2_plain<T>(o8[6] * inv, o8[7] * inv);
+              *reinterpret_cast<uint4*>(out + 32 * cg + 8 * j) = pk;
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              po[8 * cg + j] = make_float4(__uint_as_float(ov[4 * j]), __uint_as_float(ov[4 * j + 1]),
+                                           __uint_as_float(ov[4 * j + 2]), __uint_as_float(ov[4 * j + 3]));
           }
-        } else {
-          const size_t prow_i = static_cast<size_t>(part_row);
-          float4* po = reinterpret_cast<float4*>(p.part_o + prow_i * D);
-#pragma unroll
-          for (int j = 0; j < D / 4; ++j) po[j] = make_float4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
-          reinterpret_cast<float2*>(p.part_ml)[prow_i] = make_float2(m, l);
         }
       }
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(&oempty[ob]);
+      if (row_valid && !p.final_mode) reinterpret_cast<float2*>(p.part_ml)[part_row] = make_float2(m, l);
     }
   }
 
