@@ -19,15 +19,19 @@
 //                 are written in the same layout.
 //   warp 6      : gathers the next item's query rows into the other half of a
 //                 double-buffered Q tile while the current item computes.
-//   warp 1      : allocates TMEM; lane 0 issues tcgen05.mma:
-//                 S = Q K^T (M=128, N=64, K=D) and O_k = P V (M=128, N=D, K=64),
-//                 both double-buffered in TMEM, and commits to mbarriers.
+//   warp 1      : allocates TMEM; the whole warp runs the issue loop and one
+//                 elected lane issues tcgen05.mma: S = Q K^T (M=128, N=64,
+//                 K=D, double-buffered in TMEM) and O += P V (M=128, N=D,
+//                 K=64) into the item's O buffer (double-buffered by item),
+//                 and commits to mbarriers.
 //   warps 2..5  : one thread per query row: read S from TMEM, online softmax in
-//                 log2 units, write the rounded probabilities P to shared
-//                 memory as the A operand of the PV product, fold each chunk's
-//                 O_k into fp32 registers (o = o * alpha + O_k), then write the
-//                 item's partial rows (the merge kernel combines them) or, for a
-//                 prefill block, the normalised output rows.
+//                 log2 units against a reference max that moves only when a
+//                 chunk's max passes it by more than 2^8 (then O and the row
+//                 sum are rescaled in TMEM), write the rounded probabilities P
+//                 to shared memory as the A operand of the PV product, and at
+//                 the item's end stream O out of TMEM: the item's partial rows
+//                 (the merge kernel combines them) or, for a prefill block, the
+//                 normalised output rows.
 // Every wait is bounded; on a timeout the CTA records an error, drains its
 // copies and MMAs, frees TMEM and exits.
 #include <cuda_bf16.h>
@@ -54,21 +58,6 @@ __host__ __device__ constexpr uint32_t tc_q_bytes(int D) { return kBM * D * 2u; 
 __host__ __device__ constexpr uint32_t tc_p_bytes() { return kBM * kC * 2u; }
 __host__ __device__ constexpr size_t tc_smem_bytes(int D) {
   return 1024 + 2 * tc_q_bytes(D) + kNS * tc_tile_bytes(D) + 2 * tc_p_bytes() + 256;
-}
-
-template <typename T>
-__device__ __forceinline__ uint32_t pack2(float a, float b, float& sum) {
-  if constexpr (std::is_same<T, __half>::value) {
-    const __half2 h = __floats2half2_rn(a, b);
-    const float2 f = __half22float2(h);
-    sum += f.x + f.y;
-    return *reinterpret_cast<const uint32_t*>(&h);
-  } else {
-    const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
-    const float2 f = __bfloat1622float2(h);
-    sum += f.x + f.y;
-    return *reinterpret_cast<const uint32_t*>(&h);
-  }
 }
 
 template <typename T>
@@ -332,14 +321,20 @@ __global__ void __launch_bounds__(224, 1) attn_tc_kernel(const AttnParams p) {
         ptx::tc_fence_before();
         ptx::mbar_arrive(&sfree[b]);
 
+        // Raw scores; the chunk max is taken before scaling (the scale is
+        // positive), and the scale is folded into the exponent's FMA below.
         float x[kC];
-        float mx = -INFINITY;
 #pragma unroll
-        for (int k2 = 0; k2 < kC; ++k2) {
-          const uint32_t raw = k2 < 32 ? sv0[k2] : sv1[k2 - 32];
-          x[k2] = (k2 < lim) ? __uint_as_float(raw) * p.scale_log2 : -INFINITY;
-          mx = fmaxf(mx, x[k2]);
+        for (int k2 = 0; k2 < kC; ++k2) x[k2] = __uint_as_float(k2 < 32 ? sv0[k2] : sv1[k2 - 32]);
+        if (lim < kC) {
+#pragma unroll
+          for (int k2 = 0; k2 < kC; ++k2)
+            if (k2 >= lim) x[k2] = -INFINITY;
         }
+        float mxr = -INFINITY;
+#pragma unroll
+        for (int k2 = 0; k2 < kC; ++k2) mxr = fmaxf(mxr, x[k2]);
+        const float mx = mxr * p.scale_log2;
         // Move the reference max: always on the item's first chunk (nothing
         // accumulated yet); later only when this chunk's max runs past it.
         const bool move = (c == 0) || (mx > m + kRescale);
@@ -372,17 +367,26 @@ __global__ void __launch_bounds__(224, 1) attn_tc_kernel(const AttnParams p) {
           ok = false;
           break;
         }
-        float psum = 0.f;
+        // P = 2^(x * scale - m); the row sum is taken in fp32 before P is
+        // rounded to the operand type (two partial sums for a shorter chain).
+        const float neg_m = -m_use, sc = p.scale_log2;
+        float ps0 = 0.f, ps1 = 0.f;
         uint8_t* prow = ps + b * PB;
 #pragma unroll
         for (int j = 0; j < CCH; ++j) {
+          float e[8];
+#pragma unroll
+          for (int q = 0; q < 8; ++q) e[q] = ptx::ex2(fmaf(x[8 * j + q], sc, neg_m));
+          ps0 += (e[0] + e[1]) + (e[2] + e[3]);
+          ps1 += (e[4] + e[5]) + (e[6] + e[7]);
           uint4 pk;
-          pk.x = pack2<T>(ptx::ex2(x[8 * j + 0] - m_use), ptx::ex2(x[8 * j + 1] - m_use), psum);
-          pk.y = pack2<T>(ptx::ex2(x[8 * j + 2] - m_use), ptx::ex2(x[8 * j + 3] - m_use), psum);
-          pk.z = pack2<T>(ptx::ex2(x[8 * j + 4] - m_use), ptx::ex2(x[8 * j + 5] - m_use), psum);
-          pk.w = pack2<T>(ptx::ex2(x[8 * j + 6] - m_use), ptx::ex2(x[8 * j + 7] - m_use), psum);
+          pk.x = pack2_plain<T>(e[0], e[1]);
+          pk.y = pack2_plain<T>(e[2], e[3]);
+          pk.z = pack2_plain<T>(e[4], e[5]);
+          pk.w = pack2_plain<T>(e[6], e[7]);
           *reinterpret_cast<uint4*>(prow + r * 128 + ((j ^ (r & 7)) << 4)) = pk;
         }
+        const float psum = ps0 + ps1;
         ptx::fence_proxy_async_smem();
         ptx::tc_fence_before();  // orders any TMEM stores above before the PV product
         ptx::mbar_arrive(&pfull[b]);
