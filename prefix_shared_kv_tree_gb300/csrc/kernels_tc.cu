@@ -443,6 +443,7 @@ __global__ void __launch_bounds__(224, 1) attn_tc_kernel(const AttnParams p) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tbase, TMEM_COLS);
   }
+  if (p.pdl) ptx::pdl_wait();  // never complete before the kernel we overlap
 }
 
 template <typename T, int D>
@@ -451,8 +452,17 @@ cudaError_t launch_tc_t(const AttnParams& p, int grid, cudaStream_t s) {
   auto fn = attn_tc_kernel<T, D>;
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  fn<<<grid, 224, smem, s>>>(p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(224);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = p.pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, fn, p);
 }
 
 }  // namespace

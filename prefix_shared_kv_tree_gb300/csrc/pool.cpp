@@ -114,10 +114,13 @@ struct pst_pool {
   // Cost model for splitting the SMs between the phases (GB300, 64-token
   // chunks, head size 128): one chunk of one tensor-core item, the fixed cost
   // of an item, one CUDA-core tile when the phases run on split SMs, the
-  // DRAM rate one SM of the CUDA-core kernel sustains, and the whole GPU's.
-  double tc_chunk_us = 1.4, tc_item_us = 1.0, simt_tile_us = 0.75, simt_sm_gbs = 60.0, hbm_gbs = 6500.0;
+  // DRAM rate one SM of the CUDA-core kernel sustains (query groups of one),
+  // and the whole GPU's.
+  double tc_chunk_us = 1.8, tc_item_us = 1.0, simt_tile_us = 0.75, simt_sm_gbs = 80.0, hbm_gbs = 6500.0;
   int32_t simt_unit = 0;      // CUDA-core work-item size in chunks; 0 = automatic
   int32_t simt_max_ctas = 0;  // cap on the CUDA-core grid; 0 = one CTA per SM
+  bool simt_first = false;     // launch order of the decode step (see launch_overlapped)
+  bool tc_first_forced = false;
   int32_t simt_grid = 0, simt_stages = 3, simt_wpc = 8;
   int64_t n_part_rows = 0, shared_chunks = 0;
   std::vector<int32_t> canon_shared;   // 4 per row
@@ -458,6 +461,7 @@ pst_status rebuild(pst_pool* p) {
   // simple cost model so both finish together; items go to CTAs longest first.
   std::vector<int32_t> tc_cta_off(1, 0);
   p->n_tc_ctas = 0;
+  p->simt_first = false;
   if (p->n_tc_items > 0) {
     const int32_t n = p->n_tc_items;
     const bool concurrent = T > 0 && (p->cfg.flags & PST_FLAG_CONCURRENT_PHASES);
@@ -478,7 +482,9 @@ pst_status rebuild(pst_pool* p) {
       // k that minimises the modelled end time of both (with 20% margin on the
       // chunk-first estimate, fewer SMs on ties).
       const double simt_bytes = static_cast<double>(T) * p->tile_bytes;
-      const double hbm = p->hbm_gbs * 1e3, per_sm = p->simt_sm_gbs * 1e3;  // bytes per microsecond
+      // bytes per microsecond; the CUDA-core kernel's per-SM rate falls with
+      // the query-group size g (its arithmetic per byte grows with g)
+      const double hbm = p->hbm_gbs * 1e3, per_sm = p->simt_sm_gbs * 1e3 / std::pow(static_cast<double>(g), 0.7);
       double best = 1e300;
       for (int32_t kk = 1; kk <= std::min(p->n_sm, n); ++kk) {
         const double t_tc = 1.2 * std::max(w_tc / kk, max_cost);
@@ -490,6 +496,11 @@ pst_status rebuild(pst_pool* p) {
           k = kk;
         }
       }
+      // Sequence-first kernel first when the chunk-first phase is the shorter
+      // one (it then waits for the first kernel without holding its SMs long).
+      const double t_tc = 1.2 * std::max(w_tc / k, max_cost);
+      const double t_simt = simt_bytes / std::min(hbm, std::max(1, p->n_sm - k) * per_sm);
+      p->simt_first = k < p->n_sm && t_tc <= 1.1 * t_simt && !p->tc_first_forced;
     }
     if (concurrent && p->n_sm > 1) {
       const double w_simt = static_cast<double>(T) * p->simt_tile_us;
@@ -694,6 +705,7 @@ pst_status pst_pool_create(const pst_config* cfg, int device, pst_pool** out) {
   if (const char* e = std::getenv("PST_SIMT_SM_GBS")) p->simt_sm_gbs = std::atof(e);
   if (const char* e = std::getenv("PST_HBM_GBS")) p->hbm_gbs = std::atof(e);
   if (const char* e = std::getenv("PST_SIMT_UNIT")) p->simt_unit = std::atoi(e);
+  if (const char* e = std::getenv("PST_TC_FIRST")) p->tc_first_forced = std::atoi(e) != 0;
   // CUDA-core kernel shape: up to 8 consumer warps (plus the producer warp)
   // x 6 stages of 4 KB pieces, as far as shared memory allows
   p->simt_wpc = attn_simt_max_warps(g);
@@ -898,6 +910,57 @@ pst_status pst_seq_length(const pst_pool* p, int64_t seq_id, int64_t* n_tokens) 
   return PST_OK;
 }
 
+// Launch the decode kernels on one stream, overlapped, each later kernel a
+// programmatic dependent that waits at its end for the one before (so the
+// merge sees every partial row).  When the chunk-first phase is the shorter
+// one: the sequence-first kernel first, on the SMs the chunk-first kernel will
+// not use; the chunk-first kernel (its CTAs take the free SMs at once); a
+// second sequence-first launch sharing the work counter, for SMs released
+// late; the merge.  Otherwise the chunk-first kernel first and the
+// sequence-first kernel behind it on the whole grid (its CTAs start on the
+// free SMs at once, on the others as chunk-first CTAs leave); the merge.
+static pst_status launch_overlapped(pst_pool* p, const AttnParams& a, int32_t B, cudaStream_t s) {
+  const bool tc = p->n_tc_items > 0, simt = p->n_simt_items > 0;
+  const int32_t grid_a =
+      simt ? (tc ? (p->simt_first ? std::min(p->simt_grid, std::max(0, p->n_sm - p->n_tc_ctas)) : 0) : p->simt_grid) : 0;
+  const int32_t grid_b = simt ? p->simt_grid - grid_a : 0;
+  AttnParams a2 = a;
+  a2.items = reinterpret_cast<const WorkItem*>(p->d_tab + p->off_simt);
+  a2.n_items = p->n_simt_items;
+  bool before = false;  // a kernel of this step is already on the stream
+  if (grid_a > 0) {
+    a2.pdl = 0;
+    cudaError_t e = launch_attn_simt(p->cfg.dtype, p->D, p->C, p->g, a2, grid_a, s);
+    if (e != cudaSuccess) return fail(PST_ERR_CUDA, "sequence-first launch: %s", cudaGetErrorString(e));
+    p->last_launches++;
+    before = true;
+  }
+  if (tc) {
+    AttnParams a1 = a;
+    a1.items = reinterpret_cast<const WorkItem*>(p->d_tab + p->off_tc);
+    a1.n_items = p->n_tc_items;
+    a1.warp_items = p->d_tab + p->off_tc_cta;
+    a1.pdl = before ? 1 : 0;
+    cudaError_t e = launch_attn_tc(p->cfg.dtype, p->D, a1, p->n_tc_ctas, s);
+    if (e != cudaSuccess) return fail(PST_ERR_CUDA, "chunk-first launch: %s", cudaGetErrorString(e));
+    p->last_launches++;
+    before = true;
+  }
+  if (grid_b > 0) {
+    a2.pdl = before ? 1 : 0;
+    cudaError_t e = launch_attn_simt(p->cfg.dtype, p->D, p->C, p->g, a2, grid_b, s);
+    if (e != cudaSuccess) return fail(PST_ERR_CUDA, "sequence-first launch: %s", cudaGetErrorString(e));
+    p->last_launches++;
+    before = true;
+  }
+  AttnParams am = a;
+  am.pdl = before ? 1 : 0;
+  cudaError_t e = launch_merge(p->cfg.dtype, p->D, am, B, s);
+  if (e != cudaSuccess) return fail(PST_ERR_CUDA, "merge launch: %s", cudaGetErrorString(e));
+  p->last_launches++;
+  return PST_OK;
+}
+
 static pst_status decode_impl(pst_pool* p, const void* q, void* out, cudaStream_t s) {
   pst_status st = ensure_tables(p);
   if (st != PST_OK) return st;
@@ -919,8 +982,11 @@ static pst_status decode_impl(pst_pool* p, const void* q, void* out, cudaStream_
   a.row_idx = p->d_tab + p->off_rows;
   const bool fork = p->n_tc_items > 0 && p->n_simt_items > 0 && (p->cfg.flags & PST_FLAG_CONCURRENT_PHASES);
   cudaStream_t s1 = fork ? p->aux : s;
-  if (p->profiling) CUDA_TRY(cudaEventRecord(p->pev[4], s));
   if (p->n_simt_items > 0) CUDA_TRY(cudaMemsetAsync(p->d_sched, 0, sizeof(int32_t), s));
+  if (!fork && !p->profiling) return launch_overlapped(p, a, B, s);
+  // Profiling (per-phase events between the kernels, so no overlap) or forked
+  // phases: chunk-first, then sequence-first on the whole grid, then merge.
+  if (p->profiling) CUDA_TRY(cudaEventRecord(p->pev[4], s));
   if (fork) {
     CUDA_TRY(cudaEventRecord(p->ev_fork, s));
     CUDA_TRY(cudaStreamWaitEvent(p->aux, p->ev_fork, 0));
@@ -1010,27 +1076,8 @@ pst_status pst_decode_attention_noalloc(pst_pool* p, const void* q, void* out, v
   a.chunks = p->d_tab + p->off_chunks;
   a.m_off = p->d_tab + p->off_moff;
   a.row_idx = p->d_tab + p->off_rows;
-  if (p->n_tc_items > 0) {
-    AttnParams a1 = a;
-    a1.items = reinterpret_cast<const WorkItem*>(p->d_tab + p->off_tc);
-    a1.n_items = p->n_tc_items;
-    a1.warp_items = p->d_tab + p->off_tc_cta;
-    e = launch_attn_tc(p->cfg.dtype, p->D, a1, p->n_tc_ctas, s);
-    if (e != cudaSuccess) return fail(PST_ERR_CUDA, "chunk-first launch: %s", cudaGetErrorString(e));
-  }
-  if (p->n_simt_items > 0) {
-    AttnParams a2 = a;
-    a2.items = reinterpret_cast<const WorkItem*>(p->d_tab + p->off_simt);
-    a2.n_items = p->n_simt_items;
-    a2.pdl = p->n_tc_items > 0 ? 1 : 0;
-    e = launch_attn_simt(p->cfg.dtype, p->D, p->C, p->g, a2, p->simt_grid, s);
-    if (e != cudaSuccess) return fail(PST_ERR_CUDA, "sequence-first launch: %s", cudaGetErrorString(e));
-  }
-  AttnParams am = a;
-  am.pdl = 1;
-  e = launch_merge(p->cfg.dtype, p->D, am, B, s);
-  if (e != cudaSuccess) return fail(PST_ERR_CUDA, "merge launch: %s", cudaGetErrorString(e));
-  return PST_OK;
+  p->last_launches = 0;
+  return launch_overlapped(p, a, B, s);
 }
 
 pst_status pst_decode_attention_host(pst_pool* p, const void* q_host, void* out_host, void* stream) {
