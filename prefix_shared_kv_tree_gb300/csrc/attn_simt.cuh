@@ -57,7 +57,14 @@ __host__ __device__ inline size_t simt_stage_bytes(int C, int D, int es) {
 #ifndef PST_SIMT_G4_WARPS
 #define PST_SIMT_G4_WARPS 7
 #endif
-__host__ __device__ constexpr int simt_max_warps(int G) { return G >= 8 ? 7 : G >= 4 ? PST_SIMT_G4_WARPS : 8; }
+#ifndef PST_SIMT_G1_WARPS
+#define PST_SIMT_G1_WARPS 8
+#endif
+constexpr int kSimtMaxWarps = 12;  // capacity of the producer's per-CTA structures
+__host__ __device__ constexpr int simt_max_warps(int G) {
+  return G >= 8 ? 7 : G >= 4 ? PST_SIMT_G4_WARPS : G >= 2 ? 8 : PST_SIMT_G1_WARPS;
+}
+static_assert(PST_SIMT_G1_WARPS <= kSimtMaxWarps && PST_SIMT_G4_WARPS <= kSimtMaxWarps, "consumer warps");
 
 // Item slot: a 64-byte header -- [0] n_chunks (0: no more work), [1] kv,
 // [2] group0, [3] part_base, [4..7] valid tokens of the first four chunks,
@@ -156,7 +163,7 @@ __global__ void __launch_bounds__(32 * (simt_max_warps(G) + 1), 1) attn_simt_ker
 
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ int s_abort;
-  __shared__ __align__(16) SimtItem s_batch[2][8];  // claimed item descriptors, two batches of NW
+  __shared__ __align__(16) SimtItem s_batch[2][kSimtMaxWarps];  // claimed item descriptors, two batches of NW
   __shared__ uint64_t s_bbar[2];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -203,15 +210,15 @@ __global__ void __launch_bounds__(32 * (simt_max_warps(G) + 1), 1) attn_simt_ker
     };
     int base0 = 0, base1 = 0, pend = 0;
     if (lane == 0) {
-      base0 = atomicAdd(p.sched, NW);
-      base1 = atomicAdd(p.sched, NW);
+      base0 = atomicAdd(p.sched, NW) + p.claim_base;
+      base1 = atomicAdd(p.sched, NW) + p.claim_base;
     }
     base0 = __shfl_sync(0xffffffffu, base0, 0);
     base1 = __shfl_sync(0xffffffffu, base1, 0);
     if (lane == 0) {
       fill_batch(0, base0);
       fill_batch(1, base1);
-      pend = base1 + NW < n_items ? atomicAdd(p.sched, NW) : n_items;
+      pend = base1 + NW < n_items ? atomicAdd(p.sched, NW) + p.claim_base : n_items;
     }
     uint32_t fills0 = 1, fills1 = 1;
     int bcur = 0, bpos = 0;
@@ -278,7 +285,7 @@ __global__ void __launch_bounds__(32 * (simt_max_warps(G) + 1), 1) attn_simt_ker
           }
           if (lane == 0) {
             fill_batch(bcur, nb);
-            pend = nb + NW < n_items ? atomicAdd(p.sched, NW) : n_items;
+            pend = nb + NW < n_items ? atomicAdd(p.sched, NW) + p.claim_base : n_items;
           }
           bcur ^= 1;
           bpos -= NW;
@@ -320,6 +327,16 @@ __global__ void __launch_bounds__(32 * (simt_max_warps(G) + 1), 1) attn_simt_ker
     uint64_t* sfull = bars + 2 * S;
     uint64_t* sempty = bars + 2 * S + 2;
 
+    // The first item may be handed out statically (item blockIdx * NW + warp
+    // of the launch's first wave) and read straight from the item table, so
+    // the warp starts streaming without waiting for its producer; items after
+    // it come through the slots.
+    const int sidx = static_cast<int>(blockIdx.x) * NW + warp;
+    const bool has_static = sidx < min(p.first_items, n_items);
+    const uint32_t kofs = has_static ? 1u : 0u;
+    const SimtMeta st = simt_load_item(items, has_static ? sidx : n_items, n_items);
+    const T* qptr_g = static_cast<const T*>(p.q);
+
     // Staging (lane 0): the tiles of item si (this item or the next) go into
     // the warp's ring of S pieces; an item's chunk ids come from its slot
     // header, which the producer wrote before that slot completed.
@@ -333,16 +350,24 @@ __global__ void __launch_bounds__(32 * (simt_max_warps(G) + 1), 1) attn_simt_ker
     auto issue_next = [&]() -> bool {  // false: nothing can be issued now
       if (s_done || si > k + 1) return false;
       if (!s_ready) {
-        if (!ptx::mbar_test_wait(&sfull[si & 1], (si >> 1) & 1)) return false;
-        const int* h = reinterpret_cast<const int*>(slots + static_cast<size_t>(si & 1) * L.slot_bytes);
-        s_n = h[0];
-        if (s_n == 0) {
-          s_done = true;
-          return false;
+        if (si < kofs) {
+          s_n = st.b.x;
+          s_kv = st.b.y;
+          s_list = st.a.x;
+          s_ids = st.a;
+        } else {
+          const uint32_t js = si - kofs;
+          if (!ptx::mbar_test_wait(&sfull[js & 1], (js >> 1) & 1)) return false;
+          const int* h = reinterpret_cast<const int*>(slots + static_cast<size_t>(js & 1) * L.slot_bytes);
+          s_n = h[0];
+          if (s_n == 0) {
+            s_done = true;
+            return false;
+          }
+          s_kv = h[1];
+          s_list = h[8];
+          s_ids = *reinterpret_cast<const int4*>(h + 12);
         }
-        s_kv = h[1];
-        s_list = h[8];
-        s_ids = *reinterpret_cast<const int4*>(h + 12);
         s_ready = true;
         pc = 0;
         pp = 0;
@@ -379,16 +404,36 @@ __global__ void __launch_bounds__(32 * (simt_max_warps(G) + 1), 1) attn_simt_ker
     bool aborted = false;
 
     for (; !aborted; ++k) {
-      const int qs = k & 1;
-      if (!ptx::mbar_wait(&sfull[qs], (k >> 1) & 1, abort_flag, p.err)) break;
+      const bool stat = k < kofs;
+      const uint32_t js = k - kofs;  // slot sequence number of a non-static item
+      const int qs = js & 1;
       const uint8_t* sl = slots + static_cast<size_t>(qs) * L.slot_bytes;
-      const int* hdr = reinterpret_cast<const int*>(sl);
-      const int n_chunks = hdr[0];
-      if (n_chunks == 0) break;  // end marker
-      const int kv = hdr[1], grp = hdr[2], part_base = hdr[3], list_off = hdr[8];
-      // valid tokens of chunks 0 .. 31 of this item, one per lane (long runs,
-      // from prefill only, read them from the chunk-length array)
-      int my_len = lane < n_chunks ? hdr[4 + min(lane, kSimtInline - 1)] : 0;
+      int n_chunks, kv, grp, part_base, list_off, my_len;
+      const uint8_t* qsrc;  // the item's G query rows as stored
+      if (stat) {
+        n_chunks = st.b.x;
+        kv = st.b.y;
+        grp = st.b.z;
+        part_base = st.b.w;
+        list_off = st.a.x;
+        my_len = (lane < n_chunks && n_chunks <= kSimtInline)
+                     ? p.chunk_len[simt_chunk_id(st, min(lane, kSimtInline - 1), p.chunks)]
+                     : 0;
+        qsrc = reinterpret_cast<const uint8_t*>(qptr_g + (static_cast<size_t>(grp) * p.Hq + kv * p.g) * D);
+      } else {
+        if (!ptx::mbar_wait(&sfull[qs], (js >> 1) & 1, abort_flag, p.err)) break;
+        const int* hdr = reinterpret_cast<const int*>(sl);
+        n_chunks = hdr[0];
+        if (n_chunks == 0) break;  // end marker
+        kv = hdr[1];
+        grp = hdr[2];
+        part_base = hdr[3];
+        list_off = hdr[8];
+        // valid tokens of chunks 0 .. 31 of this item, one per lane
+        my_len = lane < n_chunks ? hdr[4 + min(lane, kSimtInline - 1)] : 0;
+        qsrc = sl + kSlotHeader;
+      }
+      // long runs (prefill only) read their chunk lengths from the chunk-length array
       if (n_chunks > kSimtInline) my_len = lane < n_chunks ? p.chunk_len[p.chunks[list_off + lane]] : 0;
       // query rows of this item, pre-scaled into log2 units
 #pragma unroll
@@ -397,8 +442,7 @@ __global__ void __launch_bounds__(32 * (simt_max_warps(G) + 1), 1) attn_simt_ker
         if (idx < G * DCH) {
           const int h = idx / DCH, j = idx % DCH;
           float f[VEC];
-          unpack16<T>(*reinterpret_cast<const uint4*>(sl + kSlotHeader + (static_cast<size_t>(h) * D + j * VEC) * ES),
-                      f);
+          unpack16<T>(*reinterpret_cast<const uint4*>(qsrc + (static_cast<size_t>(h) * D + j * VEC) * ES), f);
 #pragma unroll
           for (int e = 0; e < VEC; ++e) qbuf[h * D + j * VEC + e] = f[e] * p.scale_log2;
         }
@@ -410,7 +454,7 @@ __global__ void __launch_bounds__(32 * (simt_max_warps(G) + 1), 1) attn_simt_ker
       __syncwarp();
       // The slot is free once the header and rows are in registers / qbuf;
       // staging (lane 0, above) read item k+1's slot, never item k's after this.
-      if (lane == 0) ptx::mbar_arrive_relaxed(&sempty[qs]);
+      if (!stat && lane == 0) ptx::mbar_arrive_relaxed(&sempty[qs]);
 
       // o[h][i]: two partial sums (even / odd keys of each 16-byte run) of
       // output feature lane + 32 i, added at the end; packed fp32x2 FMAs

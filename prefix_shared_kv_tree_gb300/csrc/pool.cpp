@@ -914,22 +914,27 @@ pst_status pst_seq_length(const pst_pool* p, int64_t seq_id, int64_t* n_tokens) 
 // programmatic dependent that waits at its end for the one before (so the
 // merge sees every partial row).  When the chunk-first phase is the shorter
 // one: the sequence-first kernel first, on the SMs the chunk-first kernel will
-// not use; the chunk-first kernel (its CTAs take the free SMs at once); a
-// second sequence-first launch sharing the work counter, for SMs released
-// late; the merge.  Otherwise the chunk-first kernel first and the
+// not use; the chunk-first kernel (its CTAs take the free SMs at once); the
+// merge.  Otherwise the chunk-first kernel first and the
 // sequence-first kernel behind it on the whole grid (its CTAs start on the
 // free SMs at once, on the others as chunk-first CTAs leave); the merge.
 static pst_status launch_overlapped(pst_pool* p, const AttnParams& a, int32_t B, cudaStream_t s) {
   const bool tc = p->n_tc_items > 0, simt = p->n_simt_items > 0;
   const int32_t grid_a =
       simt ? (tc ? (p->simt_first ? std::min(p->simt_grid, std::max(0, p->n_sm - p->n_tc_ctas)) : 0) : p->simt_grid) : 0;
-  const int32_t grid_b = simt ? p->simt_grid - grid_a : 0;
+  // (With the sequence-first kernel first, the chunk-first CTAs hold their SMs
+  // until that kernel ends, so a second sequence-first launch could start only
+  // when no work is left: there is none.)
+  const int32_t grid_b = (simt && grid_a == 0) ? p->simt_grid : 0;
   AttnParams a2 = a;
   a2.items = reinterpret_cast<const WorkItem*>(p->d_tab + p->off_simt);
   a2.n_items = p->n_simt_items;
   bool before = false;  // a kernel of this step is already on the stream
   if (grid_a > 0) {
     a2.pdl = 0;
+    // every consumer of this launch starts on one item of the first wave
+    a2.first_items = grid_a * p->simt_wpc;
+    a2.claim_base = a2.first_items;
     cudaError_t e = launch_attn_simt(p->cfg.dtype, p->D, p->C, p->g, a2, grid_a, s);
     if (e != cudaSuccess) return fail(PST_ERR_CUDA, "sequence-first launch: %s", cudaGetErrorString(e));
     p->last_launches++;
@@ -948,6 +953,8 @@ static pst_status launch_overlapped(pst_pool* p, const AttnParams& a, int32_t B,
   }
   if (grid_b > 0) {
     a2.pdl = before ? 1 : 0;
+    a2.first_items = 0;  // its CTAs start at different times: every item is claimed
+    a2.claim_base = 0;
     cudaError_t e = launch_attn_simt(p->cfg.dtype, p->D, p->C, p->g, a2, grid_b, s);
     if (e != cudaSuccess) return fail(PST_ERR_CUDA, "sequence-first launch: %s", cudaGetErrorString(e));
     p->last_launches++;

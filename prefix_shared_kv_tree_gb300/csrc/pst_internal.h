@@ -72,7 +72,9 @@ struct AttnParams {
   const int32_t* chunks;      // chunk-id lists
   const WorkItem* items;      // tensor-core kernel items, or the CUDA-core kernel's SimtItem array
   const int32_t* warp_items;  // tensor-core kernel: item range [warp_items[c], warp_items[c+1]) of CTA c
-  int32_t* sched;             // CUDA-core kernel: next unclaimed item (zero at launch)
+  int32_t* sched;             // CUDA-core kernel: claim counter (zero at the step's start)
+  int32_t first_items;        // CUDA-core kernel: items [0, first_items) go to consumer blockIdx * NW + warp
+  int32_t claim_base;         // CUDA-core kernel: claimed index = counter value + claim_base
   int32_t n_items;
   int32_t n_warps;            // unused
   const void* q;              // [groups][Hq][D]
