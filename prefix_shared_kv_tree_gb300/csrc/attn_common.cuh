@@ -50,6 +50,19 @@ __device__ __forceinline__ __half from_float<__half>(float x) { return __float2h
 template <>
 __device__ __forceinline__ __nv_bfloat16 from_float<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
 
+// Two fp32 values rounded to nearest into one 32-bit word of 16-bit T
+// (a first, in the low half).  T is __half or __nv_bfloat16.
+template <typename T>
+__device__ __forceinline__ uint32_t pack2_16(float a, float b) {
+  if constexpr (std::is_same<T, __half>::value) {
+    const __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<const uint32_t*>(&h);
+  } else {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<const uint32_t*>(&h);
+  }
+}
+
 __device__ __forceinline__ float warp_max(float x) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));

@@ -51,9 +51,14 @@ __host__ __device__ inline size_t simt_stage_bytes(int C, int D, int es) {
   return kpb > vpb ? kpb : vpb;
 }
 
-// Consumer warps per CTA at most (one more warp produces).  With nine warps
-// one SM sub-partition holds three, which caps registers at 168 per thread:
-// query groups of four and more take seven consumers (255 registers).
+// Consumer warps per CTA at most (one more warp produces).  16-bit K/V take
+// the tensor-core consumer (about 100 registers at any query group).  The fp32
+// consumer keeps its G query rows' partial sums in registers: with nine warps
+// one SM sub-partition holds three, which caps registers at 168 per thread,
+// so query groups of four and more take seven consumers (255 registers).
+#ifndef PST_SIMT_MMA_WARPS
+#define PST_SIMT_MMA_WARPS 8
+#endif
 #ifndef PST_SIMT_G4_WARPS
 #define PST_SIMT_G4_WARPS 7
 #endif
@@ -61,10 +66,12 @@ __host__ __device__ inline size_t simt_stage_bytes(int C, int D, int es) {
 #define PST_SIMT_G1_WARPS 8
 #endif
 constexpr int kSimtMaxWarps = 12;  // capacity of the producer's per-CTA structures
-__host__ __device__ constexpr int simt_max_warps(int G) {
-  return G >= 8 ? 7 : G >= 4 ? PST_SIMT_G4_WARPS : G >= 2 ? 8 : PST_SIMT_G1_WARPS;
+__host__ __device__ constexpr int simt_max_warps(int G, int es) {
+  return es == 2 ? PST_SIMT_MMA_WARPS : G >= 8 ? 7 : G >= 4 ? PST_SIMT_G4_WARPS : G >= 2 ? 8 : PST_SIMT_G1_WARPS;
 }
-static_assert(PST_SIMT_G1_WARPS <= kSimtMaxWarps && PST_SIMT_G4_WARPS <= kSimtMaxWarps, "consumer warps");
+static_assert(PST_SIMT_G1_WARPS <= kSimtMaxWarps && PST_SIMT_G4_WARPS <= kSimtMaxWarps &&
+                  PST_SIMT_MMA_WARPS <= kSimtMaxWarps,
+              "consumer warps");
 
 // Item slot: a 64-byte header -- [0] n_chunks (0: no more work), [1] kv,
 // [2] group0, [3] part_base, [4..7] valid tokens of the first four chunks,
@@ -73,8 +80,12 @@ static_assert(PST_SIMT_G1_WARPS <= kSimtMaxWarps && PST_SIMT_G4_WARPS <= kSimtMa
 constexpr int kSlotHeader = 64;
 
 // Shared memory of one consumer warp, all offsets from the warp's base:
-// [stages x piece][q rows fp32][p fp32][2 item slots][barriers: full[S],
-// empty[S], slot_full[2], slot_empty[2]].
+// [stages x piece][q rows fp32][p][2 item slots][barriers: full[S], empty[S],
+// slot_full[2], slot_empty[2]].  The fp32 consumer keeps the scaled query rows
+// and the probabilities (G x C fp32); the tensor-core consumer (16-bit K/V)
+// keeps its query rows in registers and the probabilities as the transposed
+// C x 8 block of 16-bit values (one 16-byte row per key, columns past G
+// unused) that the P V product reads back.
 struct SimtLayout {
   uint32_t stage, q, p, slot, slot_bytes, bars, total;
 };
@@ -83,10 +94,11 @@ __host__ __device__ inline SimtLayout simt_layout(int C, int D, int G, int S, in
   SimtLayout L;
   L.stage = static_cast<uint32_t>(simt_stage_bytes(C, D, es));
   size_t off = static_cast<size_t>(S) * L.stage;
+  const bool mma = es == 2;
   L.q = static_cast<uint32_t>(off);
-  off += static_cast<size_t>(G) * D * 4;
+  off += mma ? 0 : static_cast<size_t>(G) * D * 4;
   L.p = static_cast<uint32_t>(off);
-  off += static_cast<size_t>(G) * C * 4;
+  off += mma ? static_cast<size_t>(C) * 16 : static_cast<size_t>(G) * C * 4;
   off = simt_align_up(off, 128);
   L.slot = static_cast<uint32_t>(off);
   L.slot_bytes = static_cast<uint32_t>(kSlotHeader + static_cast<size_t>(G) * D * es);
@@ -133,7 +145,7 @@ __device__ __forceinline__ int simt_chunk_id(const SimtMeta& m, int c, const int
 }
 
 template <typename T, int D, int G, int C>
-__global__ void __launch_bounds__(32 * (simt_max_warps(G) + 1), 1) attn_simt_kernel(const AttnParams p) {
+__global__ void __launch_bounds__(32 * (simt_max_warps(G, sizeof(T)) + 1), 1) attn_simt_kernel(const AttnParams p) {
   constexpr int ES = sizeof(T);
   constexpr int VEC = 16 / ES;
   constexpr int DCH = D / VEC;     // 16-byte chunks per query row
@@ -157,6 +169,11 @@ __global__ void __launch_bounds__(32 * (simt_max_warps(G) + 1), 1) attn_simt_ker
   constexpr size_t TILE = 2 * static_cast<size_t>(HALF);
   constexpr uint32_t QBYTES = static_cast<uint32_t>(G) * D * ES;
   constexpr int NQ = (G * DCH + 31) / 32;  // 16-byte query pieces per lane
+  // 16-bit K/V: warp-level tensor-core products with the keys (scores) and
+  // the output features (values) as the 16-row M side and the item's query
+  // rows as the 8-column N side.
+  constexpr bool kMma = ES == 2;
+  static_assert(!kMma || (G <= 8 && C % 32 == 0 && KPR % 16 == 0 && VB == 1 && VPR % 16 == 0), "mma shape");
   const int S = p.stages;
   const int NW = p.warps_per_cta;  // consumer warps; warp NW produces
   const SimtLayout L = simt_layout(C, D, G, S, ES);
@@ -321,6 +338,7 @@ __global__ void __launch_bounds__(32 * (simt_max_warps(G) + 1), 1) attn_simt_ker
     uint8_t* stages = rb;
     float* qbuf = reinterpret_cast<float*>(rb + L.q);
     float* pbuf = reinterpret_cast<float*>(rb + L.p);
+    uint8_t* pbuf_b = rb + L.p;  // tensor-core consumer: P^T, C rows of 16 bytes
     const uint8_t* slots = rb + L.slot;
     uint64_t* bars = reinterpret_cast<uint64_t*>(rb + L.bars);
     uint64_t* full = bars;
@@ -435,16 +453,33 @@ __global__ void __launch_bounds__(32 * (simt_max_warps(G) + 1), 1) attn_simt_ker
       }
       // long runs (prefill only) read their chunk lengths from the chunk-length array
       if (n_chunks > kSimtInline) my_len = lane < n_chunks ? p.chunk_len[p.chunks[list_off + lane]] : 0;
-      // query rows of this item, pre-scaled into log2 units
+      // query rows of this item: the tensor-core consumer holds them as the
+      // B operand of S^T = K Q^T (column n = query row lane / 4, zero past G);
+      // the fp32 consumer keeps them in qbuf, pre-scaled into log2 units
+      uint32_t qf[kMma ? D / 16 : 1][2];
+      if constexpr (kMma) {
+        const int n = lane >> 2;
 #pragma unroll
-      for (int kq = 0; kq < NQ; ++kq) {
-        const int idx = lane + 32 * kq;
-        if (idx < G * DCH) {
-          const int h = idx / DCH, j = idx % DCH;
-          float f[VEC];
-          unpack16<T>(*reinterpret_cast<const uint4*>(qsrc + (static_cast<size_t>(h) * D + j * VEC) * ES), f);
+        for (int ks = 0; ks < D / 16; ++ks) {
+          if (n < G) {
+            const uint8_t* qr = qsrc + (static_cast<size_t>(n) * D + ks * 16 + 2 * (lane & 3)) * ES;
+            qf[ks][0] = *reinterpret_cast<const uint32_t*>(qr);
+            qf[ks][1] = *reinterpret_cast<const uint32_t*>(qr + 16);
+          } else {
+            qf[ks][0] = qf[ks][1] = 0u;
+          }
+        }
+      } else {
 #pragma unroll
-          for (int e = 0; e < VEC; ++e) qbuf[h * D + j * VEC + e] = f[e] * p.scale_log2;
+        for (int kq = 0; kq < NQ; ++kq) {
+          const int idx = lane + 32 * kq;
+          if (idx < G * DCH) {
+            const int h = idx / DCH, j = idx % DCH;
+            float f[VEC];
+            unpack16<T>(*reinterpret_cast<const uint4*>(qsrc + (static_cast<size_t>(h) * D + j * VEC) * ES), f);
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) qbuf[h * D + j * VEC + e] = f[e] * p.scale_log2;
+          }
         }
       }
       if (lane == 0) {  // stage ahead: the rest of this item and the start of the next
@@ -456,6 +491,186 @@ __global__ void __launch_bounds__(32 * (simt_max_warps(G) + 1), 1) attn_simt_ker
       // staging (lane 0, above) read item k+1's slot, never item k's after this.
       if (!stat && lane == 0) ptx::mbar_arrive_relaxed(&sempty[qs]);
 
+      if constexpr (kMma) {
+        // ---- tensor-core consumer.  Lane roles of the m16n8k16 fragments:
+        // rows (keys of S^T, features of O^T) lg = lane / 4 and lg + 8 of
+        // each 16-row tile, query columns 2 lq and 2 lq + 1, lq = lane % 4.
+        constexpr int MT = C / 16;        // key tiles of a chunk
+        constexpr int KMT = KPR / 16;     // key tiles of a K piece
+        constexpr int VMT = VPR / 16;     // feature tiles of a V^T piece
+        constexpr int OMT = D / 16;       // feature tiles of the output
+        constexpr bool BF = std::is_same<T, __nv_bfloat16>::value;
+        const int lg = lane >> 2, lq = lane & 3;
+        // ldmatrix row of this lane within a 16-row tile, and its 16-byte
+        // column half: matrices 0..3 = (rows 0-7, k 0-7), (rows 8-15, k 0-7),
+        // (rows 0-7, k 8-15), (rows 8-15, k 8-15) -- the A fragment order
+        const int a_row = (lane & 7) + ((lane >> 3) & 1) * 8;
+        const int a_hi = lane >> 4;
+        const uint32_t pb = ptx::smem_u32(pbuf);
+        float m2[2] = {-INFINITY, -INFINITY}, nl2[2] = {0.f, 0.f};
+        float o[OMT][4];
+#pragma unroll
+        for (int t = 0; t < OMT; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.f;
+
+        for (int c = 0; c < n_chunks && !aborted; ++c) {
+          if ((c & 31) == 0 && c > 0) {  // valid tokens of chunks c .. c+31 (long runs only)
+            my_len = c + lane < n_chunks ? p.chunk_len[p.chunks[list_off + c + lane]] : 0;
+          }
+          int lim = __shfl_sync(0xffffffffu, my_len, c & 31);
+          if (p.causal_p0 >= 0) lim = min(lim, p.causal_p0 + grp + 1 - c * C);
+
+          // ---- S^T = K Q^T over the K pieces (raw scores, fp32)
+          float sacc[MT][4];
+#pragma unroll
+          for (int t = 0; t < MT; ++t) sacc[t][0] = sacc[t][1] = sacc[t][2] = sacc[t][3] = 0.f;
+#pragma unroll
+          for (int kp = 0; kp < KB * KPC; ++kp) {
+            const int kb = kp / KPC, kh = kp % KPC;  // feature block of 64, key run kh * KPR
+            if (!ptx::mbar_wait(&full[cs], cph, abort_flag, p.err)) {
+              aborted = true;
+              break;
+            }
+            const uint32_t kt = ptx::smem_u32(stages + static_cast<size_t>(cs) * L.stage);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {
+#pragma unroll
+              for (int t = 0; t < KMT; ++t) {
+                const int r = t * 16 + a_row;
+                uint32_t a[4];
+                ptx::ldsm_x4(kt + r * 128 + (((ks * 2 + a_hi) ^ (r & 7)) << 4), a);
+                ptx::mma_16816<BF>(sacc[kh * KMT + t], a, qf[kb * 4 + ks][0], qf[kb * 4 + ks][1]);
+              }
+            }
+            __syncwarp();  // every lane is done with the stage
+            ++consumed;
+            if (++cs == S) {
+              cs = 0;
+              cph ^= 1u;
+            }
+            if (lane == 0) issue_next();
+          }
+          if (aborted) break;
+
+          // ---- online softmax (Knowl 3, log2 units): the running max of a
+          // query column is taken on raw scores and scaled once; the scale
+          // is folded into the exponent's FMA
+          float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+          for (int t = 0; t < MT; ++t) {
+            if (t * 16 + lg >= lim) sacc[t][0] = sacc[t][1] = -INFINITY;
+            if (t * 16 + lg + 8 >= lim) sacc[t][2] = sacc[t][3] = -INFINITY;
+            mx0 = fmaxf(mx0, fmaxf(sacc[t][0], sacc[t][2]));
+            mx1 = fmaxf(mx1, fmaxf(sacc[t][1], sacc[t][3]));
+          }
+#pragma unroll
+          for (int sh = 4; sh < 32; sh <<= 1) {
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, sh));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, sh));
+          }
+          const float sl2 = p.scale_log2;
+          const float mn0 = fmaxf(m2[0], mx0 * sl2), mn1 = fmaxf(m2[1], mx1 * sl2);
+          const float mu0 = mn0 == -INFINITY ? 0.f : mn0, mu1 = mn1 == -INFINITY ? 0.f : mn1;
+          const float al0 = ptx::ex2(m2[0] - mu0), al1 = ptx::ex2(m2[1] - mu1);
+          m2[0] = mn0;
+          m2[1] = mn1;
+          float ps0 = 0.f, ps1 = 0.f;
+#pragma unroll
+          for (int t = 0; t < MT; ++t) {
+            const float e0 = ptx::ex2(fmaf(sacc[t][0], sl2, -mu0));
+            const float e1 = ptx::ex2(fmaf(sacc[t][1], sl2, -mu1));
+            const float e2 = ptx::ex2(fmaf(sacc[t][2], sl2, -mu0));
+            const float e3 = ptx::ex2(fmaf(sacc[t][3], sl2, -mu1));
+            ps0 += e0 + e2;
+            ps1 += e1 + e3;
+            // P^T row of key t*16 + lg (+8): query columns 2 lq, 2 lq + 1
+            *reinterpret_cast<uint32_t*>(pbuf_b + (t * 16 + lg) * 16 + lq * 4) = pack2_16<T>(e0, e1);
+            *reinterpret_cast<uint32_t*>(pbuf_b + (t * 16 + lg + 8) * 16 + lq * 4) = pack2_16<T>(e2, e3);
+          }
+          nl2[0] = nl2[0] * al0 + ps0;
+          nl2[1] = nl2[1] * al1 + ps1;
+#pragma unroll
+          for (int t = 0; t < OMT; ++t) {
+            o[t][0] *= al0;
+            o[t][1] *= al1;
+            o[t][2] *= al0;
+            o[t][3] *= al1;
+          }
+          __syncwarp();  // P^T is written
+          // B fragments of P^T (keys x query columns), k-steps of 16 keys:
+          // matrices of 8 key rows, transposed on load
+          uint32_t pf[MT][2];
+#pragma unroll
+          for (int t2 = 0; t2 < MT / 2; ++t2) {
+            uint32_t r[4];
+            ptx::ldsm_x4_trans(pb + (t2 * 32 + lane) * 16, r);
+            pf[2 * t2][0] = r[0];
+            pf[2 * t2][1] = r[1];
+            pf[2 * t2 + 1][0] = r[2];
+            pf[2 * t2 + 1][1] = r[3];
+          }
+
+          // ---- O^T += V^T P^T over the V^T pieces (VPR feature rows each)
+#pragma unroll
+          for (int vg = 0; vg < VG; ++vg) {
+            if (!ptx::mbar_wait(&full[cs], cph, abort_flag, p.err)) {
+              aborted = true;
+              break;
+            }
+            const uint32_t vt = ptx::smem_u32(stages + static_cast<size_t>(cs) * L.stage);
+#pragma unroll
+            for (int t = 0; t < VMT; ++t) {
+              const int r = t * 16 + a_row;
+#pragma unroll
+              for (int ks = 0; ks < MT; ++ks) {
+                const int j = ks * 2 + a_hi;
+                uint32_t a[4];
+                ptx::ldsm_x4(vt + (VSW ? r * 128 + ((j ^ (r & 7)) << 4) : cm_off(r, j, VCH)), a);
+                ptx::mma_16816<BF>(o[vg * VMT + t], a, pf[ks][0], pf[ks][1]);
+              }
+            }
+            __syncwarp();  // every lane is done with the stage (and with P^T before the next chunk)
+            ++consumed;
+            if (++cs == S) {
+              cs = 0;
+              cph ^= 1u;
+            }
+            if (lane == 0) issue_next();
+          }
+        }
+        if (aborted) break;
+
+        // ---- item result: lane holds features t*16 + lg (+8) of query
+        // columns 2 lq, 2 lq + 1; the row sums are lane-partial until here
+#pragma unroll
+        for (int sh = 4; sh < 32; sh <<= 1) {
+          nl2[0] += __shfl_xor_sync(0xffffffffu, nl2[0], sh);
+          nl2[1] += __shfl_xor_sync(0xffffffffu, nl2[1], sh);
+        }
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const int h = 2 * lq + j;
+          if (h < G) {
+            if (p.final_mode) {
+              const float inv = 1.f / nl2[j];
+              T* out = static_cast<T*>(p.out) + (static_cast<size_t>(grp) * p.Hq + kv * p.g + h) * D;
+#pragma unroll
+              for (int t = 0; t < OMT; ++t) {
+                out[t * 16 + lg] = from_float<T>(o[t][j] * inv);
+                out[t * 16 + lg + 8] = from_float<T>(o[t][2 + j] * inv);
+              }
+            } else {
+              const size_t row = static_cast<size_t>(part_base) + h;
+              float* po = p.part_o + row * D;
+#pragma unroll
+              for (int t = 0; t < OMT; ++t) {
+                po[t * 16 + lg] = o[t][j];
+                po[t * 16 + lg + 8] = o[t][2 + j];
+              }
+              if (lg == 0) reinterpret_cast<float2*>(p.part_ml)[row] = make_float2(m2[j], nl2[j]);
+            }
+          }
+        }
+      } else {
       // o[h][i]: two partial sums (even / odd keys of each 16-byte run) of
       // output feature lane + 32 i, added at the end; packed fp32x2 FMAs
       float m[G], nl[G];
@@ -623,6 +838,7 @@ __global__ void __launch_bounds__(32 * (simt_max_warps(G) + 1), 1) attn_simt_ker
           if (lane == 0) reinterpret_cast<float2*>(p.part_ml)[row] = make_float2(m[h], n);
         }
       }
+      }  // fp32 consumer
     }
     if (lane == 0) {
       // Let every copy still in flight land before the warp leaves (only
@@ -638,7 +854,7 @@ __global__ void __launch_bounds__(32 * (simt_max_warps(G) + 1), 1) attn_simt_ker
 
 template <typename T, int D, int G, int C>
 cudaError_t launch_simt_t(const AttnParams& p, int grid, cudaStream_t s) {
-  if (p.warps_per_cta < 1 || p.warps_per_cta > simt_max_warps(G)) return cudaErrorInvalidValue;
+  if (p.warps_per_cta < 1 || p.warps_per_cta > simt_max_warps(G, sizeof(T))) return cudaErrorInvalidValue;
   const size_t smem = simt_warp_bytes(C, D, G, p.stages, sizeof(T)) * p.warps_per_cta;
   auto fn = attn_simt_kernel<T, D, G, C>;
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));

@@ -152,7 +152,7 @@ bool simt_supported(int dtype, int D, int g) {
          (g == 1 || g == 2 || g == 4 || g == 8);
 }
 
-int attn_simt_max_warps(int g) { return simt_max_warps(g); }
+int attn_simt_max_warps(int dtype, int g) { return simt_max_warps(g, dtype_size(dtype)); }
 
 size_t attn_simt_smem(int dtype, int D, int C, int g, int stages, int warps_per_cta) {
   return simt_warp_bytes(C, D, g, stages, dtype_size(dtype)) * warps_per_cta;

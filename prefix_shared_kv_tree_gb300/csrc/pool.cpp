@@ -708,10 +708,10 @@ pst_status pst_pool_create(const pst_config* cfg, int device, pst_pool** out) {
   if (const char* e = std::getenv("PST_TC_FIRST")) p->tc_first_forced = std::atoi(e) != 0;
   // CUDA-core kernel shape: up to 8 consumer warps (plus the producer warp)
   // x 6 stages of 4 KB pieces, as far as shared memory allows
-  p->simt_wpc = attn_simt_max_warps(g);
+  p->simt_wpc = attn_simt_max_warps(c.dtype, g);
   p->simt_stages = 6;
   if (const char* e = std::getenv("PST_SIMT_WPC"))
-    p->simt_wpc = std::max(1, std::min(attn_simt_max_warps(g), std::atoi(e)));
+    p->simt_wpc = std::max(1, std::min(attn_simt_max_warps(c.dtype, g), std::atoi(e)));
   if (const char* e = std::getenv("PST_SIMT_STAGES")) p->simt_stages = std::max(2, std::min(16, std::atoi(e)));
   if (const char* e = std::getenv("PST_SIMT_SMS")) p->simt_max_ctas = std::max(1, std::atoi(e));
   while (attn_simt_smem(c.dtype, p->D, p->C, g, p->simt_stages, p->simt_wpc) > 220 * 1024) {

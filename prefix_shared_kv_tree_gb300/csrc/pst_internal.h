@@ -136,7 +136,7 @@ cudaError_t launch_scatter(int dtype, int D, int C, const ScatterParams& p, cuda
 cudaError_t launch_gather(int dtype, int D, int C, const ScatterParams& p, cudaStream_t s);
 cudaError_t launch_attn_simt(int dtype, int D, int C, int g, const AttnParams& p, int grid, cudaStream_t s);
 size_t attn_simt_smem(int dtype, int D, int C, int g, int stages, int warps_per_cta);
-int attn_simt_max_warps(int g);  // consumer warps per CTA of the CUDA-core kernel, at most
+int attn_simt_max_warps(int dtype, int g);  // consumer warps per CTA of the CUDA-core kernel, at most
 // per-dtype launchers (one translation unit each)
 cudaError_t launch_attn_simt_f16(int D, int C, int g, const AttnParams& p, int grid, cudaStream_t s);
 cudaError_t launch_attn_simt_bf16(int D, int C, int g, const AttnParams& p, int grid, cudaStream_t s);

@@ -307,5 +307,52 @@ __device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[32]) {
                  "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31]));
 }
 
+// ---------------------------------------------------------------------------
+// Warp-level tensor-core products (one warp, registers in and out), for
+// contractions whose M is a handful of query rows: the tcgen05 instruction
+// needs M >= 64 rows staged in shared memory and a TMEM accumulator per CTA,
+// which a warp streaming its own sequence has neither use nor room for.
+// ---------------------------------------------------------------------------
+
+// Four 8 x 8 matrices of 16-bit elements from shared memory; lanes 8i .. 8i+7
+// give the row addresses (16 bytes each) of matrix i, which lands in r[i]:
+// lane t holds row t / 4, elements 2 (t % 4) and 2 (t % 4) + 1.
+__device__ __forceinline__ void ldsm_x4(uint32_t saddr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(saddr));
+}
+
+// As ldsm_x4, each matrix transposed: lane t holds elements (2 (t % 4), t / 4)
+// and (2 (t % 4) + 1, t / 4) of matrix i in r[i].
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t saddr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(saddr));
+}
+
+// d (16 x 8 fp32) += a (16 x 16, row-major) * b (16 x 8, column-major), 16-bit
+// operands of one type.  Fragments: a[0..3] = rows g / g+8 at columns 2q, 2q+1,
+// then the same at columns 2q+8, 2q+9 (order a0: (g, k), a1: (g+8, k),
+// a2: (g, k+8), a3: (g+8, k+8)); b[0] = rows 2q, 2q+1 of column g, b[1] = rows
+// 2q+8, 2q+9; d[0..1] = row g, columns 2q, 2q+1, d[2..3] = row g+8 -- where
+// g = lane / 4 and q = lane % 4.
+template <bool BF16>
+__device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  if constexpr (BF16) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+  } else {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+  }
+}
+
 }  // namespace ptx
 }  // namespace pst
