@@ -74,101 +74,115 @@ __device__ __forceinline__ float warp_sum(float x) {
   return x;
 }
 
-// Merge the partial rows of one output row -- query head kv*g + hg of batch
-// row u, task = (u * Hkv + kv) * g + hg -- whose pair owns entries [e0, e1)
-// (entry e: partial row e*g + hg), and write the normalised output row.
-// Whole warp; lane owns D/32 contiguous features.  Partials are read through
-// L2 (other SMs wrote them): the (m, n) of every entry at once (lane = entry)
-// for the row max, then the weighted sums taken in entry order, then one
-// multiply by 1/n (ChunkAttention, Knowl 3: attn_reduce, then O = o / n).
-template <typename T, int D>
-__device__ __forceinline__ void merge_row(const AttnParams& p, int task, int e0, int e1, int lane) {
-  constexpr int DPL = D / 32;
-  constexpr int kFast = 16;  // entries merged from registers after one round of loads
-  const int g = p.g, hg = task % g;
+// Merge the partial rows of one (batch row u, KV head kv) pair, key =
+// u * Hkv + kv, whose entries are [e0, e1): entry e holds the G partial rows
+// e*G .. e*G + G-1 (query heads kv*G + hg), so an entry is one contiguous
+// block of G*D floats and the (m, n) of all the pair's rows are the
+// contiguous float2s [e0*G, e1*G).  Writes output rows key*G + hg.
+// Whole warp.  Lane l takes float4 l + 32 i of every entry block (row
+// (l + 32 i) / (D/4)); (m, n) pair x = j*G + hg sits in lane x mod 32.  Per
+// query row: the max of the entries' m, each entry's weight 2^(m_j - max),
+// n = sum of weight * n_j, o = sum of weight * o_j taken in entry order, then
+// one multiply by 1/n (ChunkAttention, Knowl 3: attn_reduce, then O = o / n).
+// Partials are read through L2: other SMs wrote them.
+template <typename T, int D, int G>
+__device__ __forceinline__ void merge_task(const AttnParams& p, int key, int e0, int e1, int lane) {
+  constexpr int RF = D / 4;                   // float4 per row
+  constexpr int F4 = G * RF;                  // float4 per entry block
+  constexpr int NI = (F4 + 31) / 32;          // float4 per lane per entry
+  constexpr int kFast = NI >= 16 ? 1 : 16 / NI;  // entries merged from registers after one round of loads
+  constexpr int EPR = 32 / G;                 // entries per 32 (m, n) pairs
   const int cnt = e1 - e0;
-  const float2* ml = reinterpret_cast<const float2*>(p.part_ml);
-  if (cnt <= kFast) {
-    // Every load first -- each entry's (m, n) (lane = entry) and this lane's
-    // features of every entry's o row -- then the same arithmetic, in the same
-    // entry order, as the general path below.
-    using VecT = typename std::conditional<DPL == 4, float4, float2>::type;
-    VecT ov[kFast];
+  const float4* po = reinterpret_cast<const float4*>(p.part_o) + static_cast<size_t>(e0) * F4 + lane;
+  const float2* ml = reinterpret_cast<const float2*>(p.part_ml) + static_cast<size_t>(e0) * G;
+  int hg_i[NI];  // query row of this lane's float4 i
+#pragma unroll
+  for (int i = 0; i < NI; ++i) hg_i[i] = min((lane + 32 * i) / RF, G - 1);
+  float4 acc[NI];
+#pragma unroll
+  for (int i = 0; i < NI; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  float mx, nn;  // lanes with lane % G == hg end up holding row hg's max and n
+  if (cnt <= kFast && cnt <= EPR) {
+    // Every load first -- the pairs' (m, n) (lane = pair) and this lane's
+    // float4s of every entry block -- then the arithmetic.
+    float4 ov[kFast][NI];
 #pragma unroll
     for (int j = 0; j < kFast; ++j)
-      if (j < cnt)
-        ov[j] = __ldcg(reinterpret_cast<const VecT*>(p.part_o + (static_cast<size_t>(e0 + j) * g + hg) * D + lane * DPL));
-    const float2 mn = lane < cnt ? __ldcg(ml + static_cast<size_t>(e0 + lane) * g + hg) : make_float2(-INFINITY, 0.f);
-    const float m = warp_max(mn.x);
-    float o[DPL];
 #pragma unroll
-    for (int i = 0; i < DPL; ++i) o[i] = 0.f;
-    float n = 0.f;
+      for (int i = 0; i < NI; ++i)
+        if (j < cnt && lane + 32 * i < F4) ov[j][i] = __ldcg(po + j * F4 + 32 * i);
+    const float2 mn = lane < cnt * G ? __ldcg(ml + lane) : make_float2(-INFINITY, 0.f);
+    mx = mn.x;
+#pragma unroll
+    for (int s = G; s < 32; s <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, s));
+    const float w = mn.x == -INFINITY ? 0.f : ptx::ex2(mn.x - mx);  // an entry with no valid key adds nothing
+    nn = w * mn.y;
+#pragma unroll
+    for (int s = G; s < 32; s <<= 1) nn += __shfl_xor_sync(0xffffffffu, nn, s);
 #pragma unroll
     for (int j = 0; j < kFast; ++j) {
       if (j < cnt) {
-        const float mj = __shfl_sync(0xffffffffu, mn.x, j);
-        const float nj = __shfl_sync(0xffffffffu, mn.y, j);
-        const float wj = mj == -INFINITY ? 0.f : ptx::ex2(mj - m);
-        n = fmaf(wj, nj, n);
-        if constexpr (DPL == 4) {
-          o[0] = fmaf(wj, ov[j].x, o[0]);
-          o[1] = fmaf(wj, ov[j].y, o[1]);
-          o[2] = fmaf(wj, ov[j].z, o[2]);
-          o[3] = fmaf(wj, ov[j].w, o[3]);
-        } else {
-          o[0] = fmaf(wj, ov[j].x, o[0]);
-          o[1] = fmaf(wj, ov[j].y, o[1]);
+#pragma unroll
+        for (int i = 0; i < NI; ++i) {
+          const float wj = __shfl_sync(0xffffffffu, w, j * G + hg_i[i]);
+          acc[i].x = fmaf(wj, ov[j][i].x, acc[i].x);
+          acc[i].y = fmaf(wj, ov[j][i].y, acc[i].y);
+          acc[i].z = fmaf(wj, ov[j][i].z, acc[i].z);
+          acc[i].w = fmaf(wj, ov[j][i].w, acc[i].w);
         }
       }
     }
-    const float inv = 1.f / n;
-    T* out = static_cast<T*>(p.out) + static_cast<size_t>(task) * D + lane * DPL;
+  } else {
+    // Rounds of 32 pairs (EPR entries): the max over every round first, then
+    // per round the weights, n, and the weighted entry blocks.
+    const int rounds = (cnt + EPR - 1) / EPR;
+    mx = -INFINITY;
+    for (int r = 0; r < rounds; ++r) {
+      const int x = r * 32 + lane;
+      if (x < cnt * G) mx = fmaxf(mx, __ldcg(ml + x).x);
+    }
 #pragma unroll
-    for (int i = 0; i < DPL; ++i) out[i] = from_float<T>(o[i] * inv);
-    return;
-  }
-  float2 first = make_float2(-INFINITY, 0.f);  // entry `lane` of the first 32
-  float m = -INFINITY;
-  for (int e = lane; e < cnt; e += 32) {
-    const float2 t = __ldcg(ml + static_cast<size_t>(e0 + e) * g + hg);
-    if (e < 32) first = t;
-    m = fmaxf(m, t.x);
-  }
-  m = warp_max(m);
-  float o[DPL];
+    for (int s = G; s < 32; s <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, s));
+    nn = 0.f;
+    for (int r = 0; r < rounds; ++r) {
+      const int x = r * 32 + lane;
+      const float2 mn = x < cnt * G ? __ldcg(ml + x) : make_float2(-INFINITY, 0.f);
+      const float w = mn.x == -INFINITY ? 0.f : ptx::ex2(mn.x - mx);
+      nn = fmaf(w, mn.y, nn);
+      const int c = min(EPR, cnt - r * EPR);
+#pragma unroll 4
+      for (int j = 0; j < c; ++j) {
+        const float4* src = po + static_cast<size_t>(r * EPR + j) * F4;
 #pragma unroll
-  for (int i = 0; i < DPL; ++i) o[i] = 0.f;
-  float n = 0.f;
-  for (int base = 0; base < cnt; base += 32) {
-    float2 mn = first;
-    if (base > 0) mn = lane < cnt - base ? __ldcg(ml + static_cast<size_t>(e0 + base + lane) * g + hg)
-                                         : make_float2(-INFINITY, 0.f);
-    const int c = min(32, cnt - base);
-#pragma unroll 8
-    for (int j = 0; j < c; ++j) {
-      const float mj = __shfl_sync(0xffffffffu, mn.x, j);
-      const float nj = __shfl_sync(0xffffffffu, mn.y, j);
-      const float wj = mj == -INFINITY ? 0.f : ptx::ex2(mj - m);  // an entry with no valid key adds nothing
-      n = fmaf(wj, nj, n);
-      const float* src = p.part_o + (static_cast<size_t>(e0 + base + j) * g + hg) * D + lane * DPL;
-      if constexpr (DPL == 4) {
-        const float4 t = __ldcg(reinterpret_cast<const float4*>(src));
-        o[0] = fmaf(wj, t.x, o[0]);
-        o[1] = fmaf(wj, t.y, o[1]);
-        o[2] = fmaf(wj, t.z, o[2]);
-        o[3] = fmaf(wj, t.w, o[3]);
+        for (int i = 0; i < NI; ++i) {
+          const float wj = __shfl_sync(0xffffffffu, w, j * G + hg_i[i]);
+          if (lane + 32 * i < F4) {
+            const float4 t = __ldcg(src + 32 * i);
+            acc[i].x = fmaf(wj, t.x, acc[i].x);
+            acc[i].y = fmaf(wj, t.y, acc[i].y);
+            acc[i].z = fmaf(wj, t.z, acc[i].z);
+            acc[i].w = fmaf(wj, t.w, acc[i].w);
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int s = G; s < 32; s <<= 1) nn += __shfl_xor_sync(0xffffffffu, nn, s);
+  }
+#pragma unroll
+  for (int i = 0; i < NI; ++i) {
+    const float inv = 1.f / __shfl_sync(0xffffffffu, nn, hg_i[i]);
+    const int f = lane + 32 * i;
+    if (f < F4) {
+      T* out = static_cast<T*>(p.out) + (static_cast<size_t>(key) * G + f / RF) * D + (f % RF) * 4;
+      if constexpr (sizeof(T) == 2) {
+        *reinterpret_cast<uint2*>(out) =
+            make_uint2(pack2_16<T>(acc[i].x * inv, acc[i].y * inv), pack2_16<T>(acc[i].z * inv, acc[i].w * inv));
       } else {
-        const float2 t = __ldcg(reinterpret_cast<const float2*>(src));
-        o[0] = fmaf(wj, t.x, o[0]);
-        o[1] = fmaf(wj, t.y, o[1]);
+        *reinterpret_cast<float4*>(out) = make_float4(acc[i].x * inv, acc[i].y * inv, acc[i].z * inv, acc[i].w * inv);
       }
     }
   }
-  const float inv = 1.f / n;
-  T* out = static_cast<T*>(p.out) + static_cast<size_t>(task) * D + lane * DPL;
-#pragma unroll
-  for (int i = 0; i < DPL; ++i) out[i] = from_float<T>(o[i] * inv);
 }
 
 }  // namespace pst

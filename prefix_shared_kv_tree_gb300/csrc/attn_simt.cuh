@@ -365,6 +365,7 @@ __global__ void __launch_bounds__(32 * (simt_max_warps(G, sizeof(T)) + 1), 1) at
     int s_n = 0, s_kv = 0, s_list = 0, pc = 0, pp = 0, ps = 0;
     int4 s_ids = make_int4(0, 0, 0, 0);
     uint32_t issued = 0;
+    const uint64_t kv_policy = ptx::policy_evict_first();
     auto issue_next = [&]() -> bool {  // false: nothing can be issued now
       if (s_done || si > k + 1) return false;
       if (!s_ready) {
@@ -404,7 +405,10 @@ __global__ void __launch_bounds__(32 * (simt_max_warps(G, sizeof(T)) + 1), 1) at
         bytes = VPB;
       }
       ptx::mbar_arrive_expect_tx_relaxed(&full[ps], bytes);
-      ptx::bulk_g2s(stages + static_cast<size_t>(ps) * L.stage, src, bytes, &full[ps]);
+      if (p.kv_evict_first)
+        ptx::bulk_g2s_hint(stages + static_cast<size_t>(ps) * L.stage, src, bytes, &full[ps], kv_policy);
+      else
+        ptx::bulk_g2s(stages + static_cast<size_t>(ps) * L.stage, src, bytes, &full[ps]);
       ++issued;
       if (++ps == S) ps = 0;
       if (++pp == NP) {

@@ -103,27 +103,37 @@ __global__ void __launch_bounds__(256) gather_kernel(const ScatterParams p, int 
 // it on the stream.  Launched as a programmatic dependent: it becomes
 // resident while they run and waits for their completion before reading.
 // ---------------------------------------------------------------------------
-template <typename T, int D>
+template <typename T, int D, int G>
 __global__ void __launch_bounds__(128) merge_kernel(const AttnParams p, int B) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int task = blockIdx.x * 4 + warp;  // output row: (u * Hkv + kv) * g + hg
-  const bool live = task < B * p.Hq;
+  const int key = blockIdx.x * 4 + warp;  // (batch row, KV head) pair: u * Hkv + kv
+  const bool live = key < B * p.Hkv;
   int e0 = 0, e1 = 0;
   if (live) {  // the merge table was uploaded before the attention kernels ran
-    const int key = task / p.g;
     e0 = __ldg(p.m_off + key);
     e1 = __ldg(p.m_off + key + 1);
   }
   if (p.pdl) ptx::pdl_wait();
-  if (live) merge_row<T, D>(p, task, e0, e1, lane);
+  if (live) merge_task<T, D, G>(p, key, e0, e1, lane);
+}
+
+template <typename T, int D>
+cudaError_t launch_merge_d(const cudaLaunchConfig_t& cfg, int g, const AttnParams& p, int B) {
+  switch (g) {
+    case 1: return cudaLaunchKernelEx(&cfg, merge_kernel<T, D, 1>, p, B);
+    case 2: return cudaLaunchKernelEx(&cfg, merge_kernel<T, D, 2>, p, B);
+    case 4: return cudaLaunchKernelEx(&cfg, merge_kernel<T, D, 4>, p, B);
+    case 8: return cudaLaunchKernelEx(&cfg, merge_kernel<T, D, 8>, p, B);
+  }
+  return cudaErrorInvalidValue;
 }
 
 template <typename T>
 cudaError_t launch_merge_t(int D, const AttnParams& p, int B, cudaStream_t s) {
-  const int tasks = B * p.Hq;
-  if (tasks == 0) return cudaSuccess;
+  const int keys = B * p.Hkv;
+  if (keys == 0) return cudaSuccess;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((tasks + 3) / 4);
+  cfg.gridDim = dim3((keys + 3) / 4);
   cfg.blockDim = dim3(128);
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
@@ -131,8 +141,8 @@ cudaError_t launch_merge_t(int D, const AttnParams& p, int B, cudaStream_t s) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = p.pdl ? 1 : 0;
-  if (D == 64) return cudaLaunchKernelEx(&cfg, merge_kernel<T, 64>, p, B);
-  if (D == 128) return cudaLaunchKernelEx(&cfg, merge_kernel<T, 128>, p, B);
+  if (D == 64) return launch_merge_d<T, 64>(cfg, p.g, p, B);
+  if (D == 128) return launch_merge_d<T, 128>(cfg, p.g, p, B);
   return cudaErrorInvalidValue;
 }
 

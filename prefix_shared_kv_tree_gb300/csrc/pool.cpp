@@ -116,7 +116,7 @@ struct pst_pool {
   // of an item, one CUDA-core tile when the phases run on split SMs, the
   // DRAM rate one SM of the CUDA-core kernel sustains (query groups of one),
   // and the whole GPU's.
-  double tc_chunk_us = 1.8, tc_item_us = 1.0, simt_tile_us = 0.75, simt_sm_gbs = 80.0, hbm_gbs = 6500.0;
+  double tc_chunk_us = 1.8, tc_item_us = 1.0, simt_tile_us = 0.75, simt_sm_gbs = 60.0, hbm_gbs = 6500.0;
   int32_t simt_unit = 0;      // CUDA-core work-item size in chunks; 0 = automatic
   int32_t simt_max_ctas = 0;  // cap on the CUDA-core grid; 0 = one CTA per SM
   bool simt_first = false;     // launch order of the decode step (see launch_overlapped)
@@ -482,9 +482,12 @@ pst_status rebuild(pst_pool* p) {
       // k that minimises the modelled end time of both (with 20% margin on the
       // chunk-first estimate, fewer SMs on ties).
       const double simt_bytes = static_cast<double>(T) * p->tile_bytes;
-      // bytes per microsecond; the CUDA-core kernel's per-SM rate falls with
-      // the query-group size g (its arithmetic per byte grows with g)
-      const double hbm = p->hbm_gbs * 1e3, per_sm = p->simt_sm_gbs * 1e3 / std::pow(static_cast<double>(g), 0.7);
+      // bytes per microsecond; with fp32 K/V the sequence-first kernel's
+      // per-SM rate falls with the query-group size g (its FMAs per byte grow
+      // with g); its tensor-core products for 16-bit K/V cover g <= 8 alike
+      const double g_exp = p->cfg.dtype == kF32 ? 0.7 : 0.0;
+      const double hbm = p->hbm_gbs * 1e3,
+                   per_sm = p->simt_sm_gbs * 1e3 / std::pow(static_cast<double>(g), g_exp);
       double best = 1e300;
       for (int32_t kk = 1; kk <= std::min(p->n_sm, n); ++kk) {
         const double t_tc = 1.2 * std::max(w_tc / kk, max_cost);
@@ -639,6 +642,10 @@ pst_status need_device(const pst_pool* p) {
   if (e != cudaSuccess) return fail(PST_ERR_CUDA, "cudaSetDevice: %s", cudaGetErrorString(e));
   return PST_OK;
 }
+
+// Decode: with the shared chunks on the tensor cores and min_share <= 2,
+// every sequence-first tile belongs to one sequence, so each is read once.
+int32_t decode_evict_first(const pst_pool* p) { return (p->use_tc && p->cfg.min_share <= 2) ? 1 : 0; }
 
 AttnParams base_params(const pst_pool* p) {
   AttnParams a{};
@@ -985,6 +992,7 @@ static pst_status decode_impl(pst_pool* p, const void* q, void* out, cudaStream_
   a.part_o = p->d_part_o;
   a.part_ml = p->d_part_ml;
   a.chunks = p->d_tab + p->off_chunks;
+  a.kv_evict_first = decode_evict_first(p);
   a.m_off = p->d_tab + p->off_moff;
   a.row_idx = p->d_tab + p->off_rows;
   const bool fork = p->n_tc_items > 0 && p->n_simt_items > 0 && (p->cfg.flags & PST_FLAG_CONCURRENT_PHASES);
@@ -1081,6 +1089,7 @@ pst_status pst_decode_attention_noalloc(pst_pool* p, const void* q, void* out, v
   a.part_o = reinterpret_cast<float*>(b8 + sched_bytes + ml_bytes);
   CUDA_TRY(cudaMemsetAsync(a.sched, 0, sizeof(int32_t), s));
   a.chunks = p->d_tab + p->off_chunks;
+  a.kv_evict_first = decode_evict_first(p);
   a.m_off = p->d_tab + p->off_moff;
   a.row_idx = p->d_tab + p->off_rows;
   p->last_launches = 0;

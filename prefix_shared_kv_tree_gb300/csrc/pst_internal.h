@@ -94,6 +94,11 @@ struct AttnParams {
   // kv*g + hg at row e*g + hg.
   const int32_t* m_off;       // [B * Hkv + 1]
   const int32_t* row_idx;     // tensor-core kernel: partial row of item row r at row_idx[item.part_base + r]
+  // CUDA-core kernel: 1 when every K/V tile it stages is read by one item
+  // only (decode with the shared chunks on the tensor cores): its copies then
+  // take the L2 evict-first priority, so the streamed tiles do not push the
+  // partial rows that the merge reads next out of L2.
+  int32_t kv_evict_first;
   // 1: launched as a programmatic dependent of the previous kernel on the
   // stream (it may start while that kernel drains; it must not finish first)
   int32_t pdl;
