@@ -41,6 +41,7 @@ __host__ __device__ inline size_t simt_align_up(size_t x, size_t a) { return (x 
 #define PST_SIMT_PIECE_ROWS 64
 #endif
 constexpr int kSimtPieceRows = PST_SIMT_PIECE_ROWS;
+
 static_assert(kSimtPieceRows == 32 || kSimtPieceRows == 64, "piece rows");
 
 __host__ __device__ inline size_t simt_stage_bytes(int C, int D, int es) {
@@ -355,9 +356,10 @@ __global__ void __launch_bounds__(32 * (simt_max_warps(G, sizeof(T)) + 1), 1) at
     const SimtMeta st = simt_load_item(items, has_static ? sidx : n_items, n_items);
     const T* qptr_g = static_cast<const T*>(p.q);
 
-    // Staging (lane 0): the tiles of item si (this item or the next) go into
-    // the warp's ring of S pieces; an item's chunk ids come from its slot
-    // header, which the producer wrote before that slot completed.
+    // Staging (whole warp, all lanes in step): the tiles of item si (this
+    // item or the next) go into the warp's ring of S pieces; an item's chunk
+    // ids come from its slot header, which the producer wrote before that
+    // slot completed.
     uint32_t k = 0;  // items started
     uint32_t si = 0;          // item being staged
     bool s_ready = false;     // its header is in s_* below
@@ -376,7 +378,9 @@ __global__ void __launch_bounds__(32 * (simt_max_warps(G, sizeof(T)) + 1), 1) at
           s_ids = st.a;
         } else {
           const uint32_t js = si - kofs;
-          if (!ptx::mbar_test_wait(&sfull[js & 1], (js >> 1) & 1)) return false;
+          // every lane observes the phase (each read below is ordered by its
+          // own acquire); the decision is the warp's
+          if (!__all_sync(0xffffffffu, ptx::mbar_test_wait(&sfull[js & 1], (js >> 1) & 1))) return false;
           const int* h = reinterpret_cast<const int*>(slots + static_cast<size_t>(js & 1) * L.slot_bytes);
           s_n = h[0];
           if (s_n == 0) {
@@ -404,11 +408,13 @@ __global__ void __launch_bounds__(32 * (simt_max_warps(G, sizeof(T)) + 1), 1) at
         src = tile + HALF + (VSW ? (static_cast<size_t>(vb) * D * 128 + vg * VPB) : static_cast<size_t>(vg) * VPB);
         bytes = VPB;
       }
-      ptx::mbar_arrive_expect_tx_relaxed(&full[ps], bytes);
-      if (p.kv_evict_first)
-        ptx::bulk_g2s_hint(stages + static_cast<size_t>(ps) * L.stage, src, bytes, &full[ps], kv_policy);
-      else
-        ptx::bulk_g2s(stages + static_cast<size_t>(ps) * L.stage, src, bytes, &full[ps]);
+      if (lane == 0) {
+        ptx::mbar_arrive_expect_tx_relaxed(&full[ps], bytes);
+        if (p.kv_evict_first)
+          ptx::bulk_g2s_hint(stages + static_cast<size_t>(ps) * L.stage, src, bytes, &full[ps], kv_policy);
+        else
+          ptx::bulk_g2s(stages + static_cast<size_t>(ps) * L.stage, src, bytes, &full[ps]);
+      }
       ++issued;
       if (++ps == S) ps = 0;
       if (++pp == NP) {
@@ -462,15 +468,31 @@ __global__ void __launch_bounds__(32 * (simt_max_warps(G, sizeof(T)) + 1), 1) at
       // the fp32 consumer keeps them in qbuf, pre-scaled into log2 units
       uint32_t qf[kMma ? D / 16 : 1][2];
       if constexpr (kMma) {
-        const int n = lane >> 2;
+        if (!stat) {
+          // from the slot, two k-steps per ldmatrix: matrix i holds features
+          // 8 i .. 8 i + 7 of the pair's 16-feature span, rows = query rows
+          // (rows past G repeat row G-1: their columns are never stored)
+          const uint32_t qb = ptx::smem_u32(qsrc) + static_cast<uint32_t>(min(lane & 7, G - 1) * D * ES) + (lane >> 3) * 16;
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          if (n < G) {
-            const uint8_t* qr = qsrc + (static_cast<size_t>(n) * D + ks * 16 + 2 * (lane & 3)) * ES;
-            qf[ks][0] = *reinterpret_cast<const uint32_t*>(qr);
-            qf[ks][1] = *reinterpret_cast<const uint32_t*>(qr + 16);
-          } else {
-            qf[ks][0] = qf[ks][1] = 0u;
+          for (int k2 = 0; k2 < D / 32; ++k2) {
+            uint32_t r[4];
+            ptx::ldsm_x4(qb + k2 * 64, r);
+            qf[2 * k2][0] = r[0];
+            qf[2 * k2][1] = r[1];
+            qf[2 * k2 + 1][0] = r[2];
+            qf[2 * k2 + 1][1] = r[3];
+          }
+        } else {
+          const int n = lane >> 2;
+#pragma unroll
+          for (int ks = 0; ks < D / 16; ++ks) {
+            if (n < G) {
+              const uint8_t* qr = qsrc + (static_cast<size_t>(n) * D + ks * 16 + 2 * (lane & 3)) * ES;
+              qf[ks][0] = *reinterpret_cast<const uint32_t*>(qr);
+              qf[ks][1] = *reinterpret_cast<const uint32_t*>(qr + 16);
+            } else {
+              qf[ks][0] = qf[ks][1] = 0u;
+            }
           }
         }
       } else {
@@ -486,13 +508,12 @@ __global__ void __launch_bounds__(32 * (simt_max_warps(G, sizeof(T)) + 1), 1) at
           }
         }
       }
-      if (lane == 0) {  // stage ahead: the rest of this item and the start of the next
-        while (issued < consumed + S && issue_next()) {
-        }
+      // stage ahead: the rest of this item and the start of the next
+      while (issued < consumed + S && issue_next()) {
       }
       __syncwarp();
       // The slot is free once the header and rows are in registers / qbuf;
-      // staging (lane 0, above) read item k+1's slot, never item k's after this.
+      // staging (above) read item k+1's slot, never item k's after this.
       if (!stat && lane == 0) ptx::mbar_arrive_relaxed(&sempty[qs]);
 
       if constexpr (kMma) {
@@ -535,15 +556,23 @@ __global__ void __launch_bounds__(32 * (simt_max_warps(G, sizeof(T)) + 1), 1) at
               break;
             }
             const uint32_t kt = ptx::smem_u32(stages + static_cast<size_t>(cs) * L.stage);
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks) {
+            // A fragments one k-step ahead of the products that use them, so
+            // every product finds its operands loaded
+            uint32_t af[2][KMT][4];
+            auto load_k = [&](int ks, uint32_t (&dst)[KMT][4]) {
 #pragma unroll
               for (int t = 0; t < KMT; ++t) {
                 const int r = t * 16 + a_row;
-                uint32_t a[4];
-                ptx::ldsm_x4(kt + r * 128 + (((ks * 2 + a_hi) ^ (r & 7)) << 4), a);
-                ptx::mma_16816<BF>(sacc[kh * KMT + t], a, qf[kb * 4 + ks][0], qf[kb * 4 + ks][1]);
+                ptx::ldsm_x4(kt + r * 128 + (((ks * 2 + a_hi) ^ (r & 7)) << 4), dst[t]);
               }
+            };
+            load_k(0, af[0]);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {
+              if (ks + 1 < 4) load_k(ks + 1, af[(ks + 1) & 1]);
+#pragma unroll
+              for (int t = 0; t < KMT; ++t)
+                ptx::mma_16816<BF>(sacc[kh * KMT + t], af[ks & 1][t], qf[kb * 4 + ks][0], qf[kb * 4 + ks][1]);
             }
             __syncwarp();  // every lane is done with the stage
             ++consumed;
@@ -551,7 +580,7 @@ __global__ void __launch_bounds__(32 * (simt_max_warps(G, sizeof(T)) + 1), 1) at
               cs = 0;
               cph ^= 1u;
             }
-            if (lane == 0) issue_next();
+            issue_next();
           }
           if (aborted) break;
 
@@ -621,16 +650,21 @@ __global__ void __launch_bounds__(32 * (simt_max_warps(G, sizeof(T)) + 1), 1) at
               break;
             }
             const uint32_t vt = ptx::smem_u32(stages + static_cast<size_t>(cs) * L.stage);
+            uint32_t af[2][VMT][4];
+            auto load_v = [&](int ks, uint32_t (&dst)[VMT][4]) {
+              const int j = ks * 2 + a_hi;
 #pragma unroll
-            for (int t = 0; t < VMT; ++t) {
-              const int r = t * 16 + a_row;
-#pragma unroll
-              for (int ks = 0; ks < MT; ++ks) {
-                const int j = ks * 2 + a_hi;
-                uint32_t a[4];
-                ptx::ldsm_x4(vt + (VSW ? r * 128 + ((j ^ (r & 7)) << 4) : cm_off(r, j, VCH)), a);
-                ptx::mma_16816<BF>(o[vg * VMT + t], a, pf[ks][0], pf[ks][1]);
+              for (int t = 0; t < VMT; ++t) {
+                const int r = t * 16 + a_row;
+                ptx::ldsm_x4(vt + (VSW ? r * 128 + ((j ^ (r & 7)) << 4) : cm_off(r, j, VCH)), dst[t]);
               }
+            };
+            load_v(0, af[0]);
+#pragma unroll
+            for (int ks = 0; ks < MT; ++ks) {
+              if (ks + 1 < MT) load_v(ks + 1, af[(ks + 1) & 1]);
+#pragma unroll
+              for (int t = 0; t < VMT; ++t) ptx::mma_16816<BF>(o[vg * VMT + t], af[ks & 1][t], pf[ks][0], pf[ks][1]);
             }
             __syncwarp();  // every lane is done with the stage (and with P^T before the next chunk)
             ++consumed;
@@ -638,7 +672,7 @@ __global__ void __launch_bounds__(32 * (simt_max_warps(G, sizeof(T)) + 1), 1) at
               cs = 0;
               cph ^= 1u;
             }
-            if (lane == 0) issue_next();
+            issue_next();
           }
         }
         if (aborted) break;
@@ -735,7 +769,7 @@ __global__ void __launch_bounds__(32 * (simt_max_warps(G, sizeof(T)) + 1), 1) at
             cs = 0;
             cph ^= 1u;
           }
-          if (lane == 0) issue_next();
+          issue_next();
         }
         if (aborted) break;
         float sc[G][KPL];
@@ -817,7 +851,7 @@ __global__ void __launch_bounds__(32 * (simt_max_warps(G, sizeof(T)) + 1), 1) at
             cs = 0;
             cph ^= 1u;
           }
-          if (lane == 0) issue_next();
+          issue_next();
         }
       }
       if (aborted) break;

@@ -121,6 +121,10 @@ struct pst_pool {
   int32_t simt_max_ctas = 0;  // cap on the CUDA-core grid; 0 = one CTA per SM
   bool simt_first = false;     // launch order of the decode step (see launch_overlapped)
   bool tc_first_forced = false;
+  int32_t tc_ctas_forced = 0;  // > 0: chunk-first CTAs when both phases run (tuning knob)
+  // sequence-first items: about T / (simt_unit_div * W) chunks each (at most
+  // kSimtInline), the last simt_tail * W chunks as single-chunk items
+  double simt_unit_div = 8.0, simt_tail = 2.0;
   int32_t simt_grid = 0, simt_stages = 3, simt_wpc = 8;
   int64_t n_part_rows = 0, shared_chunks = 0;
   std::vector<int32_t> canon_shared;   // 4 per row
@@ -499,6 +503,7 @@ pst_status rebuild(pst_pool* p) {
           k = kk;
         }
       }
+      if (p->tc_ctas_forced > 0) k = std::min({p->tc_ctas_forced, p->n_sm, n});
       // Sequence-first kernel first when the chunk-first phase is the shorter
       // one (it then waits for the first kernel without holding its SMs long).
       const double t_tc = 1.2 * std::max(w_tc / k, max_cost);
@@ -541,16 +546,22 @@ pst_status rebuild(pst_pool* p) {
   if (p->simt_max_ctas > 0) p->simt_grid = std::min(p->simt_grid, p->simt_max_ctas);
   p->n_simt_warps = p->simt_grid * p->simt_wpc;
   {
-    const int64_t W = p->n_simt_warps;
+    // W: the warps that stream from the start -- with the chunk-first
+    // kernel alongside, those on the SMs it leaves free
+    const bool beside_tc = p->n_tc_ctas > 0 && p->n_tc_ctas < p->n_sm;
+    const int64_t W =
+        static_cast<int64_t>(beside_tc ? std::min(p->simt_grid, p->n_sm - p->n_tc_ctas) : p->simt_grid) * p->simt_wpc;
     const int32_t unit = std::min<int32_t>(
-        kSimtInline, p->simt_unit > 0 ? p->simt_unit : static_cast<int32_t>(std::max<int64_t>(1, T / (8 * W))));
+        kSimtInline,
+        p->simt_unit > 0 ? p->simt_unit : static_cast<int32_t>(std::max<int64_t>(
+                                          1, static_cast<int64_t>(static_cast<double>(T) / (p->simt_unit_div * W)))));
     std::vector<Stream> units;
     for (const auto& st : streams)
       for (int32_t a = 0; a < st.n; a += unit) units.push_back({st.chunk_off + a, std::min(unit, st.n - a), st.kv, st.group});
     std::stable_sort(units.begin(), units.end(), [](const Stream& x, const Stream& y) { return x.n > y.n; });
     int64_t tail = 0;
     size_t cut = units.size();
-    while (cut > 0 && tail < 2 * W) tail += units[--cut].n;
+    while (cut > 0 && static_cast<double>(tail) < p->simt_tail * W) tail += units[--cut].n;
     std::vector<Stream> ordered(units.begin(), units.begin() + cut);
     for (size_t x = cut; x < units.size(); ++x)
       for (int32_t a = 0; a < units[x].n; ++a) ordered.push_back({units[x].chunk_off + a, 1, units[x].kv, units[x].group});
@@ -713,6 +724,9 @@ pst_status pst_pool_create(const pst_config* cfg, int device, pst_pool** out) {
   if (const char* e = std::getenv("PST_HBM_GBS")) p->hbm_gbs = std::atof(e);
   if (const char* e = std::getenv("PST_SIMT_UNIT")) p->simt_unit = std::atoi(e);
   if (const char* e = std::getenv("PST_TC_FIRST")) p->tc_first_forced = std::atoi(e) != 0;
+  if (const char* e = std::getenv("PST_TC_CTAS")) p->tc_ctas_forced = std::max(0, std::atoi(e));
+  if (const char* e = std::getenv("PST_SIMT_UNIT_DIV")) p->simt_unit_div = std::max(0.25, std::atof(e));
+  if (const char* e = std::getenv("PST_SIMT_TAIL")) p->simt_tail = std::max(0.0, std::atof(e));
   // CUDA-core kernel shape: up to 8 consumer warps (plus the producer warp)
   // x 6 stages of 4 KB pieces, as far as shared memory allows
   p->simt_wpc = attn_simt_max_warps(c.dtype, g);
