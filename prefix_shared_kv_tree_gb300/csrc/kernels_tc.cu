@@ -13,23 +13,27 @@
 // mbarriers are set up once and the pipelines run across item boundaries.
 // Warp roles:
 //   warp 0      : producer.  Lane 0 moves each chunk's 32 KB K + V^T tile image
-//                 from the pool into a 4-stage shared-memory ring with one bulk
+//                 from the pool into a 5-stage shared-memory ring with one bulk
 //                 async copy (TMA engine); the pool already stores tiles in the
-//                 tensor cores' 128-byte-swizzled K-major layout, and Q and P
-//                 are written in the same layout.
+//                 tensor cores' 128-byte-swizzled K-major layout, and Q is
+//                 written in the same layout.
 //   warp 6      : gathers the next item's query rows into the other half of a
 //                 double-buffered Q tile while the current item computes.
-//   warp 1      : allocates TMEM; the whole warp runs the issue loop and one
-//                 elected lane issues tcgen05.mma: S = Q K^T (M=128, N=64,
-//                 K=D, double-buffered in TMEM) and O += P V (M=128, N=D,
-//                 K=64) into the item's O buffer (double-buffered by item),
-//                 and commits to mbarriers.
+//   warp 1      : allocates TMEM and issues S = Q K^T (M=128, N=64, K=D) into
+//                 three TMEM buffers, as far ahead of the softmax as they allow,
+//                 across item boundaries.
+//   warp 7      : issues O += P V (M=128, N=D, K=64, A = P read from TMEM) into
+//                 the item's O buffer (double-buffered by item).
+//                 Both issuer warps run their loops whole; one elected lane
+//                 issues each tcgen05 instruction and commit.  Two issuers,
+//                 because one thread's stream of MMAs and commits for a chunk
+//                 takes longer than the tensor cores need for it.
 //   warps 2..5  : one thread per query row: read S from TMEM, online softmax in
 //                 log2 units against a reference max that moves only when a
 //                 chunk's max passes it by more than 2^8 (then O and the row
 //                 sum are rescaled in TMEM), write the rounded probabilities P
-//                 to shared memory as the A operand of the PV product, and at
-//                 the item's end stream O out of TMEM: the item's partial rows
+//                 into TMEM as the A operand of the PV product, and at the
+//                 item's end stream O out of TMEM: the item's partial rows
 //                 (the merge kernel combines them) or, for a prefill block, the
 //                 normalised output rows.
 // Every wait is bounded; on a timeout the CTA records an error, drains its
@@ -51,13 +55,13 @@ namespace {
 
 constexpr int kC = 64;     // tokens per chunk
 constexpr int kBM = 128;   // stacked query rows per item
-constexpr int kNS = 4;     // K/V tile stages
+constexpr int kNS = 5;     // K/V tile stages
+constexpr int kSB = 3;     // S buffers in TMEM: S runs kSB - 1 chunks ahead of the PV product
 
 __host__ __device__ constexpr uint32_t tc_tile_bytes(int D) { return 2u * kC * D * 2u; }
 __host__ __device__ constexpr uint32_t tc_q_bytes(int D) { return kBM * D * 2u; }
-__host__ __device__ constexpr uint32_t tc_p_bytes() { return kBM * kC * 2u; }
 __host__ __device__ constexpr size_t tc_smem_bytes(int D) {
-  return 1024 + 2 * tc_q_bytes(D) + kNS * tc_tile_bytes(D) + 2 * tc_p_bytes() + 256;
+  return 1024 + 2 * tc_q_bytes(D) + kNS * tc_tile_bytes(D) + 320;
 }
 
 template <typename T>
@@ -72,16 +76,20 @@ __device__ __forceinline__ uint32_t pack2_plain(float a, float b) {
 }
 
 template <typename T, int D>
-__global__ void __launch_bounds__(224, 1) attn_tc_kernel(const AttnParams p) {
+__global__ void __launch_bounds__(256, 1) attn_tc_kernel(const AttnParams p) {
   constexpr uint32_t HALF = kC * D * 2;
   constexpr uint32_t TILE = tc_tile_bytes(D);
   constexpr uint32_t QB = tc_q_bytes(D);
-  constexpr uint32_t PB = tc_p_bytes();
   constexpr int DCH = D / 8;    // 16-byte chunks per row when the reduction runs over D
   constexpr int CCH = kC / 8;   // 16-byte chunks per row when the reduction runs over keys
-  constexpr uint32_t TMEM_COLS = (128 + 2 * D) <= 256 ? 256u : 512u;
-  constexpr uint32_t S_COL = 0;    // S double buffer: columns [0, 64), [64, 128)
-  constexpr uint32_t O_COL = 128;  // O of an item, double-buffered by item: [128, 128 + D), [128 + D, 128 + 2D)
+  constexpr uint32_t S_COL = 0;  // S buffers: columns [kC b, kC b + kC), b < kSB
+  // O of an item, double-buffered by item: [O_COL, O_COL + D), [O_COL + D, O_COL + 2D)
+  constexpr uint32_t O_COL = kSB * kC;
+  // P double buffer, the A operand of the PV product: a row's kC 16-bit
+  // probabilities packed two per column, [P_COL, P_COL + 32), [.. + 32, .. + 64)
+  constexpr uint32_t P_COL = O_COL + 2 * D;
+  constexpr uint32_t TMEM_COLS = (P_COL + kC) <= 256 ? 256u : 512u;
+  static_assert(P_COL + kC <= 512, "tensor memory columns");
   constexpr bool BF = std::is_same<T, __nv_bfloat16>::value;
   constexpr uint32_t ID_S = ptx::idesc_f16(kBM, kC, BF);
   constexpr uint32_t ID_O = ptx::idesc_f16(kBM, D, BF);
@@ -90,20 +98,19 @@ __global__ void __launch_bounds__(224, 1) attn_tc_kernel(const AttnParams p) {
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* qs = smem;                 // [2] Q tiles
   uint8_t* kvs = qs + 2 * QB;         // [kNS] K + V^T tiles
-  uint8_t* ps = kvs + kNS * TILE;     // [2] P tiles
-  uint64_t* bars = reinterpret_cast<uint64_t*>(ps + 2 * PB);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(kvs + kNS * TILE);
   uint64_t* full = bars;             // [kNS] tile landed
   uint64_t* empty = bars + kNS;      // [kNS] tile no longer read by the tensor cores
   uint64_t* qfull = bars + 2 * kNS;  // [2] Q tile written (32 Q-loader lanes)
   uint64_t* qfree = qfull + 2;       // [2] Q tile no longer read by the tensor cores
-  uint64_t* sfull = qfree + 2;       // [2] S ready in TMEM
-  uint64_t* sfree = sfull + 2;       // [2] S read by the softmax threads (128)
-  uint64_t* pfull = sfree + 2;       // [2] P written, O rescaled if needed (128)
+  uint64_t* sfull = qfree + 2;       // [kSB] S ready in TMEM
+  uint64_t* sfree = sfull + kSB;     // [kSB] S read by the softmax threads (128)
+  uint64_t* pfull = sfree + kSB;     // [2] P written, O rescaled if needed (128)
   uint64_t* pfree = pfull + 2;       // [2] the PV product that read P buffer b has completed
   uint64_t* ofull = pfree + 2;       // [2] every PV product of an item has completed (O buffer by item)
   uint64_t* oempty = ofull + 2;      // [2] the item's O was read out (128)
-  uint64_t* done = oempty + 2;       // all MMAs of this CTA completed
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+  uint64_t* done = oempty + 2;       // [2] all MMAs of the S / PV issuer completed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* issued_slot = abort_flag + 1;
   volatile int* consumed_slot = abort_flag + 2;
@@ -119,17 +126,20 @@ __global__ void __launch_bounds__(224, 1) attn_tc_kernel(const AttnParams p) {
       ptx::mbar_init(&full[s], 1);
       ptx::mbar_init(&empty[s], 1);
     }
+    for (int b = 0; b < kSB; ++b) {
+      ptx::mbar_init(&sfull[b], 1);
+      ptx::mbar_init(&sfree[b], 128);
+    }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(&qfull[b], 32);
       ptx::mbar_init(&qfree[b], 1);
-      ptx::mbar_init(&sfull[b], 1);
-      ptx::mbar_init(&sfree[b], 128);
       ptx::mbar_init(&pfull[b], 128);
       ptx::mbar_init(&pfree[b], 1);
       ptx::mbar_init(&ofull[b], 1);
       ptx::mbar_init(&oempty[b], 128);
     }
-    ptx::mbar_init(done, 1);
+    ptx::mbar_init(&done[0], 1);
+    ptx::mbar_init(&done[1], 1);
     *abort_flag = 0;
     *issued_slot = 0;
     *consumed_slot = 0;
@@ -201,22 +211,21 @@ __global__ void __launch_bounds__(224, 1) attn_tc_kernel(const AttnParams p) {
       ptx::fence_proxy_async_smem();
       ptx::mbar_arrive(&qfull[qb]);
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    // The whole warp runs this loop (operands stay warp-uniform); one
-    // elected lane issues each tcgen05 instruction.
+  } else if (warp == 1 || warp == 7) {
+    // ---------------------------------------------------- MMA issuers (S, PV)
+    // The whole warp runs its loop (operands stay warp-uniform); one elected
+    // lane issues each tcgen05 instruction.
     {
       const uint32_t q_addr = ptx::smem_u32(qs);
       const uint32_t kv_addr = ptx::smem_u32(kvs);
-      const uint32_t p_addr = ptx::smem_u32(ps);
       auto wait_all = [&](uint64_t* bar, uint32_t parity) {
         return __all_sync(0xffffffffu, ptx::mbar_wait(bar, parity, abort_flag, p.err));
       };
       auto issue_s = [&](int t, int qb) -> bool {
-        const int s = t % kNS, b = t & 1;
+        const int s = t % kNS, b = t % kSB;
         if (!wait_all(&full[s], (t / kNS) & 1)) return false;
         if (lane == 0) *consumed_slot = t + 1;
-        if (t >= 2 && !wait_all(&sfree[b], ((t - 2) >> 1) & 1)) return false;
+        if (t >= kSB && !wait_all(&sfree[b], ((t - kSB) / kSB) & 1)) return false;
         ptx::tc_fence_after();
         // Descriptors of each K step = the tile's base descriptor + the step's
         // byte offset / 16 (the 14-bit start-address field never carries).
@@ -240,37 +249,52 @@ __global__ void __launch_bounds__(224, 1) attn_tc_kernel(const AttnParams p) {
         if (!wait_all(&pfull[b], (t >> 1) & 1)) return false;
         if (c == 0 && it >= 2 && !wait_all(&oempty[ob], ((it - 2) >> 1) & 1)) return false;
         ptx::tc_fence_after();
-        const uint64_t a0 = ptx::smem_desc_sw128(p_addr + b * PB, 1024);
         const uint64_t b0 = ptx::smem_desc_sw128(kv_addr + s * TILE + HALF, 1024);
 #pragma unroll
-        for (int kk = 0; kk < kC / 16; ++kk)
-          ptx::mma_f16_warp(tbase + O_COL + ob * D, a0 + kk * 2, b0 + kk * 2, ID_O, (c > 0 || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < kC / 16; ++kk)  // K step kk: keys [16kk, 16kk+16) = P columns [8kk, 8kk+8)
+          ptx::mma_f16_tmem_a_warp(tbase + O_COL + ob * D, tbase + P_COL + b * 32 + kk * 8, b0 + kk * 2, ID_O,
+                                   (c > 0 || kk > 0) ? 1u : 0u);
         ptx::mma_commit_warp(&pfree[b]);
         ptx::mma_commit_warp(&empty[s]);
         if (last) ptx::mma_commit_warp(&ofull[ob]);
         return true;
       };
-      int t = 0;
+      // S runs over this CTA's chunk sequence (across item boundaries) as far
+      // ahead as the kSB S buffers allow, so the softmax threads find each S
+      // ready when they finish the previous chunk.
+      int s_ii = i0, s_c = 0, s_t = 0;
+      int s_nk = i0 < i1 ? p.items[i0].n_chunks : 0;
+      auto issue_next_s = [&]() -> bool {
+        const int it = s_ii - i0, qb = it & 1;
+        if (s_c == 0) {  // the item's Q tile
+          if (!wait_all(&qfull[qb], (it >> 1) & 1)) return false;
+          ptx::tc_fence_after();
+        }
+        if (!issue_s(s_t, qb)) return false;
+        if (s_c + 1 == s_nk) ptx::mma_commit_warp(&qfree[qb]);  // every S of this item is issued
+        ++s_t;
+        if (++s_c == s_nk) {
+          s_c = 0;
+          ++s_ii;
+          s_nk = s_ii < i1 ? p.items[s_ii].n_chunks : 0;
+        }
+        return true;
+      };
       bool ok = true;
-      for (int ii = i0; ii < i1 && ok; ++ii) {
-        const int it = ii - i0, qb = it & 1;
-        const int nk = p.items[ii].n_chunks;
-        ok = wait_all(&qfull[qb], (it >> 1) & 1);
-        if (!ok) break;
-        ptx::tc_fence_after();
-        ok = issue_s(t, qb);
-        for (int c = 0; c < nk && ok; ++c, ++t) {
-          if (c + 1 < nk) {
-            ok = issue_s(t + 1, qb);
-          } else {
-            ptx::mma_commit_warp(&qfree[qb]);  // every S of this item is issued
-          }
-          if (ok) ok = issue_pv(t, it, c, c + 1 == nk);
+      if (warp == 1) {
+        while (ok && s_ii < i1) ok = issue_next_s();
+      } else {
+        int t = 0;
+        for (int ii = i0; ii < i1 && ok; ++ii) {
+          const int it = ii - i0;
+          const int nk = p.items[ii].n_chunks;
+          for (int c = 0; c < nk && ok; ++c, ++t) ok = issue_pv(t, it, c, c + 1 == nk);
         }
       }
-      // Every MMA of this CTA must have finished before TMEM is released.
-      ptx::mma_commit_warp(done);
-      ptx::mbar_wait(done, 0, nullptr, p.err);
+      // Every MMA of this issuer must have finished before TMEM is released.
+      uint64_t* my_done = &done[warp == 1 ? 0 : 1];
+      ptx::mma_commit_warp(my_done);
+      ptx::mbar_wait(my_done, 0, nullptr, p.err);
     }
     __syncwarp();
   } else if (warp >= 2 && warp <= 5) {
@@ -307,19 +331,19 @@ __global__ void __launch_bounds__(224, 1) attn_tc_kernel(const AttnParams p) {
           if (c + lane < nk) my_len = p.chunk_len[p.chunks[w.chunk_off + c + lane]];
         }
         const int lim = min(__shfl_sync(0xffffffffu, my_len, c & 31), key_limit - c * kC);
-        const int b = t & 1;
-        if (!ptx::mbar_wait(&sfull[b], (t >> 1) & 1, abort_flag, p.err)) {
+        const int b = t & 1, sb = t % kSB;
+        if (!ptx::mbar_wait(&sfull[sb], (t / kSB) & 1, abort_flag, p.err)) {
           ok = false;
           break;
         }
         ptx::tc_fence_after();
         uint32_t sv0[32], sv1[32];
-        ptx::tmem_ld32(tl + S_COL + b * kC, sv0);
-        ptx::tmem_ld32(tl + S_COL + b * kC + 32, sv1);
+        ptx::tmem_ld32(tl + S_COL + sb * kC, sv0);
+        ptx::tmem_ld32(tl + S_COL + sb * kC + 32, sv1);
         ptx::tmem_ld_wait(sv0);
         ptx::tmem_ld_wait(sv1);
         ptx::tc_fence_before();
-        ptx::mbar_arrive(&sfree[b]);
+        ptx::mbar_arrive(&sfree[sb]);
 
         // Raw scores; the chunk max is taken before scaling (the scale is
         // positive), and the scale is folded into the exponent's FMA below.
@@ -371,7 +395,7 @@ __global__ void __launch_bounds__(224, 1) attn_tc_kernel(const AttnParams p) {
         // rounded to the operand type (two partial sums for a shorter chain).
         const float neg_m = -m_use, sc = p.scale_log2;
         float ps0 = 0.f, ps1 = 0.f;
-        uint8_t* prow = ps + b * PB;
+        uint32_t pw[kC / 2];
 #pragma unroll
         for (int j = 0; j < CCH; ++j) {
           float e[8];
@@ -379,16 +403,13 @@ __global__ void __launch_bounds__(224, 1) attn_tc_kernel(const AttnParams p) {
           for (int q = 0; q < 8; ++q) e[q] = ptx::ex2(fmaf(x[8 * j + q], sc, neg_m));
           ps0 += (e[0] + e[1]) + (e[2] + e[3]);
           ps1 += (e[4] + e[5]) + (e[6] + e[7]);
-          uint4 pk;
-          pk.x = pack2_plain<T>(e[0], e[1]);
-          pk.y = pack2_plain<T>(e[2], e[3]);
-          pk.z = pack2_plain<T>(e[4], e[5]);
-          pk.w = pack2_plain<T>(e[6], e[7]);
-          *reinterpret_cast<uint4*>(prow + r * 128 + ((j ^ (r & 7)) << 4)) = pk;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) pw[4 * j + q] = pack2_plain<T>(e[2 * q], e[2 * q + 1]);
         }
         const float psum = ps0 + ps1;
-        ptx::fence_proxy_async_smem();
-        ptx::tc_fence_before();  // orders any TMEM stores above before the PV product
+        ptx::tmem_st32(tl + P_COL + b * 32, pw);
+        ptx::tmem_st_wait();
+        ptx::tc_fence_before();  // orders the TMEM stores above before the PV product
         ptx::mbar_arrive(&pfull[b]);
         l += psum;
       }
@@ -454,7 +475,7 @@ cudaError_t launch_tc_t(const AttnParams& p, int grid, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(224);
+  cfg.blockDim = dim3(256);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];

@@ -116,7 +116,11 @@ struct pst_pool {
   // of an item, one CUDA-core tile when the phases run on split SMs, the
   // DRAM rate one SM of the CUDA-core kernel sustains (query groups of one),
   // and the whole GPU's.
-  double tc_chunk_us = 1.8, tc_item_us = 1.0, simt_tile_us = 0.75, simt_sm_gbs = 60.0, hbm_gbs = 6500.0;
+  // SM-split model: chunk-first cost per chunk (plus tc_hbm_us when the item
+  // is the first row tile of its run, i.e. its tiles come from DRAM, not L2)
+  // and per item; sequence-first bytes per microsecond per SM; DRAM rate
+  double tc_chunk_us = 1.1, tc_hbm_us = 0.3, tc_item_us = 1.0, simt_tile_us = 0.75, simt_sm_gbs = 60.0,
+         hbm_gbs = 6500.0;
   int32_t simt_unit = 0;      // CUDA-core work-item size in chunks; 0 = automatic
   int32_t simt_max_ctas = 0;  // cap on the CUDA-core grid; 0 = one CTA per SM
   bool simt_first = false;     // launch order of the decode step (see launch_overlapped)
@@ -472,7 +476,8 @@ pst_status rebuild(pst_pool* p) {
     std::vector<double> cost(n);
     double w_tc = 0;
     for (int32_t x = 0; x < n; ++x) {
-      cost[x] = tc_items[8 * x + 1] * p->tc_chunk_us + p->tc_item_us;
+      const bool first_tile = tc_items[8 * x + 4] == 0;  // row0: the run's first row tile reads its tiles from DRAM
+      cost[x] = tc_items[8 * x + 1] * (p->tc_chunk_us + (first_tile ? p->tc_hbm_us : 0.0)) + p->tc_item_us;
       w_tc += cost[x];
     }
     const double max_cost = *std::max_element(cost.begin(), cost.end());
@@ -718,6 +723,7 @@ pst_status pst_pool_create(const pst_config* cfg, int device, pst_pool** out) {
   for (int64_t x = c.max_chunks - 1; x >= 0; --x) p->free_chunks.push_back(static_cast<int32_t>(x));
 
   if (const char* e = std::getenv("PST_TC_CHUNK_US")) p->tc_chunk_us = std::atof(e);
+  if (const char* e = std::getenv("PST_TC_HBM_US")) p->tc_hbm_us = std::atof(e);
   if (const char* e = std::getenv("PST_SIMT_TILE_US")) p->simt_tile_us = std::atof(e);
   if (const char* e = std::getenv("PST_TC_ITEM_US")) p->tc_item_us = std::atof(e);
   if (const char* e = std::getenv("PST_SIMT_SM_GBS")) p->simt_sm_gbs = std::atof(e);

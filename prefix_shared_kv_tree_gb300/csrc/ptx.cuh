@@ -245,6 +245,20 @@ __device__ __forceinline__ void mma_f16_warp(uint32_t d_tmem, uint64_t adesc, ui
       : "memory");
 }
 
+// As mma_f16_warp with the A operand in tensor memory: M = 128 rows in lanes
+// 0..127, row m's K 16-bit elements packed two per 32-bit column from a_tmem
+// (element k in column k / 2, the even one in the low half).
+__device__ __forceinline__ void mma_f16_tmem_a_warp(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                                    uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Commit by the lane elect.sync picks in a whole converged warp (the same lane
 // that issued the MMAs through mma_f16_warp).
 __device__ __forceinline__ void mma_commit_warp(uint64_t* bar) {
