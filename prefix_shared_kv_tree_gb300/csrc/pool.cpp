@@ -126,9 +126,11 @@ struct pst_pool {
   bool simt_first = false;     // launch order of the decode step (see launch_overlapped)
   bool tc_first_forced = false;
   int32_t tc_ctas_forced = 0;  // > 0: chunk-first CTAs when both phases run (tuning knob)
-  // sequence-first items: about T / (simt_unit_div * W) chunks each (at most
-  // kSimtInline), the last simt_tail * W chunks as single-chunk items
+  // sequence-first items: about sqrt(g) * T / (simt_unit_div * W) chunks each
+  // (at most kSimtInline; an item's set-up and partial rows grow with g), the
+  // last simt_tail * W chunks as single-chunk items
   double simt_unit_div = 8.0, simt_tail = 2.0;
+  int32_t tc_max_run = 32;  // chunk-first items: at most this many chunks
   int32_t simt_grid = 0, simt_stages = 3, simt_wpc = 8;
   int64_t n_part_rows = 0, shared_chunks = 0;
   std::vector<int32_t> canon_shared;   // 4 per row
@@ -410,7 +412,7 @@ pst_status rebuild(pst_pool* p) {
   // back to back; fewer, longer ones when they share the GPU
   const int64_t split1 = (p->cfg.flags & PST_FLAG_CONCURRENT_PHASES)
                              ? 8
-                             : std::min<int64_t>(16, std::max<int64_t>(2, ceil_div(p1_iters, std::max(1, p->n_sm))));
+                             : std::min<int64_t>(p->tc_max_run, std::max<int64_t>(2, ceil_div(p1_iters, std::max(1, p->n_sm))));
   for (const auto& r : runs) {
     const int32_t i = ni[r.front()], j = nj[r.front()];
     const int32_t rows = (j - i) * g;
@@ -558,8 +560,10 @@ pst_status rebuild(pst_pool* p) {
         static_cast<int64_t>(beside_tc ? std::min(p->simt_grid, p->n_sm - p->n_tc_ctas) : p->simt_grid) * p->simt_wpc;
     const int32_t unit = std::min<int32_t>(
         kSimtInline,
-        p->simt_unit > 0 ? p->simt_unit : static_cast<int32_t>(std::max<int64_t>(
-                                          1, static_cast<int64_t>(static_cast<double>(T) / (p->simt_unit_div * W)))));
+        p->simt_unit > 0 ? p->simt_unit
+                         : static_cast<int32_t>(std::max<int64_t>(
+                               1, static_cast<int64_t>(static_cast<double>(T) * std::sqrt(static_cast<double>(g)) /
+                                                       (p->simt_unit_div * W)))));
     std::vector<Stream> units;
     for (const auto& st : streams)
       for (int32_t a = 0; a < st.n; a += unit) units.push_back({st.chunk_off + a, std::min(unit, st.n - a), st.kv, st.group});
@@ -732,6 +736,7 @@ pst_status pst_pool_create(const pst_config* cfg, int device, pst_pool** out) {
   if (const char* e = std::getenv("PST_TC_FIRST")) p->tc_first_forced = std::atoi(e) != 0;
   if (const char* e = std::getenv("PST_TC_CTAS")) p->tc_ctas_forced = std::max(0, std::atoi(e));
   if (const char* e = std::getenv("PST_SIMT_UNIT_DIV")) p->simt_unit_div = std::max(0.25, std::atof(e));
+  if (const char* e = std::getenv("PST_TC_MAX_RUN")) p->tc_max_run = std::max(2, std::atoi(e));
   if (const char* e = std::getenv("PST_SIMT_TAIL")) p->simt_tail = std::max(0.0, std::atof(e));
   // CUDA-core kernel shape: up to 8 consumer warps (plus the producer warp)
   // x 6 stages of 4 KB pieces, as far as shared memory allows
