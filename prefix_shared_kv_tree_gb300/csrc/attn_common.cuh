@@ -185,4 +185,66 @@ __device__ __forceinline__ void merge_task(const AttnParams& p, int key, int e0,
   }
 }
 
+// merge_task with every entry block of the pair staged in shared memory by
+// 16-byte asynchronous copies through L2 (all of them in flight at once, no
+// registers held), then the same arithmetic in the same order.  buf holds
+// cnt * G * D floats; cnt * G <= 32 (one round of (m, n) pairs).
+template <typename T, int D, int G>
+__device__ __forceinline__ void merge_task_staged(const AttnParams& p, int key, int e0, int e1, int lane,
+                                                  float4* buf) {
+  constexpr int RF = D / 4;
+  constexpr int F4 = G * RF;
+  constexpr int NI = (F4 + 31) / 32;
+  const int cnt = e1 - e0;
+  const float4* po = reinterpret_cast<const float4*>(p.part_o) + static_cast<size_t>(e0) * F4;
+  const uint32_t sb = ptx::smem_u32(buf);
+  for (int x = lane; x < cnt * F4; x += 32)
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sb + x * 16), "l"(po + x) : "memory");
+  asm volatile("cp.async.commit_group;" ::: "memory");
+  const float2* ml = reinterpret_cast<const float2*>(p.part_ml) + static_cast<size_t>(e0) * G;
+  const float2 mn = lane < cnt * G ? __ldcg(ml + lane) : make_float2(-INFINITY, 0.f);
+  int hg_i[NI];
+#pragma unroll
+  for (int i = 0; i < NI; ++i) hg_i[i] = min((lane + 32 * i) / RF, G - 1);
+  float mx = mn.x;
+#pragma unroll
+  for (int s = G; s < 32; s <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, s));
+  const float w = mn.x == -INFINITY ? 0.f : ptx::ex2(mn.x - mx);  // an entry with no valid key adds nothing
+  float nn = w * mn.y;
+#pragma unroll
+  for (int s = G; s < 32; s <<= 1) nn += __shfl_xor_sync(0xffffffffu, nn, s);
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
+  __syncwarp();
+  float4 acc[NI];
+#pragma unroll
+  for (int i = 0; i < NI; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int j = 0; j < cnt; ++j) {
+#pragma unroll
+    for (int i = 0; i < NI; ++i) {
+      const float wj = __shfl_sync(0xffffffffu, w, j * G + hg_i[i]);
+      if (lane + 32 * i < F4) {
+        const float4 t = buf[j * F4 + lane + 32 * i];
+        acc[i].x = fmaf(wj, t.x, acc[i].x);
+        acc[i].y = fmaf(wj, t.y, acc[i].y);
+        acc[i].z = fmaf(wj, t.z, acc[i].z);
+        acc[i].w = fmaf(wj, t.w, acc[i].w);
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < NI; ++i) {
+    const float inv = 1.f / __shfl_sync(0xffffffffu, nn, hg_i[i]);
+    const int f = lane + 32 * i;
+    if (f < F4) {
+      T* out = static_cast<T*>(p.out) + (static_cast<size_t>(key) * G + f / RF) * D + (f % RF) * 4;
+      if constexpr (sizeof(T) == 2) {
+        *reinterpret_cast<uint2*>(out) =
+            make_uint2(pack2_16<T>(acc[i].x * inv, acc[i].y * inv), pack2_16<T>(acc[i].z * inv, acc[i].w * inv));
+      } else {
+        *reinterpret_cast<float4*>(out) = make_float4(acc[i].x * inv, acc[i].y * inv, acc[i].z * inv, acc[i].w * inv);
+      }
+    }
+  }
+}
+
 }  // namespace pst

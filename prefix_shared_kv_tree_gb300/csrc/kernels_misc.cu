@@ -100,8 +100,10 @@ __global__ void __launch_bounds__(256) gather_kernel(const ScatterParams p, int 
 // Merge (ChunkAttention, Knowl 3: attn_reduce over all partial rows of a
 // query row, then O = o / n).  One warp per (batch row, KV head) pair; the
 // partials come from the chunk-first and sequence-first kernels that precede
-// it on the stream.  Launched as a programmatic dependent: it becomes
-// resident while they run and waits for their completion before reading.
+// it on the stream.  A pair with at most merge_cap entries stages them in the
+// warp's part of shared memory, all copies in flight at once.  Launched as a
+// programmatic dependent: it becomes resident while they run and waits for
+// their completion before reading.
 // ---------------------------------------------------------------------------
 template <typename T, int D, int G>
 __global__ void __launch_bounds__(128) merge_kernel(const AttnParams p, int B) {
@@ -114,16 +116,34 @@ __global__ void __launch_bounds__(128) merge_kernel(const AttnParams p, int B) {
     e1 = __ldg(p.m_off + key + 1);
   }
   if (p.pdl) ptx::pdl_wait();
-  if (live) merge_task<T, D, G>(p, key, e0, e1, lane);
+  if (live) {
+    extern __shared__ float4 merge_smem[];
+    if (e1 - e0 <= p.merge_cap)
+      merge_task_staged<T, D, G>(p, key, e0, e1, lane, merge_smem + static_cast<size_t>(warp) * p.merge_cap * (G * D / 4));
+    else
+      merge_task<T, D, G>(p, key, e0, e1, lane);
+  }
+}
+
+template <typename T, int D, int G>
+cudaError_t launch_merge_g(cudaLaunchConfig_t cfg, const AttnParams& p, int B) {
+  auto fn = merge_kernel<T, D, G>;
+  cfg.dynamicSmemBytes = static_cast<size_t>(4) * p.merge_cap * G * D * sizeof(float);
+  if (cfg.dynamicSmemBytes > 48 * 1024) {
+    const cudaError_t e =
+        cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(cfg.dynamicSmemBytes));
+    if (e != cudaSuccess) return e;
+  }
+  return cudaLaunchKernelEx(&cfg, fn, p, B);
 }
 
 template <typename T, int D>
 cudaError_t launch_merge_d(const cudaLaunchConfig_t& cfg, int g, const AttnParams& p, int B) {
   switch (g) {
-    case 1: return cudaLaunchKernelEx(&cfg, merge_kernel<T, D, 1>, p, B);
-    case 2: return cudaLaunchKernelEx(&cfg, merge_kernel<T, D, 2>, p, B);
-    case 4: return cudaLaunchKernelEx(&cfg, merge_kernel<T, D, 4>, p, B);
-    case 8: return cudaLaunchKernelEx(&cfg, merge_kernel<T, D, 8>, p, B);
+    case 1: return launch_merge_g<T, D, 1>(cfg, p, B);
+    case 2: return launch_merge_g<T, D, 2>(cfg, p, B);
+    case 4: return launch_merge_g<T, D, 4>(cfg, p, B);
+    case 8: return launch_merge_g<T, D, 8>(cfg, p, B);
   }
   return cudaErrorInvalidValue;
 }

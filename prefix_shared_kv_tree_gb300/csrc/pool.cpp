@@ -131,6 +131,7 @@ struct pst_pool {
   // last simt_tail * W chunks as single-chunk items
   double simt_unit_div = 8.0, simt_tail = 2.0;
   int32_t tc_max_run = 32;  // chunk-first items: at most this many chunks
+  int32_t merge_cap = 0, merge_cap_forced = -1;
   int32_t simt_grid = 0, simt_stages = 3, simt_wpc = 8;
   int64_t n_part_rows = 0, shared_chunks = 0;
   std::vector<int32_t> canon_shared;   // 4 per row
@@ -589,6 +590,16 @@ pst_status rebuild(pst_pool* p) {
   for (const auto& e : ents) moff[e.key + 1]++;
   for (size_t x = 1; x < moff.size(); ++x) moff[x] += moff[x - 1];
   {
+    // merge: pairs with up to merge_cap entries stage them in shared memory
+    // (G rows of d floats per entry, 4 warps per CTA, at most 64 KiB, and
+    // one round of 32 (m, n) pairs)
+    int32_t max_ent = 0;
+    for (size_t x = 0; x + 1 < moff.size(); ++x) max_ent = std::max(max_ent, moff[x + 1] - moff[x]);
+    const int32_t by_smem = static_cast<int32_t>((64 * 1024) / (4 * static_cast<size_t>(g) * p->D * sizeof(float)));
+    p->merge_cap = std::min({max_ent, by_smem, 32 / g});
+    if (p->merge_cap_forced >= 0) p->merge_cap = std::min(p->merge_cap, p->merge_cap_forced);
+  }
+  {
     std::vector<int32_t> fill(moff.begin(), moff.end() - 1);
     for (const auto& e : ents) {
       const int32_t slot = fill[e.key]++;
@@ -681,6 +692,7 @@ AttnParams base_params(const pst_pool* p) {
   a.warps_per_cta = p->simt_wpc;
   a.err = p->d_err;
   a.sched = p->d_sched;
+  a.merge_cap = p->merge_cap;
   return a;
 }
 
@@ -737,6 +749,7 @@ pst_status pst_pool_create(const pst_config* cfg, int device, pst_pool** out) {
   if (const char* e = std::getenv("PST_TC_CTAS")) p->tc_ctas_forced = std::max(0, std::atoi(e));
   if (const char* e = std::getenv("PST_SIMT_UNIT_DIV")) p->simt_unit_div = std::max(0.25, std::atof(e));
   if (const char* e = std::getenv("PST_TC_MAX_RUN")) p->tc_max_run = std::max(2, std::atoi(e));
+  if (const char* e = std::getenv("PST_MERGE_CAP")) p->merge_cap_forced = std::max(0, std::atoi(e));
   if (const char* e = std::getenv("PST_SIMT_TAIL")) p->simt_tail = std::max(0.0, std::atof(e));
   // CUDA-core kernel shape: up to 8 consumer warps (plus the producer warp)
   // x 6 stages of 4 KB pieces, as far as shared memory allows

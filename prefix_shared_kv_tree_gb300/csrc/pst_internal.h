@@ -99,6 +99,9 @@ struct AttnParams {
   // take the L2 evict-first priority, so the streamed tiles do not push the
   // partial rows that the merge reads next out of L2.
   int32_t kv_evict_first;
+  // merge kernel: pairs with at most this many entries stage them in shared
+  // memory (0: none do)
+  int32_t merge_cap;
   // 1: launched as a programmatic dependent of the previous kernel on the
   // stream (it may start while that kernel drains; it must not finish first)
   int32_t pdl;
