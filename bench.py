@@ -45,6 +45,7 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--min-share", type=int, default=0)
     ap.add_argument("--flags", type=int, default=0)
+    ap.add_argument("--loop-steps", type=int, default=128, help="decode-loop steps (0: skip)")
     return ap.parse_args()
 
 
@@ -264,6 +265,7 @@ def run_ours(args):
         torch.cuda.set_device(0)
     dev = torch.cuda.current_device()
 
+    import numpy as np
     from prefix_shared_kv_tree_gb300 import build as B
     B.build_library()
     from prefix_shared_kv_tree_gb300 import pst
@@ -276,7 +278,9 @@ def run_ours(args):
     for n, fan in spec.levels:
         mult *= fan
         chunks += mult * math.ceil(n / spec.chunk_size)
-    pool = pst.Pool(spec.n_q_heads, spec.n_kv_heads, spec.head_dim, spec.chunk_size, chunks + 64, spec.dtype,
+    # spare chunks for the decode loop's appends (a new leaf chunk every c steps)
+    spare = 64 + spec.n_sequences * (2 + args.loop_steps // spec.chunk_size)
+    pool = pst.Pool(spec.n_q_heads, spec.n_kv_heads, spec.head_dim, spec.chunk_size, chunks + spare, spec.dtype,
                     args.min_share, 0, args.flags, device=dev)
     W.insert_all(pool, wl)
     q = wl.q.contiguous()
@@ -349,6 +353,37 @@ def run_ours(args):
     assert torch.equal(out_host, out.cpu())
     e2e_ms = 1e3 * sum(e2e_times) / len(e2e_times)
 
+    # ---- decode loop: per step one token appended to every sequence, then the
+    # decode step replayed from a CUDA graph that the library captures again
+    # only after a structural change (a new leaf chunk every c steps).  Wall
+    # clock over the whole loop: appends, host table rebuilds and uploads,
+    # captures and replays.  Runs last: it grows every sequence.
+    loop = None
+    if args.loop_steps > 0:
+        ids = np.asarray(pool.batch_order(), dtype=np.int64)
+        gen = torch.Generator(device="cuda").manual_seed(99)
+        k_app = torch.randn(len(ids), spec.n_kv_heads, spec.head_dim, generator=gen, device="cuda").to(q.dtype)
+        v_app = torch.randn(len(ids), spec.n_kv_heads, spec.head_dim, generator=gen, device="cuda").to(q.dtype)
+        toks = np.full(len(ids), 5, dtype=np.int32)
+        out_loop = torch.empty_like(q)
+        pool.decode_attention_graph(q, out_loop)  # first capture, outside the timed loop
+        torch.cuda.synchronize()
+        st0 = pool.stats()
+        t0 = time.perf_counter()
+        for _ in range(args.loop_steps):
+            pool.append_batch(ids, toks, k_app, v_app)
+            pool.decode_attention_graph(q, out_loop)
+        torch.cuda.synchronize()
+        t1 = time.perf_counter()
+        st1 = pool.stats()
+        assert pool.check_device() == 0
+        loop = {"us_per_step": round(1e6 * (t1 - t0) / args.loop_steps, 3), "steps": args.loop_steps,
+                "graph_captures": st1["graph_captures"] - st0["graph_captures"],
+                "table_rebuilds": st1["rebuild_count"] - st0["rebuild_count"],
+                "last_rebuild_us": round(st1["last_rebuild_us"], 1),
+                "step": "append_batch (one token per sequence) + pst_decode_attention_graph; wall clock, "
+                        "no L2 flush between steps"}
+
     peak, peak_kind = measured_peak()
     st = pool.stats()
     phase_ms = [sum(p[j] for p in phase) / len(phase) for j in range(3)]
@@ -385,6 +420,7 @@ def run_ours(args):
         "gpu_launches": launches,
         "clocks": clk,
         "pool": {k: st[k] for k in ("used_chunks", "shared_chunks", "phase1_items", "phase2_items", "partial_rows")},
+        "decode_loop": loop,
     }
     if not args.no_cpu_baseline:
         gbs, res, step_s = oracle_rate(args.config, args.cpu_seconds)

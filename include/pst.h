@@ -86,6 +86,7 @@ typedef struct {
   int64_t phase1_items;    /* work items of the last build (chunk-first) */
   int64_t phase2_items;    /* work items of the last build (sequence-first) */
   int64_t partial_rows;    /* (o, m, n) partial rows of the last build */
+  int64_t graph_captures;  /* decode steps captured by pst_decode_attention_graph */
 } pst_stats_t;
 
 /* Create a pool.  device >= 0: CUDA device ordinal; the pool allocates its
@@ -175,6 +176,26 @@ pst_status pst_decode_attention_host(pst_pool* pool, const void* q_host, void* o
  *     pools -- race with each other.
  * Calls no cudaMalloc, cudaFree or other allocating routine. */
 pst_status pst_decode_attention_noalloc(pst_pool* pool, const void* q, void* out, void* stream);
+
+/* Decode attention replayed from a CUDA graph.  No counterpart in the paper:
+ * it serves a decode loop (per step: pst_append_batch, then this call), where
+ * the tables change structurally only every c-th step (ChunkAttention,
+ * Knowl 5: the context is copied lazily) and launch latency would otherwise
+ * show in every step.  Same inputs, outputs, result and errors as
+ * pst_decode_attention.
+ *   - It rebuilds and uploads the tables on the caller's stream when the tree
+ *     changed structurally, like pst_decode_attention; then it captures the
+ *     step's device work (counter reset, attention kernels, merge) into a CUDA
+ *     graph on a library-owned stream and launches the graph on the caller's
+ *     stream.  Later calls with the same table version and the same q and out
+ *     pointers launch the same graph: one cudaGraphLaunch.  A structural
+ *     change, or other q / out pointers, makes the next call capture again
+ *     (pst_stats: graph_captures).
+ *   - Appends that land in an existing leaf chunk change only device-side
+ *     chunk lengths, which the graph's kernels read at run time.
+ *   - Not while stream capture is active on the calling thread; with
+ *     profiling on (pst_set_profiling) it behaves as pst_decode_attention. */
+pst_status pst_decode_attention_graph(pst_pool* pool, const void* q, void* out, void* stream);
 
 /* Chunked-prefill attend (Chunked Prefill, sections 1-2): append W tokens
  * (host tokens int32[W], device k_new/v_new [W][Hkv][d]) to sequence seq_id at

@@ -164,6 +164,15 @@ struct pst_pool {
   cudaEvent_t pev[6] = {};
   bool pran[3] = {false, false, false};
   int32_t last_launches = 0;
+  // pst_decode_attention_graph: the captured step, valid for one table
+  // version and one (q, out) pair
+  cudaStream_t cap_stream = nullptr;
+  cudaGraphExec_t g_exec = nullptr;
+  int64_t g_version = -1;
+  const void* g_q = nullptr;
+  void* g_out = nullptr;
+  int32_t g_launches = 0;
+  int64_t graph_captures = 0;
 };
 
 namespace {
@@ -813,6 +822,8 @@ pst_status pst_pool_free(pst_pool* p) {
     cudaFree(p->d_out);
     if (p->h_stage) cudaFreeHost(p->h_stage);
     if (p->aux) cudaStreamDestroy(p->aux);
+    if (p->g_exec) cudaGraphExecDestroy(p->g_exec);
+    if (p->cap_stream) cudaStreamDestroy(p->cap_stream);
     if (p->ev_fork) cudaEventDestroy(p->ev_fork);
     if (p->ev_join) cudaEventDestroy(p->ev_join);
     if (p->ev_stage) cudaEventDestroy(p->ev_stage);
@@ -1013,6 +1024,8 @@ static pst_status launch_overlapped(pst_pool* p, const AttnParams& a, int32_t B,
   return PST_OK;
 }
 
+static pst_status launch_step(pst_pool* p, const void* q, void* out, cudaStream_t s);
+
 static pst_status decode_impl(pst_pool* p, const void* q, void* out, cudaStream_t s) {
   pst_status st = ensure_tables(p);
   if (st != PST_OK) return st;
@@ -1024,6 +1037,14 @@ static pst_status decode_impl(pst_pool* p, const void* q, void* out, cudaStream_
   if (misaligned16(q) || misaligned16(out)) return fail(PST_ERR_INVALID, "q and out must be 16-byte aligned");
   st = sync_device_tables(p, s);
   if (st != PST_OK) return st;
+  return launch_step(p, q, out, s);
+}
+
+// The step's device work once the tables are on the device: zero the claim
+// counter, launch the attention kernels and the merge on stream s.
+static pst_status launch_step(pst_pool* p, const void* q, void* out, cudaStream_t s) {
+  p->last_launches = 0;
+  const int32_t B = static_cast<int32_t>(p->batch.size());
   AttnParams a = base_params(p);
   a.q = q;
   a.out = out;
@@ -1090,6 +1111,55 @@ pst_status pst_decode_attention(pst_pool* p, const void* q, void* out, void* str
   pst_status st = need_device(p);
   if (st != PST_OK) return st;
   return decode_impl(p, q, out, static_cast<cudaStream_t>(stream));
+}
+
+pst_status pst_decode_attention_graph(pst_pool* p, const void* q, void* out, void* stream) {
+  pst_status st = need_device(p);
+  if (st != PST_OK) return st;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (p->profiling) return decode_impl(p, q, out, s);  // per-phase events are not captured
+  st = ensure_tables(p);
+  if (st != PST_OK) return st;
+  p->pran[0] = p->pran[1] = p->pran[2] = false;
+  const int32_t B = static_cast<int32_t>(p->batch.size());
+  if (B == 0) {
+    p->last_launches = 0;
+    return PST_OK;
+  }
+  if (!q || !out) return fail(PST_ERR_INVALID, "null q/out with %d live sequences", B);
+  if (misaligned16(q) || misaligned16(out)) return fail(PST_ERR_INVALID, "q and out must be 16-byte aligned");
+  st = sync_device_tables(p, s);  // on the caller's stream, before the graph
+  if (st != PST_OK) return st;
+  if (!p->g_exec || p->g_version != p->version || p->g_q != q || p->g_out != out) {
+    if (!p->cap_stream) CUDA_TRY(cudaStreamCreateWithFlags(&p->cap_stream, cudaStreamNonBlocking));
+    if (p->g_exec) {
+      cudaGraphExecDestroy(p->g_exec);
+      p->g_exec = nullptr;
+    }
+    CUDA_TRY(cudaStreamBeginCapture(p->cap_stream, cudaStreamCaptureModeRelaxed));
+    const pst_status ls = launch_step(p, q, out, p->cap_stream);
+    cudaGraph_t graph = nullptr;
+    const cudaError_t ce = cudaStreamEndCapture(p->cap_stream, &graph);
+    if (ls != PST_OK) {
+      if (graph) cudaGraphDestroy(graph);
+      return ls;
+    }
+    if (ce != cudaSuccess) return fail(PST_ERR_CUDA, "decode graph capture: %s", cudaGetErrorString(ce));
+    const cudaError_t ie = cudaGraphInstantiate(&p->g_exec, graph, 0);
+    cudaGraphDestroy(graph);
+    if (ie != cudaSuccess) {
+      p->g_exec = nullptr;
+      return fail(PST_ERR_CUDA, "decode graph instantiate: %s", cudaGetErrorString(ie));
+    }
+    p->g_version = p->version;
+    p->g_q = q;
+    p->g_out = out;
+    p->g_launches = p->last_launches;
+    ++p->graph_captures;
+  }
+  CUDA_TRY(cudaGraphLaunch(p->g_exec, s));
+  p->last_launches = p->g_launches;
+  return PST_OK;
 }
 
 // Decode attention without any allocation: the partial rows and the work
@@ -1321,6 +1391,7 @@ pst_status pst_stats(const pst_pool* p, pst_stats_t* o) {
   o->phase1_items = p->n_tc_items;
   o->phase2_items = p->n_simt_items;
   o->partial_rows = p->n_part_rows;
+  o->graph_captures = p->graph_captures;
   return PST_OK;
 }
 

@@ -36,7 +36,8 @@ class pst_stats_t(Structure):
     _fields_ = [("live_seqs", c_int64), ("used_chunks", c_int64), ("free_chunks", c_int64), ("max_chunks", c_int64),
                 ("shared_chunks", c_int64), ("unique_tokens", c_int64), ("logical_tokens", c_int64),
                 ("table_version", c_int64), ("rebuild_count", c_int64), ("last_rebuild_us", c_double),
-                ("phase1_items", c_int64), ("phase2_items", c_int64), ("partial_rows", c_int64)]
+                ("phase1_items", c_int64), ("phase2_items", c_int64), ("partial_rows", c_int64),
+                ("graph_captures", c_int64)]
 
 
 class PstError(RuntimeError):
@@ -63,6 +64,7 @@ SIGNATURES = {
     "pst_decode_attention": (c_int, [_P, _P, _P, _P]),
     "pst_decode_attention_host": (c_int, [_P, _P, _P, _P]),
     "pst_decode_attention_noalloc": (c_int, [_P, _P, _P, _P]),
+    "pst_decode_attention_graph": (c_int, [_P, _P, _P, _P]),
     "pst_prefill_attend": (c_int, [_P, c_int64, _P, c_int64, _P, _P, _P, _P, _P]),
     "pst_gather_kv": (c_int, [_P, c_int64, _P, _P, _P]),
     "pst_export_tables": (c_int, [_P, _P, c_int64, _I64P, _P, c_int64, _I64P, _P, c_int64, _I64P]),
@@ -196,6 +198,10 @@ class Pool:
     def decode_attention_noalloc(self, q, out, stream=None) -> None:
         """pst_decode_attention_noalloc: same result, scratch in the library's fixed device area."""
         check(lib.pst_decode_attention_noalloc(self.h, _ptr(q), _ptr(out), _stream(stream)))
+
+    def decode_attention_graph(self, q, out, stream=None) -> None:
+        """pst_decode_attention_graph: same result, the step replayed from a CUDA graph."""
+        check(lib.pst_decode_attention_graph(self.h, _ptr(q), _ptr(out), _stream(stream)))
 
     def decode_attention_host(self, q_host, out_host, stream=None) -> None:
         check(lib.pst_decode_attention_host(self.h, _ptr(q_host), _ptr(out_host), _stream(stream)))
