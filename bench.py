@@ -370,9 +370,10 @@ def run_ours(args):
         torch.cuda.synchronize()
         st0 = pool.stats()
         t0 = time.perf_counter()
+        sh = stream.cuda_stream  # raw handle: no per-call stream lookup in the binding
         for _ in range(args.loop_steps):
-            pool.append_batch(ids, toks, k_app, v_app)
-            pool.decode_attention_graph(q, out_loop)
+            pool.append_batch(ids, toks, k_app, v_app, stream=sh)
+            pool.decode_attention_graph(q, out_loop, stream=sh)
         torch.cuda.synchronize()
         t1 = time.perf_counter()
         st1 = pool.stats()

@@ -144,14 +144,16 @@ pst_status pst_seq_length(const pst_pool* pool, int64_t seq_id, int64_t* n_token
  * tables first if the tree changed (Knowl 5).  q and out must start on a
  * 16-byte boundary (PST_ERR_INVALID otherwise).  Chunk-first partials run on the
  * tensor cores (tcgen05) for f16/bf16 with c = 64, sequence-first partials on
- * the CUDA cores, then a merge kernel combines the partial rows (attn_reduce)
- * and writes out. */
+ * warp-level tensor-core products (f16/bf16) or the CUDA cores (f32), then a
+ * merge kernel combines the partial rows (attn_reduce) and writes out. */
 pst_status pst_decode_attention(pst_pool* pool, const void* q, void* out, void* stream);
 
-/* Same as pst_decode_attention with HOST q/out: copies q host->device, runs
- * the decode and copies out device->host on `stream`, then synchronises the
- * stream.  q_host, out_host: host [B][Hq][d] (pinned memory avoids staging
- * copies inside the CUDA runtime). */
+/* Same as pst_decode_attention with HOST q/out: copies q host->device into a
+ * library-owned device buffer, runs the decode step (from its CUDA graph, as
+ * pst_decode_attention_graph does, while the tables keep their structure) and
+ * copies out device->host on `stream`, then synchronises the stream.  q_host,
+ * out_host: host [B][Hq][d] (pinned memory avoids staging copies inside the
+ * CUDA runtime). */
 pst_status pst_decode_attention_host(pst_pool* pool, const void* q_host, void* out_host, void* stream);
 
 /* Decode attention that allocates nothing.  No counterpart in the paper: it

@@ -1223,7 +1223,9 @@ pst_status pst_decode_attention_host(pst_pool* p, const void* q_host, void* out_
     p->qo_cap = bytes;
   }
   CUDA_TRY(cudaMemcpyAsync(p->d_q, q_host, bytes, cudaMemcpyHostToDevice, s));
-  st = decode_impl(p, p->d_q, p->d_out, s);
+  // the staging buffers stay put between calls, so the step is replayed from
+  // its CUDA graph until the tables change structurally
+  st = pst_decode_attention_graph(p, p->d_q, p->d_out, stream);
   if (st != PST_OK) return st;
   CUDA_TRY(cudaMemcpyAsync(out_host, p->d_out, bytes, cudaMemcpyDeviceToHost, s));
   CUDA_TRY(cudaStreamSynchronize(s));
