@@ -46,6 +46,8 @@ def parse():
     ap.add_argument("--min-share", type=int, default=0)
     ap.add_argument("--flags", type=int, default=0)
     ap.add_argument("--loop-steps", type=int, default=128, help="decode-loop steps (0: skip)")
+    ap.add_argument("--sweep", choices=["batch", "divergence"], default=None,
+                    help="one line per workload of a family instead of the single default line")
     return ap.parse_args()
 
 
@@ -434,10 +436,34 @@ def run_ours(args):
         torch.distributed.destroy_process_group()
 
 
+def run_sweep(args):
+    """One JSON line per workload of a family (ChunkAttention Knowl 9: batch
+    scaling; Knowl 8: divergence), each from its own bench run (no CPU
+    baseline, no decode loop), plus decode tokens per second (B / step time),
+    the unit the pages quote."""
+    from prefix_shared_kv_tree_gb300 import workloads as W
+    names = {"batch": W.BATCH_FAMILY, "divergence": W.DIVERGENCE_FAMILY}[args.sweep]
+    for name in names:
+        cmd = [sys.executable, os.path.abspath(__file__), "--config", name, "--steps", str(args.steps),
+               "--warmup", str(args.warmup), "--no-cpu-baseline", "--loop-steps", "0",
+               "--min-share", str(args.min_share), "--flags", str(args.flags)]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        line = next((x for x in r.stdout.splitlines() if x.startswith("{")), None)
+        if r.returncode != 0 or line is None:
+            print(json.dumps({"config": name, "error": (r.stderr or r.stdout)[-400:]}), flush=True)
+            continue
+        d = json.loads(line)
+        d["sweep"] = args.sweep
+        d["decode_tokens_per_s"] = round(W.SPECS[name].n_sequences / (d["ms_per_step"] * 1e-3), 1)
+        print(json.dumps(d), flush=True)
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         run_reference(args)
+    elif args.sweep:
+        run_sweep(args)
     else:
         run_ours(args)
 

@@ -109,6 +109,26 @@ DESCRIPTIONS = {
 }
 
 
+# Batch-scaling family (ChunkAttention, Knowl 9: n_s = 2048 shared tokens,
+# n_c = 64 per sequence, b from 16 to 96): the chunk-first phase's stacked rows
+# grow with the batch.
+BATCH_FAMILY = tuple(f"batch{b}" for b in (16, 32, 48, 64, 80, 96))
+for _b in (16, 32, 48, 64, 80, 96):
+    SPECS[f"batch{_b}"] = WorkloadSpec(f"batch{_b}", 32, 32, 128, 64, "f16", ((2048, 1), (64, _b)), 1100 + _b)
+    DESCRIPTIONS[f"batch{_b}"] = f"32 heads, d=128, fp16, batch {_b}, 2048 shared + 64 private, chunk 64"
+
+# Divergence family (ChunkAttention, Knowl 8: b = 32, c = 64, fp16, the
+# (n_s, n_c) pairs it reports): as completions n_c grow, the shared share of
+# the KV cache falls.
+DIVERGENCE_GRID = ((1024, 256), (1024, 512), (1024, 1024), (2048, 512), (2048, 1024), (2048, 2048),
+                   (4096, 512), (4096, 4096))
+DIVERGENCE_FAMILY = tuple(f"div_s{ns}_c{nc}" for ns, nc in DIVERGENCE_GRID)
+for _i, (_ns, _nc) in enumerate(DIVERGENCE_GRID):
+    _name = f"div_s{_ns}_c{_nc}"
+    SPECS[_name] = WorkloadSpec(_name, 32, 32, 128, 64, "f16", ((_ns, 1), (_nc, 32)), 1300 + _i)
+    DESCRIPTIONS[_name] = f"32 heads, d=128, fp16, batch 32, {_ns} shared + {_nc} private, chunk 64"
+
+
 @dataclass
 class Segment:
     index: int

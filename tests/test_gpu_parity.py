@@ -271,7 +271,7 @@ def _sample_rows(b, hq, n, seed):
     return sorted(rows)
 
 
-@pytest.mark.parametrize("name", ["share1k", "share4k", "noshare", "gqa_tree"])
+@pytest.mark.parametrize("name", ["share1k", "share4k", "noshare", "gqa_tree", "batch96", "div_s1024_c1024"])
 def test_full_config_sampled_rows(pst, name):
     spec = W.SPECS[name]
     wl = W.generate(spec, device="cuda")
