@@ -30,6 +30,26 @@ __global__ void __launch_bounds__(256) scatter_kernel(const ScatterParams p, int
   uint8_t* tile = p.pool + (static_cast<size_t>(op.chunk) * p.Hkv + kv) * 2 * half;
   const int rend = op.zero_tail ? C : op.r1;
   const size_t src_row_bytes = static_cast<size_t>(p.Hkv) * D * ES;
+  if (op.r1 == op.r0 + 1 && !op.zero_tail) {
+    // One row into a chunk that already holds rows [0, r0): a decode append.
+    // K: the row's 16-byte chunks; V^T: one element in each of the D feature
+    // rows, stored on its own (the rest of each 16-byte chunk is left alone).
+    const uint8_t* ks = p.k + static_cast<size_t>(op.src_row) * src_row_bytes + static_cast<size_t>(kv) * D * ES;
+    const uint8_t* vs = p.v + static_cast<size_t>(op.src_row) * src_row_bytes + static_cast<size_t>(kv) * D * ES;
+    for (int j = threadIdx.x; j < DCH; j += blockDim.x)
+      *reinterpret_cast<uint4*>(tile + tile_off(op.r0, j, D * ES, C)) = *reinterpret_cast<const uint4*>(ks + j * 16);
+    const int j = op.r0 / VEC, e = op.r0 % VEC;
+    for (int dr = threadIdx.x; dr < D; dr += blockDim.x) {
+      uint8_t* dst = tile + half + tile_off(dr, j, C * ES, D) + e * ES;
+      if constexpr (ES == 2) {
+        *reinterpret_cast<uint16_t*>(dst) = *reinterpret_cast<const uint16_t*>(vs + dr * ES);
+      } else {
+        *reinterpret_cast<uint32_t*>(dst) = *reinterpret_cast<const uint32_t*>(vs + dr * ES);
+      }
+    }
+    if (kv == 0 && threadIdx.x == 0) p.chunk_len[op.chunk] = op.r1;
+    return;
+  }
   // K: whole 16-byte chunks of rows [r0, rend)
   for (int idx = threadIdx.x; idx < (rend - op.r0) * DCH; idx += blockDim.x) {
     const int r = op.r0 + idx / DCH, j = idx % DCH;

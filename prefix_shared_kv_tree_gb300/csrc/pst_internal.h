@@ -116,7 +116,9 @@ struct ScatterOp {
   int32_t r0, r1;    // rows [r0, r1) of the chunk are written from src_row...
   int32_t zero_tail; // 1: rows [r1, C) are zero-filled (freshly allocated chunk)
 };
-constexpr int kScatterMax = 128;
+// Ops per scatter launch: they travel in the kernel parameters (20 bytes
+// each), so a decode step's batched append of up to 512 sequences is one launch.
+constexpr int kScatterMax = 512;
 struct ScatterParams {
   const uint8_t* k;   // scatter: source [rows][Hkv][D]; gather: destination
   const uint8_t* v;
