@@ -136,6 +136,9 @@ __global__ void __launch_bounds__(128) merge_kernel(const AttnParams p, int B) {
     e1 = __ldg(p.m_off + key + 1);
   }
   if (p.pdl) ptx::pdl_wait();
+  // every attention kernel of the step has completed: clear the work-claim
+  // counter for the next step
+  if (blockIdx.x == 0 && threadIdx.x == 0 && p.sched != nullptr) *p.sched = 0;
   if (live) {
     extern __shared__ float4 merge_smem[];
     if (e1 - e0 <= p.merge_cap)

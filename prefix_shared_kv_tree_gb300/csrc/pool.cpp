@@ -149,6 +149,9 @@ struct pst_pool {
   size_t part_cap = 0;  // rows
   int32_t* d_err = nullptr;
   int32_t* d_sched = nullptr;  // work-claim counter of the CUDA-core kernel
+  // d_sched is zero when the next decode starts: every decode's merge kernel
+  // clears it at its end; a prefill (no merge) or a failed launch leaves it set
+  bool sched_zero = true;
   int32_t* d_pre = nullptr;
   size_t pre_cap = 0;
   int32_t* h_stage = nullptr;  // pinned upload staging
@@ -793,6 +796,7 @@ pst_status pst_pool_create(const pst_config* cfg, int device, pst_pool** out) {
     if ((e = cudaMalloc(&p->d_err, sizeof(int32_t))) != cudaSuccess) return bail(e, "cudaMalloc");
     if ((e = cudaMemset(p->d_err, 0, sizeof(int32_t))) != cudaSuccess) return bail(e, "cudaMemset");
     if ((e = cudaMalloc(&p->d_sched, 256)) != cudaSuccess) return bail(e, "cudaMalloc");
+    if ((e = cudaMemset(p->d_sched, 0, 256)) != cudaSuccess) return bail(e, "cudaMemset");
     if ((e = cudaStreamCreateWithFlags(&p->aux, cudaStreamNonBlocking)) != cudaSuccess) return bail(e, "stream");
     if ((e = cudaEventCreateWithFlags(&p->ev_fork, cudaEventDisableTiming)) != cudaSuccess) return bail(e, "event");
     if ((e = cudaEventCreateWithFlags(&p->ev_join, cudaEventDisableTiming)) != cudaSuccess) return bail(e, "event");
@@ -1025,6 +1029,7 @@ static pst_status launch_overlapped(pst_pool* p, const AttnParams& a, int32_t B,
 }
 
 static pst_status launch_step(pst_pool* p, const void* q, void* out, cudaStream_t s);
+static cudaError_t clear_sched(pst_pool* p, cudaStream_t s);
 
 static pst_status decode_impl(pst_pool* p, const void* q, void* out, cudaStream_t s) {
   pst_status st = ensure_tables(p);
@@ -1037,12 +1042,34 @@ static pst_status decode_impl(pst_pool* p, const void* q, void* out, cudaStream_
   if (misaligned16(q) || misaligned16(out)) return fail(PST_ERR_INVALID, "q and out must be 16-byte aligned");
   st = sync_device_tables(p, s);
   if (st != PST_OK) return st;
+  CUDA_TRY(clear_sched(p, s));
   return launch_step(p, q, out, s);
+}
+
+// Zero the claim counter on stream s unless it is known to be zero already;
+// the decode step about to run leaves it zero (its merge kernel clears it).
+static cudaError_t clear_sched(pst_pool* p, cudaStream_t s) {
+  if (!p->sched_zero) {
+    const cudaError_t e = cudaMemsetAsync(p->d_sched, 0, sizeof(int32_t), s);
+    if (e != cudaSuccess) return e;
+  }
+  p->sched_zero = true;
+  return cudaSuccess;
 }
 
 // The step's device work once the tables are on the device: zero the claim
 // counter, launch the attention kernels and the merge on stream s.
+static pst_status launch_step_impl(pst_pool* p, const void* q, void* out, cudaStream_t s);
+
+// A step whose launches all went out leaves the claim counter zero (its
+// merge kernel clears it); after a failed launch its state is unknown.
 static pst_status launch_step(pst_pool* p, const void* q, void* out, cudaStream_t s) {
+  const pst_status st = launch_step_impl(p, q, out, s);
+  p->sched_zero = st == PST_OK;
+  return st;
+}
+
+static pst_status launch_step_impl(pst_pool* p, const void* q, void* out, cudaStream_t s) {
   p->last_launches = 0;
   const int32_t B = static_cast<int32_t>(p->batch.size());
   AttnParams a = base_params(p);
@@ -1056,7 +1083,6 @@ static pst_status launch_step(pst_pool* p, const void* q, void* out, cudaStream_
   a.row_idx = p->d_tab + p->off_rows;
   const bool fork = p->n_tc_items > 0 && p->n_simt_items > 0 && (p->cfg.flags & PST_FLAG_CONCURRENT_PHASES);
   cudaStream_t s1 = fork ? p->aux : s;
-  if (p->n_simt_items > 0) CUDA_TRY(cudaMemsetAsync(p->d_sched, 0, sizeof(int32_t), s));
   if (!fork && !p->profiling) return launch_overlapped(p, a, B, s);
   // Profiling (per-phase events between the kernels, so no overlap) or forked
   // phases: chunk-first, then sequence-first on the whole grid, then merge.
@@ -1130,6 +1156,7 @@ pst_status pst_decode_attention_graph(pst_pool* p, const void* q, void* out, voi
   if (misaligned16(q) || misaligned16(out)) return fail(PST_ERR_INVALID, "q and out must be 16-byte aligned");
   st = sync_device_tables(p, s);  // on the caller's stream, before the graph
   if (st != PST_OK) return st;
+  CUDA_TRY(clear_sched(p, s));  // the graph holds no counter reset: the previous step's merge cleared it
   if (!p->g_exec || p->g_version != p->version || p->g_q != q || p->g_out != out) {
     if (!p->cap_stream) CUDA_TRY(cudaStreamCreateWithFlags(&p->cap_stream, cudaStreamNonBlocking));
     if (p->g_exec) {
@@ -1334,6 +1361,7 @@ pst_status pst_prefill_attend(pst_pool* p, int64_t seq_id, const int32_t* tokens
     CUDA_TRY(cudaMemsetAsync(p->d_sched, 0, sizeof(int32_t), s));
     (void)n_warps;
     e = launch_attn_simt(p->cfg.dtype, p->D, p->C, g, a, std::min<int32_t>(grid, p->n_sm), s);
+    p->sched_zero = false;  // no merge follows to clear it
   }
   if (e != cudaSuccess) return fail(PST_ERR_CUDA, "prefill launch: %s", cudaGetErrorString(e));
   return PST_OK;
