@@ -103,3 +103,30 @@ def test_graph_decode_loop(pst, dtype, hq, hkv):
     st = pool.stats()
     assert st["graph_captures"] == len(seen), (st["graph_captures"], len(seen))
     assert st["graph_captures"] < c  # most steps replayed a captured graph
+
+
+def test_misaligned_q_or_out_is_refused(pst):
+    """q and out must start on a 16-byte boundary (the kernels move 16-byte
+    vectors); every decode entry point refuses otherwise with PST_ERR_INVALID
+    and launches nothing."""
+    hq, hkv, d, c = 4, 2, 128, 64
+    seqs = _tree(8, "f16", hkv, d, c, 3)
+    pool = pst.Pool(hq, hkv, d, c, 64, "f16", 0, 0, 0, device=0)
+    for (t, k, v) in seqs:
+        pool.insert(t, k.cuda(), v.cuda())
+    B = len(pool.batch_order())
+    flat = torch.zeros(B * hq * d + 8, dtype=torch.float16, device="cuda")
+    good = flat[:B * hq * d].view(B, hq, d)
+    bad = flat[1:1 + B * hq * d].view(B, hq, d)  # 2 bytes past a 16-byte boundary
+    out = torch.empty(B, hq, d, dtype=torch.float16, device="cuda")
+    pool.decode_attention(good, out)  # tables on the device
+    torch.cuda.synchronize()
+    for call in (pool.decode_attention, pool.decode_attention_graph, pool.decode_attention_noalloc):
+        with pytest.raises(pst.PstError) as e:
+            call(bad, out)
+        assert e.value.status == pst.PST_ERR_INVALID
+        with pytest.raises(pst.PstError) as e:
+            call(good, bad)
+        assert e.value.status == pst.PST_ERR_INVALID
+    torch.cuda.synchronize()
+    assert pool.check_device() == 0
