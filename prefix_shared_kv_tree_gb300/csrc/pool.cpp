@@ -763,10 +763,13 @@ pst_status pst_pool_create(const pst_config* cfg, int device, pst_pool** out) {
   if (const char* e = std::getenv("PST_TC_MAX_RUN")) p->tc_max_run = std::max(2, std::atoi(e));
   if (const char* e = std::getenv("PST_MERGE_CAP")) p->merge_cap_forced = std::max(0, std::atoi(e));
   if (const char* e = std::getenv("PST_SIMT_TAIL")) p->simt_tail = std::max(0.0, std::atof(e));
-  // CUDA-core kernel shape: up to 8 consumer warps (plus the producer warp)
-  // x 6 stages of 4 KB pieces, as far as shared memory allows
+  // Sequence-first kernel shape: up to 8 consumer warps (plus the producer
+  // warp) x up to 6 stages of 8 KB pieces, as far as shared memory allows
   p->simt_wpc = attn_simt_max_warps(c.dtype, g);
-  p->simt_stages = 6;
+  // 16-bit K/V with one query row per KV head: two stages keep the DRAM-bound
+  // stream fed (fewer bytes in flight, shorter queues); larger groups compute
+  // longer per piece and want a deeper ring
+  p->simt_stages = (c.dtype != kF32 && g == 1) ? 2 : 6;
   if (const char* e = std::getenv("PST_SIMT_WPC"))
     p->simt_wpc = std::max(1, std::min(attn_simt_max_warps(c.dtype, g), std::atoi(e)));
   if (const char* e = std::getenv("PST_SIMT_STAGES")) p->simt_stages = std::max(2, std::min(16, std::atoi(e)));
