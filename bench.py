@@ -46,7 +46,7 @@ def parse():
     ap.add_argument("--min-share", type=int, default=0)
     ap.add_argument("--flags", type=int, default=0)
     ap.add_argument("--loop-steps", type=int, default=128, help="decode-loop steps (0: skip)")
-    ap.add_argument("--sweep", choices=["batch", "divergence"], default=None,
+    ap.add_argument("--sweep", choices=["batch", "divergence", "generality"], default=None,
                     help="one line per workload of a family instead of the single default line")
     return ap.parse_args()
 
@@ -394,6 +394,8 @@ def run_ours(args):
     dom = max(range(2), key=lambda j: phase_ms[j])  # the dominant kernel (not the whole call)
     min_share = args.min_share or 2
     dom_bytes = [shared_bytes(spec, min_share), private_bytes(spec, min_share)][dom]
+    if phase_ms[0] == 0.0:  # no chunk-first launch: the sequence-first kernel reads every chunk
+        dom_bytes = spec.unique_kv_bytes()
     achieved = dom_bytes / (phase_ms[dom] * 1e-3) / 1e9
 
     if rank != 0:
@@ -438,11 +440,13 @@ def run_ours(args):
 
 def run_sweep(args):
     """One JSON line per workload of a family (ChunkAttention Knowl 9: batch
-    scaling; Knowl 8: divergence), each from its own bench run (no CPU
+    scaling; Knowl 8: divergence; Knowl 10: head dims and chunk sizes), each
+    from its own bench run (no CPU
     baseline, no decode loop), plus decode tokens per second (B / step time),
     the unit the pages quote."""
     from prefix_shared_kv_tree_gb300 import workloads as W
-    names = {"batch": W.BATCH_FAMILY, "divergence": W.DIVERGENCE_FAMILY}[args.sweep]
+    names = {"batch": W.BATCH_FAMILY, "divergence": W.DIVERGENCE_FAMILY,
+             "generality": W.GENERALITY_FAMILY}[args.sweep]
     for name in names:
         cmd = [sys.executable, os.path.abspath(__file__), "--config", name, "--steps", str(args.steps),
                "--warmup", str(args.warmup), "--no-cpu-baseline", "--loop-steps", "0",

@@ -60,7 +60,9 @@ typedef struct {
   int32_t n_q_heads;   /* Hq >= 1 */
   int32_t n_kv_heads;  /* Hkv >= 1, divides Hq, Hq/Hkv in {1,2,4,8} */
   int32_t head_dim;    /* d in {64, 128} */
-  int32_t chunk_size;  /* c in {32, 64} */
+  int32_t chunk_size;  /* c in {16, 32, 64, 128}; the chunk-first phase runs on the
+                          tensor cores (tcgen05) for 16-bit K/V at c = 64, on the
+                          CUDA-core kernel otherwise */
   int64_t max_chunks;  /* pool capacity in chunks (>= 1) */
   int32_t dtype;       /* pst_dtype */
   int32_t min_share;   /* chunk-first threshold: a chunk covered by >= min_share live

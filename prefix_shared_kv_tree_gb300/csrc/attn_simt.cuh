@@ -1,7 +1,7 @@
 // Sequence-first partial attention on the CUDA cores (ChunkAttention, Knowl 2
 // phase 2, with partial_attn / attn_reduce of Knowl 3).  Also runs the
-// chunk-first phase when the tensor-core kernel does not apply (fp32, c = 32),
-// and causal prefill blocks in that case.
+// chunk-first phase when the tensor-core kernel does not apply (fp32, or a
+// chunk size other than 64), and causal prefill blocks in that case.
 //
 // Warp-specialised, warp-per-stream design.  A CTA holds NW consumer warps and
 // one producer warp; lane c of the producer serves consumer c:
@@ -153,8 +153,10 @@ __global__ void __launch_bounds__(32 * (simt_max_warps(G, sizeof(T)) + 1), 1) at
   constexpr int KB = D * ES / 128;                       // K: 128-byte column blocks of C rows
   constexpr int KPR = C < kSimtPieceRows ? C : kSimtPieceRows;  // keys per K piece
   constexpr int KPC = C / KPR;                           // K pieces per column block
-  constexpr int KT = KPR / 32;                           // keys per lane per K piece
-  constexpr int KPL = C / 32;      // keys per lane per chunk
+  // fp32 consumer, lane = key: keys per lane per K piece and per chunk (a
+  // chunk shorter than a warp leaves lanes C .. 31 on masked duplicates)
+  constexpr int KT = KPR >= 32 ? KPR / 32 : 1;
+  constexpr int KPL = C >= 32 ? C / 32 : 1;
   constexpr bool VSW = (C * ES) % 128 == 0;              // V^T rows in 128-byte swizzled blocks
   constexpr int VB = VSW ? C * ES / 128 : 1;             // V^T column blocks
   constexpr int VPR = D < kSimtPieceRows ? D : kSimtPieceRows;  // feature rows per V^T piece
@@ -174,7 +176,7 @@ __global__ void __launch_bounds__(32 * (simt_max_warps(G, sizeof(T)) + 1), 1) at
   // the output features (values) as the 16-row M side and the item's query
   // rows as the 8-column N side.
   constexpr bool kMma = ES == 2;
-  static_assert(!kMma || (G <= 8 && C % 32 == 0 && KPR % 16 == 0 && VB == 1 && VPR % 16 == 0), "mma shape");
+  static_assert(!kMma || (G <= 8 && C % 16 == 0 && KPR % 16 == 0 && VPR % 16 == 0), "mma shape");
   const int S = p.stages;
   const int NW = p.warps_per_cta;  // consumer warps; warp NW produces
   const SimtLayout L = simt_layout(C, D, G, S, ES);
@@ -632,19 +634,27 @@ __global__ void __launch_bounds__(32 * (simt_max_warps(G, sizeof(T)) + 1), 1) at
           // B fragments of P^T (keys x query columns), k-steps of 16 keys:
           // matrices of 8 key rows, transposed on load
           uint32_t pf[MT][2];
+          if constexpr (MT == 1) {
+            ptx::ldsm_x2_trans(pb + (lane & 15) * 16, pf[0]);
+          } else {
 #pragma unroll
-          for (int t2 = 0; t2 < MT / 2; ++t2) {
-            uint32_t r[4];
-            ptx::ldsm_x4_trans(pb + (t2 * 32 + lane) * 16, r);
-            pf[2 * t2][0] = r[0];
-            pf[2 * t2][1] = r[1];
-            pf[2 * t2 + 1][0] = r[2];
-            pf[2 * t2 + 1][1] = r[3];
+            for (int t2 = 0; t2 < MT / 2; ++t2) {
+              uint32_t r[4];
+              ptx::ldsm_x4_trans(pb + (t2 * 32 + lane) * 16, r);
+              pf[2 * t2][0] = r[0];
+              pf[2 * t2][1] = r[1];
+              pf[2 * t2 + 1][0] = r[2];
+              pf[2 * t2 + 1][1] = r[3];
+            }
           }
 
-          // ---- O^T += V^T P^T over the V^T pieces (VPR feature rows each)
+          // ---- O^T += V^T P^T over the V^T pieces (VPR feature rows of one
+          // key block each: VKS k-steps of 16 keys from key vb * 16 VKS)
+          constexpr int VKS = VSW ? 128 / ES / 16 : MT;
+          static_assert(VB * VKS == MT, "V^T key blocks");
 #pragma unroll
-          for (int vg = 0; vg < VG; ++vg) {
+          for (int vp = 0; vp < VB * VG; ++vp) {
+            const int vb = vp / VG, vg = vp % VG;
             if (!ptx::mbar_wait(&full[cs], cph, abort_flag, p.err)) {
               aborted = true;
               break;
@@ -661,10 +671,11 @@ __global__ void __launch_bounds__(32 * (simt_max_warps(G, sizeof(T)) + 1), 1) at
             };
             load_v(0, af[0]);
 #pragma unroll
-            for (int ks = 0; ks < MT; ++ks) {
-              if (ks + 1 < MT) load_v(ks + 1, af[(ks + 1) & 1]);
+            for (int ks = 0; ks < VKS; ++ks) {
+              if (ks + 1 < VKS) load_v(ks + 1, af[(ks + 1) & 1]);
 #pragma unroll
-              for (int t = 0; t < VMT; ++t) ptx::mma_16816<BF>(o[vg * VMT + t], af[ks & 1][t], pf[ks][0], pf[ks][1]);
+              for (int t = 0; t < VMT; ++t)
+                ptx::mma_16816<BF>(o[vg * VMT + t], af[ks & 1][t], pf[vb * VKS + ks][0], pf[vb * VKS + ks][1]);
             }
             __syncwarp();  // every lane is done with the stage (and with P^T before the next chunk)
             ++consumed;
@@ -728,12 +739,18 @@ __global__ void __launch_bounds__(32 * (simt_max_warps(G, sizeof(T)) + 1), 1) at
         int lim = __shfl_sync(0xffffffffu, my_len, c & 31);
         if (p.causal_p0 >= 0) lim = min(lim, p.causal_p0 + grp + 1 - c * C);
 
-        // ---- scores over the K pieces
-        float2 acc[G][KPL][2];  // per key: four partial sums (feature i mod 4), as two pairs
+        // ---- scores over the K pieces.  Per key four partial sums (feature
+        // i mod 4) as two pairs; at four keys per lane and G >= 4 the G * KPL
+        // keys give independent FMA chains enough, and one pair (feature i
+        // mod 2) keeps the accumulators in registers
+        constexpr int NA = (KPL >= 4 && G >= 4) ? 1 : 2;
+        float2 acc[G][KPL][NA];
 #pragma unroll
         for (int h = 0; h < G; ++h)
 #pragma unroll
-          for (int kk = 0; kk < KPL; ++kk) acc[h][kk][0] = acc[h][kk][1] = make_float2(0.f, 0.f);
+          for (int kk = 0; kk < KPL; ++kk)
+#pragma unroll
+            for (int a = 0; a < NA; ++a) acc[h][kk][a] = make_float2(0.f, 0.f);
 #pragma unroll
         for (int kp = 0; kp < KB * KPC; ++kp) {
           const int kb = kp / KPC, kh = kp % KPC;  // column block, key run: keys kh*KPR + lane + 32 t
@@ -746,7 +763,7 @@ __global__ void __launch_bounds__(32 * (simt_max_warps(G, sizeof(T)) + 1), 1) at
           for (int jj = 0; jj < KCH; ++jj) {
 #pragma unroll
             for (int t = 0; t < KT; ++t) {
-              const int r = lane + 32 * t;
+              const int r = KPR >= 32 ? lane + 32 * t : (lane & (KPR - 1));
               float kf[VEC];
               unpack16<T>(*reinterpret_cast<const uint4*>(kt + r * 128 + ((jj ^ (r & 7)) << 4)), kf);
 #pragma unroll
@@ -755,10 +772,9 @@ __global__ void __launch_bounds__(32 * (simt_max_warps(G, sizeof(T)) + 1), 1) at
 #pragma unroll
                 for (int e4 = 0; e4 < VEC / 4; ++e4) {
                   const float4 qq = qv[e4];
-                  acc[h][kh * KT + t][0] =
-                      __ffma2_rn(make_float2(qq.x, qq.y), make_float2(kf[4 * e4 + 0], kf[4 * e4 + 1]), acc[h][kh * KT + t][0]);
-                  acc[h][kh * KT + t][1] =
-                      __ffma2_rn(make_float2(qq.z, qq.w), make_float2(kf[4 * e4 + 2], kf[4 * e4 + 3]), acc[h][kh * KT + t][1]);
+                  float2* a = acc[h][kh * KT + t];
+                  a[0] = __ffma2_rn(make_float2(qq.x, qq.y), make_float2(kf[4 * e4 + 0], kf[4 * e4 + 1]), a[0]);
+                  a[NA - 1] = __ffma2_rn(make_float2(qq.z, qq.w), make_float2(kf[4 * e4 + 2], kf[4 * e4 + 3]), a[NA - 1]);
                 }
               }
             }
@@ -777,7 +793,8 @@ __global__ void __launch_bounds__(32 * (simt_max_warps(G, sizeof(T)) + 1), 1) at
         for (int h = 0; h < G; ++h)
 #pragma unroll
           for (int kk = 0; kk < KPL; ++kk)
-            sc[h][kk] = (acc[h][kk][0].x + acc[h][kk][0].y) + (acc[h][kk][1].x + acc[h][kk][1].y);
+            sc[h][kk] = NA == 2 ? (acc[h][kk][0].x + acc[h][kk][0].y) + (acc[h][kk][NA - 1].x + acc[h][kk][NA - 1].y)
+                                : acc[h][kk][0].x + acc[h][kk][0].y;
 
         // ---- online softmax over the chunk's C keys (Knowl 3, log2 units)
 #pragma unroll
@@ -796,7 +813,7 @@ __global__ void __launch_bounds__(32 * (simt_max_warps(G, sizeof(T)) + 1), 1) at
           for (int kk = 0; kk < KPL; ++kk) {
             const float pr = ptx::ex2(sc[h][kk] - m_use);
             ps_ += pr;
-            pbuf[h * C + kk * 32 + lane] = pr;
+            if (C >= 32 || lane < C) pbuf[h * C + kk * 32 + lane] = pr;
           }
           nl[h] = nl[h] * alpha + ps_;
 #pragma unroll
@@ -921,13 +938,15 @@ cudaError_t launch_simt_g(int g, const AttnParams& p, int grid, cudaStream_t s) 
   return cudaErrorInvalidValue;
 }
 
-template <typename T>
+// Chunk sizes C0 and C1 at both head dims (each translation unit instantiates
+// one pair, so the build compiles the kernel's variants in parallel).
+template <typename T, int C0, int C1>
 cudaError_t launch_simt_dc(int D, int C, int g, const AttnParams& p, int grid, cudaStream_t s) {
   if (grid <= 0) return cudaSuccess;
-  if (D == 64 && C == 32) return launch_simt_g<T, 64, 32>(g, p, grid, s);
-  if (D == 64 && C == 64) return launch_simt_g<T, 64, 64>(g, p, grid, s);
-  if (D == 128 && C == 32) return launch_simt_g<T, 128, 32>(g, p, grid, s);
-  if (D == 128 && C == 64) return launch_simt_g<T, 128, 64>(g, p, grid, s);
+  if (D == 64 && C == C0) return launch_simt_g<T, 64, C0>(g, p, grid, s);
+  if (D == 64 && C == C1) return launch_simt_g<T, 64, C1>(g, p, grid, s);
+  if (D == 128 && C == C0) return launch_simt_g<T, 128, C0>(g, p, grid, s);
+  if (D == 128 && C == C1) return launch_simt_g<T, 128, C1>(g, p, grid, s);
   return cudaErrorInvalidValue;
 }
 

@@ -207,15 +207,19 @@ bool simt_supported(int dtype, int D, int g) {
 
 int attn_simt_max_warps(int dtype, int g) { return simt_max_warps(g, dtype_size(dtype)); }
 
+size_t attn_simt_piece_bytes(int dtype, int D, int C) { return simt_stage_bytes(C, D, dtype_size(dtype)); }
+
 size_t attn_simt_smem(int dtype, int D, int C, int g, int stages, int warps_per_cta) {
   return simt_warp_bytes(C, D, g, stages, dtype_size(dtype)) * warps_per_cta;
 }
 
 cudaError_t launch_attn_simt(int dtype, int D, int C, int g, const AttnParams& p, int grid, cudaStream_t s) {
+  const bool large = C >= 64;
   switch (dtype) {
-    case kF16: return launch_attn_simt_f16(D, C, g, p, grid, s);
-    case kBF16: return launch_attn_simt_bf16(D, C, g, p, grid, s);
-    case kF32: return launch_attn_simt_f32(D, C, g, p, grid, s);
+    case kF16: return large ? launch_attn_simt_f16_large(D, C, g, p, grid, s) : launch_attn_simt_f16_small(D, C, g, p, grid, s);
+    case kBF16:
+      return large ? launch_attn_simt_bf16_large(D, C, g, p, grid, s) : launch_attn_simt_bf16_small(D, C, g, p, grid, s);
+    case kF32: return large ? launch_attn_simt_f32_large(D, C, g, p, grid, s) : launch_attn_simt_f32_small(D, C, g, p, grid, s);
   }
   return cudaErrorInvalidValue;
 }

@@ -9,14 +9,19 @@
 // (Chunked Prefill, sections 1-2).
 //
 // Persistent: each CTA walks its own list of work items (up to 128 stacked
-// query rows of one KV head against a list of 64-token chunks); TMEM and the
-// mbarriers are set up once and the pipelines run across item boundaries.
+// query rows of one KV head against a list of chunks of 64 or 128 tokens,
+// taken as tiles of 64 keys); TMEM and the mbarriers are set up once and the
+// pipelines run across item boundaries.
 // Warp roles:
-//   warp 0      : producer.  Lane 0 moves each chunk's 32 KB K + V^T tile image
-//                 from the pool into a 5-stage shared-memory ring with one bulk
-//                 async copy (TMA engine); the pool already stores tiles in the
-//                 tensor cores' 128-byte-swizzled K-major layout, and Q is
-//                 written in the same layout.
+//   warp 0      : producer.  Lane 0 moves each tile's 32 KB K + V^T image
+//                 from the pool into a 5-stage shared-memory ring by bulk
+//                 async copy (TMA engine): one copy for a 64-token chunk; for
+//                 keys [64h, 64h + 64) of a 128-token chunk, rows 64h .. of
+//                 each 128-byte column block of K and column block h of V^T.
+//                 The pool already stores tiles in the tensor cores'
+//                 128-byte-swizzled K-major layout (the swizzle follows the
+//                 row index mod 8, so a 64-row part of a block is itself a
+//                 block of that layout), and Q is written in the same layout.
 //   warp 6      : gathers the next item's query rows into the other half of a
 //                 double-buffered Q tile while the current item computes.
 //   warp 1      : allocates TMEM and issues S = Q K^T (M=128, N=64, K=D) into
@@ -75,10 +80,14 @@ __device__ __forceinline__ uint32_t pack2_plain(float a, float b) {
   }
 }
 
-template <typename T, int D>
+template <typename T, int D, int CP>
 __global__ void __launch_bounds__(256, 1) attn_tc_kernel(const AttnParams p) {
   constexpr uint32_t HALF = kC * D * 2;
   constexpr uint32_t TILE = tc_tile_bytes(D);
+  constexpr int SUB = CP / kC;                    // 64-key tiles per pool chunk
+  constexpr uint32_t PHALF = CP * D * 2;          // a pool chunk's K block (per KV head)
+  constexpr uint32_t PTILE = 2 * PHALF;           // a pool chunk's K + V^T blocks
+  static_assert(SUB == 1 || SUB == 2, "chunk size 64 or 128");
   constexpr uint32_t QB = tc_q_bytes(D);
   constexpr int DCH = D / 8;    // 16-byte chunks per row when the reduction runs over D
   constexpr int CCH = kC / 8;   // 16-byte chunks per row when the reduction runs over keys
@@ -160,16 +169,26 @@ __global__ void __launch_bounds__(256, 1) attn_tc_kernel(const AttnParams p) {
       bool ok = true;
       for (int ii = i0; ii < i1 && ok; ++ii) {
         const WorkItem w = p.items[ii];
-        for (int c = 0; c < w.n_chunks; ++c, ++t) {
+        const int nt = w.n_chunks * SUB;
+        for (int c = 0; c < nt; ++c, ++t) {
           const int s = t % kNS;
           if (t >= kNS && !ptx::mbar_wait(&empty[s], ((t / kNS) - 1) & 1, abort_flag, p.err)) {
             ok = false;
             break;
           }
-          const int chunk = p.chunks[w.chunk_off + c];
-          const uint8_t* src = p.pool + (static_cast<size_t>(chunk) * p.Hkv + w.kv) * TILE;
+          const int chunk = p.chunks[w.chunk_off + c / SUB];
+          const uint8_t* src = p.pool + (static_cast<size_t>(chunk) * p.Hkv + w.kv) * PTILE;
+          uint8_t* dst = kvs + s * TILE;
           ptx::mbar_arrive_expect_tx(&full[s], TILE);
-          ptx::bulk_g2s_hint(kvs + s * TILE, src, TILE, &full[s], pol);
+          if constexpr (SUB == 1) {
+            ptx::bulk_g2s_hint(dst, src, TILE, &full[s], pol);
+          } else {
+            const int h = c % SUB;
+#pragma unroll
+            for (int kb = 0; kb < D / 64; ++kb)  // K column block kb: rows 64h .. 64h + 63
+              ptx::bulk_g2s_hint(dst + kb * (kC * 128), src + kb * (CP * 128) + h * (kC * 128), kC * 128, &full[s], pol);
+            ptx::bulk_g2s_hint(dst + HALF, src + PHALF + h * (D * 128), D * 128, &full[s], pol);  // V^T column block h
+          }
           *issued_slot = t + 1;
         }
       }
@@ -263,7 +282,7 @@ __global__ void __launch_bounds__(256, 1) attn_tc_kernel(const AttnParams p) {
       // ahead as the kSB S buffers allow, so the softmax threads find each S
       // ready when they finish the previous chunk.
       int s_ii = i0, s_c = 0, s_t = 0;
-      int s_nk = i0 < i1 ? p.items[i0].n_chunks : 0;
+      int s_nk = i0 < i1 ? p.items[i0].n_chunks * SUB : 0;
       auto issue_next_s = [&]() -> bool {
         const int it = s_ii - i0, qb = it & 1;
         if (s_c == 0) {  // the item's Q tile
@@ -276,7 +295,7 @@ __global__ void __launch_bounds__(256, 1) attn_tc_kernel(const AttnParams p) {
         if (++s_c == s_nk) {
           s_c = 0;
           ++s_ii;
-          s_nk = s_ii < i1 ? p.items[s_ii].n_chunks : 0;
+          s_nk = s_ii < i1 ? p.items[s_ii].n_chunks * SUB : 0;
         }
         return true;
       };
@@ -287,7 +306,7 @@ __global__ void __launch_bounds__(256, 1) attn_tc_kernel(const AttnParams p) {
         int t = 0;
         for (int ii = i0; ii < i1 && ok; ++ii) {
           const int it = ii - i0;
-          const int nk = p.items[ii].n_chunks;
+          const int nk = p.items[ii].n_chunks * SUB;
           for (int c = 0; c < nk && ok; ++c, ++t) ok = issue_pv(t, it, c, c + 1 == nk);
         }
       }
@@ -312,7 +331,7 @@ __global__ void __launch_bounds__(256, 1) attn_tc_kernel(const AttnParams p) {
     for (int ii = i0; ii < i1 && ok; ++ii) {
       const int it = ii - i0, ob = it & 1;
       const WorkItem w = p.items[ii];
-      const int nk = w.n_chunks;
+      const int nk = w.n_chunks * SUB;  // 64-key tiles
       const bool row_valid = r < w.n_rows;
       int grp = 0, hg = 0;
       if (row_valid) {
@@ -326,9 +345,12 @@ __global__ void __launch_bounds__(256, 1) attn_tc_kernel(const AttnParams p) {
       int my_len = 0;
 
       for (int c = 0; c < nk; ++c, ++t) {
-        if ((c & 31) == 0) {  // valid tokens of chunks c .. c+31, one per lane
+        if ((c & 31) == 0) {  // valid keys of tiles c .. c+31, one per lane
           my_len = 0;
-          if (c + lane < nk) my_len = p.chunk_len[p.chunks[w.chunk_off + c + lane]];
+          if (c + lane < nk) {
+            const int cl = p.chunk_len[p.chunks[w.chunk_off + (c + lane) / SUB]] - ((c + lane) % SUB) * kC;
+            my_len = min(kC, max(0, cl));
+          }
         }
         const int lim = min(__shfl_sync(0xffffffffu, my_len, c & 31), key_limit - c * kC);
         const int b = t & 1, sb = t % kSB;
@@ -467,10 +489,10 @@ __global__ void __launch_bounds__(256, 1) attn_tc_kernel(const AttnParams p) {
   if (p.pdl) ptx::pdl_wait();  // never complete before the kernel we overlap
 }
 
-template <typename T, int D>
+template <typename T, int D, int CP>
 cudaError_t launch_tc_t(const AttnParams& p, int grid, cudaStream_t s) {
   const size_t smem = tc_smem_bytes(D);
-  auto fn = attn_tc_kernel<T, D>;
+  auto fn = attn_tc_kernel<T, D, CP>;
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -486,22 +508,29 @@ cudaError_t launch_tc_t(const AttnParams& p, int grid, cudaStream_t s) {
   return cudaLaunchKernelEx(&cfg, fn, p);
 }
 
+template <typename T, int D>
+cudaError_t launch_tc_c(int C, const AttnParams& p, int grid, cudaStream_t s) {
+  if (C == kC) return launch_tc_t<T, D, kC>(p, grid, s);
+  if (C == 2 * kC) return launch_tc_t<T, D, 2 * kC>(p, grid, s);
+  return cudaErrorInvalidValue;
+}
+
 }  // namespace
 
 bool tc_supported(int dtype, int D, int C) {
-  return (dtype == kF16 || dtype == kBF16) && (D == 64 || D == 128) && C == kC;
+  return (dtype == kF16 || dtype == kBF16) && (D == 64 || D == 128) && (C == kC || C == 2 * kC);
 }
 
 size_t attn_tc_smem(int D) { return tc_smem_bytes(D); }
 
-cudaError_t launch_attn_tc(int dtype, int D, const AttnParams& p, int grid, cudaStream_t s) {
+cudaError_t launch_attn_tc(int dtype, int D, int C, const AttnParams& p, int grid, cudaStream_t s) {
   if (grid <= 0) return cudaSuccess;
   if (dtype == kF16) {
-    if (D == 128) return launch_tc_t<__half, 128>(p, grid, s);
-    if (D == 64) return launch_tc_t<__half, 64>(p, grid, s);
+    if (D == 128) return launch_tc_c<__half, 128>(C, p, grid, s);
+    if (D == 64) return launch_tc_c<__half, 64>(C, p, grid, s);
   } else if (dtype == kBF16) {
-    if (D == 128) return launch_tc_t<__nv_bfloat16, 128>(p, grid, s);
-    if (D == 64) return launch_tc_t<__nv_bfloat16, 64>(p, grid, s);
+    if (D == 128) return launch_tc_c<__nv_bfloat16, 128>(C, p, grid, s);
+    if (D == 64) return launch_tc_c<__nv_bfloat16, 64>(C, p, grid, s);
   }
   return cudaErrorInvalidValue;
 }

@@ -413,19 +413,25 @@ pst_status rebuild(pst_pool* p) {
   std::vector<int32_t> tc_rows;  // tensor-core item row -> partial row
   std::vector<Stream> streams;
 
-  // ---- phase 1: chunk-first over the runs
+  // ---- phase 1: chunk-first over the runs.  The tensor-core kernel takes a
+  // chunk as tiles of 64 keys (two for 128-token chunks): its costs and item
+  // lengths are counted in tiles.
+  const int32_t sub = p->use_tc ? p->C / 64 : 1;
   int64_t p1_iters = 0;
   for (const auto& r : runs) {
     const int32_t id0 = r.front();
     const int64_t rows = static_cast<int64_t>(nj[id0] - ni[id0]) * g;
-    p1_iters += static_cast<int64_t>(r.size()) * Hkv * (p->use_tc ? ceil_div(rows, 128) : (nj[id0] - ni[id0]));
+    p1_iters += static_cast<int64_t>(r.size()) * sub * Hkv * (p->use_tc ? ceil_div(rows, 128) : (nj[id0] - ni[id0]));
     (void)rows;
   }
   // chunk-first items: enough of them to cover every SM when the phases run
-  // back to back; fewer, longer ones when they share the GPU
-  const int64_t split1 = (p->cfg.flags & PST_FLAG_CONCURRENT_PHASES)
-                             ? 8
-                             : std::min<int64_t>(p->tc_max_run, std::max<int64_t>(2, ceil_div(p1_iters, std::max(1, p->n_sm))));
+  // back to back; fewer, longer ones when they share the GPU (in chunks)
+  const int64_t split1 =
+      std::max<int64_t>(1, ((p->cfg.flags & PST_FLAG_CONCURRENT_PHASES)
+                                ? 8
+                                : std::min<int64_t>(p->tc_max_run,
+                                                    std::max<int64_t>(2, ceil_div(p1_iters, std::max(1, p->n_sm))))) /
+                               sub);
   for (const auto& r : runs) {
     const int32_t i = ni[r.front()], j = nj[r.front()];
     const int32_t rows = (j - i) * g;
@@ -492,7 +498,7 @@ pst_status rebuild(pst_pool* p) {
     double w_tc = 0;
     for (int32_t x = 0; x < n; ++x) {
       const bool first_tile = tc_items[8 * x + 4] == 0;  // row0: the run's first row tile reads its tiles from DRAM
-      cost[x] = tc_items[8 * x + 1] * (p->tc_chunk_us + (first_tile ? p->tc_hbm_us : 0.0)) + p->tc_item_us;
+      cost[x] = tc_items[8 * x + 1] * sub * (p->tc_chunk_us + (first_tile ? p->tc_hbm_us : 0.0)) + p->tc_item_us;
       w_tc += cost[x];
     }
     const double max_cost = *std::max_element(cost.begin(), cost.end());
@@ -727,7 +733,8 @@ pst_status pst_pool_create(const pst_config* cfg, int device, pst_pool** out) {
   if (c.dtype < 0 || c.dtype > 2) return fail(PST_ERR_INVALID, "bad dtype %d", c.dtype);
   if (!simt_supported(c.dtype, c.head_dim, g))
     return fail(PST_ERR_INVALID, "unsupported head_dim %d / group %d", c.head_dim, g);
-  if (c.chunk_size != 32 && c.chunk_size != 64) return fail(PST_ERR_INVALID, "chunk_size must be 32 or 64");
+  if (c.chunk_size != 16 && c.chunk_size != 32 && c.chunk_size != 64 && c.chunk_size != 128)
+    return fail(PST_ERR_INVALID, "chunk_size must be 16, 32, 64 or 128");
   if (c.max_chunks < 1 || c.max_chunks > (int64_t(1) << 30)) return fail(PST_ERR_INVALID, "bad max_chunks");
   if (c.min_share < 0 || c.max_seqs < 0) return fail(PST_ERR_INVALID, "negative min_share / max_seqs");
   if (device < -1) return fail(PST_ERR_INVALID, "bad device");
@@ -770,6 +777,9 @@ pst_status pst_pool_create(const pst_config* cfg, int device, pst_pool** out) {
   // stream fed (fewer bytes in flight, shorter queues); larger groups compute
   // longer per piece and want a deeper ring
   p->simt_stages = (c.dtype != kF32 && g == 1) ? 2 : 6;
+  // pieces smaller than 8 KB (chunks of 16 keys, 16-bit V^T rows of 32 keys)
+  // keep about the same bytes in flight with proportionally more stages
+  p->simt_stages = std::min<int>(16, p->simt_stages * std::max<int>(1, static_cast<int>(8192 / attn_simt_piece_bytes(c.dtype, p->D, p->C))));
   if (const char* e = std::getenv("PST_SIMT_WPC"))
     p->simt_wpc = std::max(1, std::min(attn_simt_max_warps(c.dtype, g), std::atoi(e)));
   if (const char* e = std::getenv("PST_SIMT_STAGES")) p->simt_stages = std::max(2, std::min(16, std::atoi(e)));
@@ -1009,7 +1019,7 @@ static pst_status launch_overlapped(pst_pool* p, const AttnParams& a, int32_t B,
     a1.n_items = p->n_tc_items;
     a1.warp_items = p->d_tab + p->off_tc_cta;
     a1.pdl = before ? 1 : 0;
-    cudaError_t e = launch_attn_tc(p->cfg.dtype, p->D, a1, p->n_tc_ctas, s);
+    cudaError_t e = launch_attn_tc(p->cfg.dtype, p->D, p->C, a1, p->n_tc_ctas, s);
     if (e != cudaSuccess) return fail(PST_ERR_CUDA, "chunk-first launch: %s", cudaGetErrorString(e));
     p->last_launches++;
     before = true;
@@ -1100,7 +1110,7 @@ static pst_status launch_step_impl(pst_pool* p, const void* q, void* out, cudaSt
     a1.n_items = p->n_tc_items;
     a1.warp_items = p->d_tab + p->off_tc_cta;
     if (p->profiling) CUDA_TRY(cudaEventRecord(p->pev[0], s1));
-    cudaError_t e = launch_attn_tc(p->cfg.dtype, p->D, a1, p->n_tc_ctas, s1);
+    cudaError_t e = launch_attn_tc(p->cfg.dtype, p->D, p->C, a1, p->n_tc_ctas, s1);
     if (e != cudaSuccess) return fail(PST_ERR_CUDA, "chunk-first launch: %s", cudaGetErrorString(e));
     if (p->profiling) CUDA_TRY(cudaEventRecord(p->pev[1], s1));
     p->pran[0] = true;
@@ -1359,7 +1369,7 @@ pst_status pst_prefill_attend(pst_pool* p, int64_t seq_id, const int32_t* tokens
   cudaError_t e;
   a.warp_items = p->d_pre + off_warp;
   if (p->use_tc) {
-    e = launch_attn_tc(p->cfg.dtype, p->D, a, n_items, s);
+    e = launch_attn_tc(p->cfg.dtype, p->D, p->C, a, n_items, s);
   } else {
     CUDA_TRY(cudaMemsetAsync(p->d_sched, 0, sizeof(int32_t), s));
     (void)n_warps;

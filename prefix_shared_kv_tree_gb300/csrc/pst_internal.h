@@ -146,12 +146,18 @@ cudaError_t launch_scatter(int dtype, int D, int C, const ScatterParams& p, cuda
 cudaError_t launch_gather(int dtype, int D, int C, const ScatterParams& p, cudaStream_t s);
 cudaError_t launch_attn_simt(int dtype, int D, int C, int g, const AttnParams& p, int grid, cudaStream_t s);
 size_t attn_simt_smem(int dtype, int D, int C, int g, int stages, int warps_per_cta);
+size_t attn_simt_piece_bytes(int dtype, int D, int C);  // bytes of one ring stage of the CUDA-core kernel
 int attn_simt_max_warps(int dtype, int g);  // consumer warps per CTA of the CUDA-core kernel, at most
-// per-dtype launchers (one translation unit each)
-cudaError_t launch_attn_simt_f16(int D, int C, int g, const AttnParams& p, int grid, cudaStream_t s);
-cudaError_t launch_attn_simt_bf16(int D, int C, int g, const AttnParams& p, int grid, cudaStream_t s);
-cudaError_t launch_attn_simt_f32(int D, int C, int g, const AttnParams& p, int grid, cudaStream_t s);
-cudaError_t launch_attn_tc(int dtype, int D, const AttnParams& p, int grid, cudaStream_t s);
+// per-dtype launchers for chunk sizes 64 / 128 (large) and 16 / 32 (small),
+// one translation unit each
+#define PST_SIMT_LAUNCHER(dt)                                                                                   \
+  cudaError_t launch_attn_simt_##dt##_large(int D, int C, int g, const AttnParams& p, int grid, cudaStream_t s); \
+  cudaError_t launch_attn_simt_##dt##_small(int D, int C, int g, const AttnParams& p, int grid, cudaStream_t s);
+PST_SIMT_LAUNCHER(f16)
+PST_SIMT_LAUNCHER(bf16)
+PST_SIMT_LAUNCHER(f32)
+#undef PST_SIMT_LAUNCHER
+cudaError_t launch_attn_tc(int dtype, int D, int C, const AttnParams& p, int grid, cudaStream_t s);
 size_t attn_tc_smem(int D);
 // Merge of the partial rows of every (batch row, KV head) pair into `out`
 // (one warp per pair); a programmatic dependent of the previous kernel when

@@ -345,6 +345,14 @@ __device__ __forceinline__ void ldsm_x4_trans(uint32_t saddr, uint32_t (&r)[4]) 
                : "r"(saddr));
 }
 
+// Two transposed 8 x 8 matrices: lanes 0 .. 15 give the row addresses
+// (lanes 8i .. 8i+7 those of matrix i; the other lanes' are not read).
+__device__ __forceinline__ void ldsm_x2_trans(uint32_t saddr, uint32_t (&r)[2]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0,%1}, [%2];"
+               : "=r"(r[0]), "=r"(r[1])
+               : "r"(saddr));
+}
+
 // d (16 x 8 fp32) += a (16 x 16, row-major) * b (16 x 8, column-major), 16-bit
 // operands of one type.  Fragments: a[0..3] = rows g / g+8 at columns 2q, 2q+1,
 // then the same at columns 2q+8, 2q+9 (order a0: (g, k), a1: (g+8, k),

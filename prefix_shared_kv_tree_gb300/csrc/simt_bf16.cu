@@ -1,11 +1,12 @@
-// Instantiations of the CUDA-core attention kernel for __nv_bfloat16 elements (one
-// translation unit per element type keeps the build parallel).
+// Instantiations of the CUDA-core attention kernel for __nv_bfloat16 elements at
+// chunk sizes 64 and 128 (one translation unit per element type and chunk-size pair
+// keeps the build parallel).
 #include "attn_simt.cuh"
 
 namespace pst {
 
-cudaError_t launch_attn_simt_bf16(int D, int C, int g, const AttnParams& p, int grid, cudaStream_t s) {
-  return launch_simt_dc<__nv_bfloat16>(D, C, g, p, grid, s);
+cudaError_t launch_attn_simt_bf16_large(int D, int C, int g, const AttnParams& p, int grid, cudaStream_t s) {
+  return launch_simt_dc<__nv_bfloat16, 64, 128>(D, C, g, p, grid, s);
 }
 
 }  // namespace pst

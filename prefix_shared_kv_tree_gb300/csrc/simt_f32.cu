@@ -1,11 +1,12 @@
-// Instantiations of the CUDA-core attention kernel for float elements (one
-// translation unit per element type keeps the build parallel).
+// Instantiations of the CUDA-core attention kernel for float elements at
+// chunk sizes 64 and 128 (one translation unit per element type and chunk-size pair
+// keeps the build parallel).
 #include "attn_simt.cuh"
 
 namespace pst {
 
-cudaError_t launch_attn_simt_f32(int D, int C, int g, const AttnParams& p, int grid, cudaStream_t s) {
-  return launch_simt_dc<float>(D, C, g, p, grid, s);
+cudaError_t launch_attn_simt_f32_large(int D, int C, int g, const AttnParams& p, int grid, cudaStream_t s) {
+  return launch_simt_dc<float, 64, 128>(D, C, g, p, grid, s);
 }
 
 }  // namespace pst

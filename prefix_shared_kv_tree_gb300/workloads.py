@@ -128,6 +128,17 @@ for _i, (_ns, _nc) in enumerate(DIVERGENCE_GRID):
     SPECS[_name] = WorkloadSpec(_name, 32, 32, 128, 64, "f16", ((_ns, 1), (_nc, 32)), 1300 + _i)
     DESCRIPTIONS[_name] = f"32 heads, d=128, fp16, batch 32, {_ns} shared + {_nc} private, chunk 64"
 
+# Head-dim / chunk-size generality (ChunkAttention, Knowl 10: the kernel is
+# specialised for common head dims, and porting it to others is listed as a
+# limitation): the share1k tree (32 heads, fp16, batch 32, 1024 shared + 512
+# private) at d in {64, 128} and c in {16, 32, 64, 128}.
+GENERALITY_GRID = tuple((d, c) for d in (128, 64) for c in (16, 32, 64, 128))
+GENERALITY_FAMILY = tuple(f"gen_d{d}_c{c}" for d, c in GENERALITY_GRID)
+for _i, (_d, _c) in enumerate(GENERALITY_GRID):
+    _name = f"gen_d{_d}_c{_c}"
+    SPECS[_name] = WorkloadSpec(_name, 32, 32, _d, _c, "f16", ((1024, 1), (512, 32)), 1400 + _i)
+    DESCRIPTIONS[_name] = f"32 heads, d={_d}, fp16, batch 32, 1024 shared + 512 private, chunk {_c}"
+
 
 @dataclass
 class Segment:

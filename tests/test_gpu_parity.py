@@ -138,6 +138,20 @@ CASES = [
     ("f16", 4, 2, 128, 32, 0, 0),           # c = 32: CUDA-core path for both phases
     ("f32", 2, 1, 64, 32, 0, 0),
     ("f32", 8, 1, 128, 64, 0, 3),
+    # c = 128: the tensor-core kernel takes each chunk as two 64-key tiles;
+    # two 128-byte key blocks per 16-bit V^T row in the CUDA-core kernel
+    ("f16", 4, 2, 128, 128, 0, 0),
+    ("bf16", 8, 1, 64, 128, 0, 0),
+    ("bf16", 8, 2, 128, 128, 1, 0),         # chunk-first phase on the CUDA-core kernel
+    ("f16", 2, 2, 128, 128, 0, 2**31 - 1),
+    ("f32", 8, 2, 128, 128, 0, 0),          # one fp32 accumulator pair per key
+    ("f32", 8, 1, 128, 128, 0, 0),
+    # c = 16: one 16-key tile per chunk (16-bit), half a warp of keys (fp32)
+    ("f16", 4, 4, 128, 16, 0, 0),
+    ("bf16", 8, 2, 64, 16, 0, 0),
+    ("bf16", 8, 1, 128, 16, 0, 2**31 - 1),
+    ("f32", 4, 2, 128, 16, 0, 0),
+    ("f32", 2, 2, 64, 16, 0, 0),
 ]
 
 
@@ -188,9 +202,10 @@ def test_ragged_tree_all_rows(pst, case):
     _assert_close(_f64(out), ref, dtype, with_ulp=True, what=str(case))
 
 
-@pytest.mark.parametrize("dtype,hq,hkv", [("f16", 4, 2), ("bf16", 8, 2), ("f32", 2, 2)])
-def test_dynamic_tree_appends_and_removes(pst, dtype, hq, hkv):
-    d, c = 128, 64 if dtype != "f32" else 32
+@pytest.mark.parametrize("dtype,hq,hkv,c", [("f16", 4, 2, 64), ("bf16", 8, 2, 64), ("f32", 2, 2, 32),
+                                            ("f16", 4, 2, 16), ("bf16", 4, 4, 128)])
+def test_dynamic_tree_appends_and_removes(pst, dtype, hq, hkv, c):
+    d = 128
     seqs, q = _ragged_tree(5, dtype, hq, hkv, d, c, n_seqs=6)
     pool = pst.Pool(hq, hkv, d, c, 512, dtype, 0, 0, 0, device=0)
     kv = {}
@@ -271,7 +286,8 @@ def _sample_rows(b, hq, n, seed):
     return sorted(rows)
 
 
-@pytest.mark.parametrize("name", ["share1k", "share4k", "noshare", "gqa_tree", "batch96", "div_s1024_c1024"])
+@pytest.mark.parametrize("name", ["share1k", "share4k", "noshare", "gqa_tree", "batch96", "div_s1024_c1024",
+                                  "gen_d128_c128", "gen_d64_c16"])
 def test_full_config_sampled_rows(pst, name):
     spec = W.SPECS[name]
     wl = W.generate(spec, device="cuda")
@@ -352,6 +368,11 @@ PREFILL_CASES = [
     ("bf16", 8, 8, 64, 64, 0, 70, [200]),
     ("f16", 4, 1, 128, 64, 1, 33, [3, 61]),       # CUDA-core prefill
     ("f32", 2, 1, 64, 32, 0, 31, [33, 2, 40]),
+    ("bf16", 8, 2, 128, 128, 0, 100, [130, 7]),   # c = 128: two tiles per chunk, the last one partial
+    ("f16", 4, 4, 128, 128, 0, 0, [50, 20]),      # c = 128: a tile with no valid key
+    ("bf16", 8, 2, 64, 128, 1, 40, [100]),        # c = 128: CUDA-core prefill
+    ("f16", 4, 4, 64, 16, 0, 20, [40, 1, 77]),    # c = 16: runs of more than four chunks
+    ("f32", 2, 1, 64, 16, 0, 5, [17, 30]),
 ]
 
 

@@ -35,7 +35,7 @@ def test_library_exports_every_declared_symbol(pst):
 
 
 def _pool(pst, c=4, min_share=0, max_chunks=10_000, max_seqs=0):
-    return pst.Pool(1, 1, 64, c if c in (32, 64) else 32, max_chunks, "f16", min_share, max_seqs, device=-1)
+    return pst.Pool(1, 1, 64, c if c in (16, 32, 64, 128) else 32, max_chunks, "f16", min_share, max_seqs, device=-1)
 
 
 def _same(pool, tree):
@@ -51,10 +51,9 @@ def _same(pool, tree):
     assert st["logical_tokens"] == sum(tree.lengths.values())
 
 
-@pytest.mark.parametrize("seed", range(8))
-def test_random_histories_bit_exact(pst, seed):
-    rng = np.random.default_rng(100 + seed)
-    c = 32
+@pytest.mark.parametrize("seed,c", [(s, 32) for s in range(8)] + [(s, c) for s in range(3) for c in (16, 128)])
+def test_random_histories_bit_exact(pst, seed, c):
+    rng = np.random.default_rng(100 + seed + (0 if c == 32 else 10 * c))
     min_share = int(rng.choice([2, 3]))
     pool = _pool(pst, c, min_share)
     tree = PrefixTree(c, min_share)
