@@ -13,6 +13,16 @@
  * Chunked Prefill (onnx-genai wiki), sections 1-2: a W-row causal query block
  * attends to an append-only cache and equals single-pass prefill.
  *
+ * Layers: a pool may hold the K/V of n_layers decoder layers under one prefix
+ * tree (the tree and the chunk tables depend on token ids only, so every
+ * layer shares them; Knowl 5 builds the context once per step, behind the
+ * layers' earlier kernels).  Calls that take K/V for a token range without a
+ * layer argument (insert, append, append_batch, prefill_attend, gather_kv)
+ * take all layers at once, layer-major: [n_layers][n][Hkv][d].  Attention
+ * calls without a layer argument read layer 0.  The *_layer calls and
+ * pst_write_kv / pst_write_kv_last serve one layer at a time, for a model
+ * whose layer l K/V exist only after layer l-1 ran.
+ *
  * Conventions for every entry point:
  *   - Returns a pst_status; on failure pst_last_error() holds a message for
  *     the calling thread.  No C++ exception crosses this boundary.
@@ -70,6 +80,7 @@ typedef struct {
                           multiple sequences"); 0 means 2; INT32_MAX disables phase 1 */
   int32_t max_seqs;    /* capacity of live sequences; 0 means 4096 */
   int32_t flags;       /* PST_FLAG_* */
+  int32_t n_layers;    /* K/V layers under the one tree, in [0, 1024]; 0 means 1 */
 } pst_config;
 
 typedef struct pst_pool pst_pool;
@@ -92,7 +103,7 @@ typedef struct {
 } pst_stats_t;
 
 /* Create a pool.  device >= 0: CUDA device ordinal; the pool allocates its
- * chunk slab (2 * max_chunks * Hkv * c * d elements), tables and scratch there
+ * chunk slab (n_layers * 2 * max_chunks * Hkv * c * d elements), tables and scratch there
  * and keeps them until pst_pool_free.  device == -1: host-only pool that runs
  * the prefix tree and tables but owns no device memory; every call that needs
  * the GPU then returns PST_ERR_STATE (k/v must be NULL on insert).
@@ -109,22 +120,26 @@ pst_status pst_match(const pst_pool* pool, const int32_t* tokens, int64_t n, int
 
 /* Sequence arrival (Knowl 1): match the longest full-chunk prefix, share it,
  * allocate chunks for the rest and copy their K/V into the pool.
- * tokens: host int32[n], n >= 1.  k, v: device [n][Hkv][d]; only rows
- * >= n_matched are read (they may be NULL when n_matched == n).
+ * tokens: host int32[n], n >= 1.  k, v: device [n_layers][n][Hkv][d]; only rows
+ * >= n_matched are read.  k = v = NULL: the tree changes but no K/V is
+ * written; the caller then writes rows [n_matched, n) of every layer with
+ * pst_write_kv before any attention reads them.
  * Atomic: on PST_ERR_OOM nothing changed.  *seq_id receives the new id (ids
  * count up from 0 and are never reused), *n_matched the shared token count. */
 pst_status pst_insert(pst_pool* pool, const int32_t* tokens, int64_t n, const void* k, const void* v,
                       void* stream, int64_t* seq_id, int64_t* n_matched);
 
 /* Decode append (Knowl 1, decoding iteration): write one token's K/V
- * (device [Hkv][d] each) into the sequence's leaf chunk, or into a new chunk
- * when the leaf is full. */
+ * (device [n_layers][Hkv][d] each) into the sequence's leaf chunk, or into a
+ * new chunk when the leaf is full.  k = v = NULL: the token is added to the
+ * tree only; write its K/V per layer with pst_write_kv_last. */
 pst_status pst_append(pst_pool* pool, int64_t seq_id, int32_t token, const void* k, const void* v,
                       void* stream);
 
 /* Batched decode append: n tokens for n distinct sequences.  seq_ids: host
- * int64[n]; tokens: host int32[n]; k, v: device [n][Hkv][d].  One kernel
- * launch.  Atomic on PST_ERR_OOM / NOT_FOUND / INVALID (duplicate ids). */
+ * int64[n]; tokens: host int32[n]; k, v: device [n_layers][n][Hkv][d], or both
+ * NULL (tree only, as for pst_append).  One kernel launch per layer.  Atomic
+ * on PST_ERR_OOM / NOT_FOUND / INVALID (duplicate ids). */
 pst_status pst_append_batch(pst_pool* pool, int64_t n, const int64_t* seq_ids, const int32_t* tokens,
                             const void* k, const void* v, void* stream);
 
@@ -202,17 +217,50 @@ pst_status pst_decode_attention_noalloc(pst_pool* pool, const void* q, void* out
 pst_status pst_decode_attention_graph(pst_pool* pool, const void* q, void* out, void* stream);
 
 /* Chunked-prefill attend (Chunked Prefill, sections 1-2): append W tokens
- * (host tokens int32[W], device k_new/v_new [W][Hkv][d]) to sequence seq_id at
+ * (host tokens int32[W], device k_new/v_new [n_layers][W][Hkv][d]) to sequence seq_id at
  * positions [p0, p0+W), p0 = its current length, then out[t][h] =
  * softmax(q[t][h] K^T / sqrt(d)) V over keys [0, p0+t] of the sequence.
  * q, out: device [W][Hq][d], 16-byte aligned.  Appended tokens are never merged with other
- * sequences' chunks.  Atomic on PST_ERR_OOM. */
+ * sequences' chunks.  Attention reads layer 0.  Atomic on PST_ERR_OOM. */
 pst_status pst_prefill_attend(pst_pool* pool, int64_t seq_id, const int32_t* tokens, int64_t W,
                               const void* q, const void* k_new, const void* v_new, void* out,
                               void* stream);
 
-/* Read a sequence's cached K/V back into device k_out, v_out [n][Hkv][d]
- * (n = its length), byte-exact. */
+/* Append W tokens (host int32[W]) to sequence seq_id as a chunked-prefill
+ * block, tree only: no K/V is written (pst_write_kv writes each layer's rows,
+ * pst_prefill_attend_layer attends).  Appended tokens are never merged with
+ * other sequences' chunks.  Atomic on PST_ERR_OOM.  Works on host-only pools. */
+pst_status pst_extend(pst_pool* pool, int64_t seq_id, const int32_t* tokens, int64_t W);
+
+/* Write layer `layer`'s K/V of the sequence's last n tokens (device k, v
+ * [n][Hkv][d]), e.g. a block added by pst_extend or a prompt inserted with
+ * k = v = NULL.  Rows in chunks that other live sequences share are not
+ * written: PST_ERR_STATE (a shared chunk got its K/V from the insert that
+ * created it).  One kernel launch. */
+pst_status pst_write_kv(pst_pool* pool, int32_t layer, int64_t seq_id, int64_t n, const void* k,
+                        const void* v, void* stream);
+
+/* Write layer `layer`'s K/V of the last token of each of n sequences (host
+ * seq_ids int64[n]; device k, v [n][Hkv][d]): the per-layer half of a decode
+ * append made with k = v = NULL.  PST_ERR_STATE if a last token lies in a
+ * shared chunk.  One kernel launch. */
+pst_status pst_write_kv_last(pst_pool* pool, int32_t layer, int64_t n, const int64_t* seq_ids,
+                             const void* k, const void* v, void* stream);
+
+/* pst_decode_attention on layer `layer` (0 <= layer < n_layers): the same
+ * tables, that layer's K/V. */
+pst_status pst_decode_attention_layer(pst_pool* pool, int32_t layer, const void* q, void* out,
+                                      void* stream);
+
+/* Causal attention of the W query rows at positions [p0, p0 + W) of sequence
+ * seq_id over its keys [0, p0 + t] in layer `layer` (Chunked Prefill, sections
+ * 1-2); appends nothing.  p0 + W <= the sequence's length; q, out: device
+ * [W][Hq][d], 16-byte aligned. */
+pst_status pst_prefill_attend_layer(pst_pool* pool, int32_t layer, int64_t seq_id, int64_t p0, int64_t W,
+                                    const void* q, void* out, void* stream);
+
+/* Read a sequence's cached K/V back into device k_out, v_out
+ * [n_layers][n][Hkv][d] (n = its length), byte-exact. */
 pst_status pst_gather_kv(const pst_pool* pool, int64_t seq_id, void* k_out, void* v_out, void* stream);
 
 /* Canonical (chunk-id free) tables, for bit-exact comparison:

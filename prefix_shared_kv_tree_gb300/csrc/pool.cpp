@@ -92,6 +92,8 @@ struct pst_pool {
   int es = 2;
   int C = 64, D = 128, g = 1;
   size_t half_bytes = 0, tile_bytes = 0;
+  int32_t n_layers = 1;
+  size_t layer_bytes = 0;  // one layer's K/V: max_chunks x Hkv tiles
   int n_sm = 1;
   bool use_tc = false;
   float scale_log2 = 0.f;
@@ -250,14 +252,15 @@ void mark_structural(pst_pool* p) {
   p->version++;
 }
 
-// Launch scatter ops in batches of kScatterMax.
+// Launch scatter ops into (or, gathering, out of) one layer's K/V, in batches
+// of kScatterMax.
 pst_status run_scatter(pst_pool* p, const std::vector<ScatterOp>& ops, const void* k, const void* v,
-                       cudaStream_t s, bool gather) {
+                       cudaStream_t s, bool gather, int32_t layer = 0) {
   if (p->host_only || ops.empty()) return PST_OK;
   ScatterParams sp;
   sp.k = static_cast<const uint8_t*>(k);
   sp.v = static_cast<const uint8_t*>(v);
-  sp.pool = p->d_pool;
+  sp.pool = p->d_pool + static_cast<size_t>(layer) * p->layer_bytes;
   sp.chunk_len = p->d_chunk_len;
   sp.Hkv = p->cfg.n_kv_heads;
   for (size_t i = 0; i < ops.size(); i += kScatterMax) {
@@ -266,6 +269,21 @@ pst_status run_scatter(pst_pool* p, const std::vector<ScatterOp>& ops, const voi
     std::memcpy(sp.ops, ops.data() + i, n * sizeof(ScatterOp));
     cudaError_t e = gather ? launch_gather(p->cfg.dtype, p->D, p->C, sp, s) : launch_scatter(p->cfg.dtype, p->D, p->C, sp, s);
     if (e != cudaSuccess) return fail(PST_ERR_CUDA, "scatter launch: %s", cudaGetErrorString(e));
+  }
+  return PST_OK;
+}
+
+// The same ops for every layer: k and v hold n_rows source rows per layer,
+// layer-major ([n_layers][n_rows][Hkv][D]).  Null k / v: nothing to write
+// (the caller writes each layer's rows later with pst_write_kv).
+pst_status scatter_layers(pst_pool* p, const std::vector<ScatterOp>& ops, const void* k, const void* v, int64_t n_rows,
+                          cudaStream_t s, bool gather = false) {
+  if (!k || !v) return PST_OK;
+  const size_t lb = static_cast<size_t>(n_rows) * p->cfg.n_kv_heads * p->D * p->es;
+  for (int32_t l = 0; l < p->n_layers; ++l) {
+    const pst_status st = run_scatter(p, ops, static_cast<const uint8_t*>(k) + l * lb,
+                                      static_cast<const uint8_t*>(v) + l * lb, s, gather, l);
+    if (st != PST_OK) return st;
   }
   return PST_OK;
 }
@@ -696,9 +714,9 @@ pst_status need_device(const pst_pool* p) {
 // every sequence-first tile belongs to one sequence, so each is read once.
 int32_t decode_evict_first(const pst_pool* p) { return (p->use_tc && p->cfg.min_share <= 2) ? 1 : 0; }
 
-AttnParams base_params(const pst_pool* p) {
+AttnParams base_params(const pst_pool* p, int32_t layer) {
   AttnParams a{};
-  a.pool = p->d_pool;
+  a.pool = p->d_pool + static_cast<size_t>(layer) * p->layer_bytes;
   a.chunk_len = p->d_chunk_len;
   a.Hq = p->cfg.n_q_heads;
   a.Hkv = p->cfg.n_kv_heads;
@@ -737,6 +755,7 @@ pst_status pst_pool_create(const pst_config* cfg, int device, pst_pool** out) {
     return fail(PST_ERR_INVALID, "chunk_size must be 16, 32, 64 or 128");
   if (c.max_chunks < 1 || c.max_chunks > (int64_t(1) << 30)) return fail(PST_ERR_INVALID, "bad max_chunks");
   if (c.min_share < 0 || c.max_seqs < 0) return fail(PST_ERR_INVALID, "negative min_share / max_seqs");
+  if (c.n_layers < 0 || c.n_layers > 1024) return fail(PST_ERR_INVALID, "n_layers %d outside [0, 1024]", c.n_layers);
   if (device < -1) return fail(PST_ERR_INVALID, "bad device");
 
   pst_pool* p = new pst_pool();
@@ -751,6 +770,8 @@ pst_status pst_pool_create(const pst_config* cfg, int device, pst_pool** out) {
   p->g = g;
   p->half_bytes = static_cast<size_t>(p->C) * p->D * p->es;
   p->tile_bytes = 2 * p->half_bytes;
+  p->n_layers = c.n_layers > 0 ? c.n_layers : 1;
+  p->layer_bytes = static_cast<size_t>(c.max_chunks) * c.n_kv_heads * p->tile_bytes;
   p->scale_log2 = static_cast<float>(1.0 / std::log(2.0) / std::sqrt(static_cast<double>(p->D)));
   p->nodes.emplace_back();  // virtual root
   p->nodes[0].live = true;
@@ -801,7 +822,7 @@ pst_status pst_pool_create(const pst_config* cfg, int device, pst_pool** out) {
     cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, device);
     cudaDeviceGetAttribute(&p->n_sm, cudaDevAttrMultiProcessorCount, device);
     p->use_tc = major == 10 && tc_supported(c.dtype, p->D, p->C) && !(c.flags & PST_FLAG_NO_TENSOR_CORES);
-    const size_t slab = static_cast<size_t>(c.max_chunks) * c.n_kv_heads * p->tile_bytes;
+    const size_t slab = p->layer_bytes * p->n_layers;
     if ((e = cudaMalloc(&p->d_pool, slab)) != cudaSuccess) return bail(e, "cudaMalloc(pool)");
     if ((e = cudaMemset(p->d_pool, 0, slab)) != cudaSuccess) return bail(e, "cudaMemset(pool)");
     if ((e = cudaMalloc(&p->d_chunk_len, sizeof(int32_t) * c.max_chunks)) != cudaSuccess) return bail(e, "cudaMalloc");
@@ -867,13 +888,9 @@ pst_status pst_insert(pst_pool* p, const int32_t* tokens, int64_t n, const void*
   const int64_t need = ceil_div(n - m, p->C);
   if (need > static_cast<int64_t>(p->free_chunks.size()))
     return fail(PST_ERR_OOM, "pool exhausted: need %lld chunks, %zu free", (long long)need, p->free_chunks.size());
-  if (m < n) {
-    if (p->host_only) {
-      if (k || v) return fail(PST_ERR_STATE, "host-only pool takes no K/V");
-    } else if (!k || !v) {
-      return fail(PST_ERR_INVALID, "k/v required for %lld unmatched tokens", (long long)(n - m));
-    }
-  }
+  if (p->host_only ? (k || v) : (!k != !v))
+    return fail(p->host_only ? PST_ERR_STATE : PST_ERR_INVALID,
+                p->host_only ? "host-only pool takes no K/V" : "k and v must both be given or both be null");
   if (!p->host_only) {
     pst_status st = need_device(p);
     if (st != PST_OK) return st;
@@ -898,7 +915,7 @@ pst_status pst_insert(pst_pool* p, const int32_t* tokens, int64_t n, const void*
   mark_structural(p);
   *seq_id = sid;
   if (n_matched) *n_matched = m;
-  return run_scatter(p, ops, k, v, static_cast<cudaStream_t>(stream), false);
+  return scatter_layers(p, ops, k, v, n, static_cast<cudaStream_t>(stream));
 }
 
 // Apply one appended token to the tree; fills *op with its scatter op.
@@ -930,7 +947,7 @@ pst_status pst_append_batch(pst_pool* p, int64_t n, const int64_t* seq_ids, cons
                             const void* v, void* stream) {
   if (!p || n < 0 || (n > 0 && (!seq_ids || !tokens))) return fail(PST_ERR_INVALID, "bad argument");
   if (n == 0) return PST_OK;
-  if (p->host_only ? (k || v) : (!k || !v)) return fail(PST_ERR_INVALID, "k/v pointers do not match pool kind");
+  if (p->host_only ? (k || v) : (!k != !v)) return fail(PST_ERR_INVALID, "k/v pointers do not match pool kind");
   int64_t need = 0;
   std::vector<int64_t> sorted(seq_ids, seq_ids + n);
   std::sort(sorted.begin(), sorted.end());
@@ -948,7 +965,7 @@ pst_status pst_append_batch(pst_pool* p, int64_t n, const int64_t* seq_ids, cons
   }
   std::vector<ScatterOp> ops(n);
   for (int64_t x = 0; x < n; ++x) append_one(p, p->seqs[seq_ids[x]], seq_ids[x], tokens[x], &ops[x], static_cast<int32_t>(x));
-  return run_scatter(p, ops, k, v, static_cast<cudaStream_t>(stream), false);
+  return scatter_layers(p, ops, k, v, n, static_cast<cudaStream_t>(stream));
 }
 
 pst_status pst_remove(pst_pool* p, int64_t seq_id) {
@@ -1041,10 +1058,10 @@ static pst_status launch_overlapped(pst_pool* p, const AttnParams& a, int32_t B,
   return PST_OK;
 }
 
-static pst_status launch_step(pst_pool* p, const void* q, void* out, cudaStream_t s);
+static pst_status launch_step(pst_pool* p, int32_t layer, const void* q, void* out, cudaStream_t s);
 static cudaError_t clear_sched(pst_pool* p, cudaStream_t s);
 
-static pst_status decode_impl(pst_pool* p, const void* q, void* out, cudaStream_t s) {
+static pst_status decode_impl(pst_pool* p, int32_t layer, const void* q, void* out, cudaStream_t s) {
   pst_status st = ensure_tables(p);
   if (st != PST_OK) return st;
   p->last_launches = 0;
@@ -1056,7 +1073,7 @@ static pst_status decode_impl(pst_pool* p, const void* q, void* out, cudaStream_
   st = sync_device_tables(p, s);
   if (st != PST_OK) return st;
   CUDA_TRY(clear_sched(p, s));
-  return launch_step(p, q, out, s);
+  return launch_step(p, layer, q, out, s);
 }
 
 // Zero the claim counter on stream s unless it is known to be zero already;
@@ -1072,20 +1089,20 @@ static cudaError_t clear_sched(pst_pool* p, cudaStream_t s) {
 
 // The step's device work once the tables are on the device: zero the claim
 // counter, launch the attention kernels and the merge on stream s.
-static pst_status launch_step_impl(pst_pool* p, const void* q, void* out, cudaStream_t s);
+static pst_status launch_step_impl(pst_pool* p, int32_t layer, const void* q, void* out, cudaStream_t s);
 
 // A step whose launches all went out leaves the claim counter zero (its
 // merge kernel clears it); after a failed launch its state is unknown.
-static pst_status launch_step(pst_pool* p, const void* q, void* out, cudaStream_t s) {
-  const pst_status st = launch_step_impl(p, q, out, s);
+static pst_status launch_step(pst_pool* p, int32_t layer, const void* q, void* out, cudaStream_t s) {
+  const pst_status st = launch_step_impl(p, layer, q, out, s);
   p->sched_zero = st == PST_OK;
   return st;
 }
 
-static pst_status launch_step_impl(pst_pool* p, const void* q, void* out, cudaStream_t s) {
+static pst_status launch_step_impl(pst_pool* p, int32_t layer, const void* q, void* out, cudaStream_t s) {
   p->last_launches = 0;
   const int32_t B = static_cast<int32_t>(p->batch.size());
-  AttnParams a = base_params(p);
+  AttnParams a = base_params(p, layer);
   a.q = q;
   a.out = out;
   a.part_o = p->d_part_o;
@@ -1149,14 +1166,21 @@ static pst_status launch_step_impl(pst_pool* p, const void* q, void* out, cudaSt
 pst_status pst_decode_attention(pst_pool* p, const void* q, void* out, void* stream) {
   pst_status st = need_device(p);
   if (st != PST_OK) return st;
-  return decode_impl(p, q, out, static_cast<cudaStream_t>(stream));
+  return decode_impl(p, 0, q, out, static_cast<cudaStream_t>(stream));
+}
+
+pst_status pst_decode_attention_layer(pst_pool* p, int32_t layer, const void* q, void* out, void* stream) {
+  pst_status st = need_device(p);
+  if (st != PST_OK) return st;
+  if (layer < 0 || layer >= p->n_layers) return fail(PST_ERR_INVALID, "layer %d outside [0, %d)", layer, p->n_layers);
+  return decode_impl(p, layer, q, out, static_cast<cudaStream_t>(stream));
 }
 
 pst_status pst_decode_attention_graph(pst_pool* p, const void* q, void* out, void* stream) {
   pst_status st = need_device(p);
   if (st != PST_OK) return st;
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (p->profiling) return decode_impl(p, q, out, s);  // per-phase events are not captured
+  if (p->profiling) return decode_impl(p, 0, q, out, s);  // per-phase events are not captured
   st = ensure_tables(p);
   if (st != PST_OK) return st;
   p->pran[0] = p->pran[1] = p->pran[2] = false;
@@ -1177,7 +1201,7 @@ pst_status pst_decode_attention_graph(pst_pool* p, const void* q, void* out, voi
       p->g_exec = nullptr;
     }
     CUDA_TRY(cudaStreamBeginCapture(p->cap_stream, cudaStreamCaptureModeRelaxed));
-    const pst_status ls = launch_step(p, q, out, p->cap_stream);
+    const pst_status ls = launch_step(p, 0, q, out, p->cap_stream);
     cudaGraph_t graph = nullptr;
     const cudaError_t ce = cudaStreamEndCapture(p->cap_stream, &graph);
     if (ls != PST_OK) {
@@ -1229,7 +1253,7 @@ pst_status pst_decode_attention_noalloc(pst_pool* p, const void* q, void* out, v
   if (e != cudaSuccess) return fail(PST_ERR_CUDA, "cudaGetSymbolAddress(scratch): %s", cudaGetErrorString(e));
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* b8 = static_cast<uint8_t*>(base);
-  AttnParams a = base_params(p);
+  AttnParams a = base_params(p, 0);
   a.q = q;
   a.out = out;
   a.sched = reinterpret_cast<int32_t*>(b8);  // must start at zero: cleared below
@@ -1272,24 +1296,17 @@ pst_status pst_decode_attention_host(pst_pool* p, const void* q_host, void* out_
   return PST_OK;
 }
 
-pst_status pst_prefill_attend(pst_pool* p, int64_t seq_id, const int32_t* tokens, int64_t W, const void* q,
-                              const void* k_new, const void* v_new, void* out, void* stream) {
-  pst_status st = need_device(p);
-  if (st != PST_OK) return st;
-  if (!tokens || W < 1 || !q || !k_new || !v_new || !out) return fail(PST_ERR_INVALID, "bad argument");
-  if (misaligned16(q) || misaligned16(out)) return fail(PST_ERR_INVALID, "q and out must be 16-byte aligned");
-  auto it = p->seqs.find(seq_id);
-  if (it == p->seqs.end()) return fail(PST_ERR_NOT_FOUND, "unknown sequence %lld", (long long)seq_id);
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  Seq& sq = it->second;
-  const int64_t p0 = sq.length;
+// Append a block of W tokens to sequence seq_id (sq): first the free rows of
+// its leaf (a partial leaf belongs to one sequence), then new private chunks.
+// *out_ops gets one scatter op per chunk touched, source rows 0 .. W-1.  Checks
+// the capacity before changing anything.
+static pst_status append_block(pst_pool* p, int64_t seq_id, Seq& sq, const int32_t* tokens, int64_t W,
+                               std::vector<ScatterOp>* out_ops) {
   const int32_t leaf = sq.path.back();
   const int64_t room = p->C - p->nodes[leaf].n_tokens;
   const int64_t need = ceil_div(std::max<int64_t>(0, W - room), p->C);
   if (need > static_cast<int64_t>(p->free_chunks.size())) return fail(PST_ERR_OOM, "pool exhausted on prefill");
-  if (p0 + W > INT32_MAX / 2) return fail(PST_ERR_INVALID, "sequence too long");
-
-  // append the block's tokens (never shared with other sequences)
+  if (sq.length + W > INT32_MAX / 2) return fail(PST_ERR_INVALID, "sequence too long");
   std::vector<ScatterOp> ops;
   int64_t pos = 0;
   if (room > 0) {
@@ -1314,9 +1331,16 @@ pst_status pst_prefill_attend(pst_pool* p, int64_t seq_id, const int32_t* tokens
   }
   sq.length += W;
   if (need > 0) mark_structural(p);
-  st = run_scatter(p, ops, k_new, v_new, s, false);
-  if (st != PST_OK) return st;
+  *out_ops = std::move(ops);
+  return PST_OK;
+}
 
+// Causal attention of the W query rows at positions [p0, p0 + W) of sequence
+// sq over its keys [0, p0 + r] in layer `layer` (Chunked Prefill, sections
+// 1-2), normalised rows into out.
+static pst_status prefill_attention(pst_pool* p, int32_t layer, Seq& sq, int64_t p0, int64_t W, const void* q,
+                                    void* out, cudaStream_t s) {
+  pst_status st = PST_OK;
   // work: the sequence's chunk list, then one item per (KV head, row tile)
   std::vector<int32_t> tab;
   for (int32_t id : sq.path) tab.push_back(p->nodes[id].chunk);
@@ -1358,7 +1382,7 @@ pst_status pst_prefill_attend(pst_pool* p, int64_t seq_id, const int32_t* tokens
   st = upload(p, &p->d_pre, &p->pre_cap, tab, s);
   if (st != PST_OK) return st;
 
-  AttnParams a = base_params(p);
+  AttnParams a = base_params(p, layer);
   a.q = q;
   a.out = out;
   a.final_mode = 1;
@@ -1380,6 +1404,49 @@ pst_status pst_prefill_attend(pst_pool* p, int64_t seq_id, const int32_t* tokens
   return PST_OK;
 }
 
+
+pst_status pst_prefill_attend(pst_pool* p, int64_t seq_id, const int32_t* tokens, int64_t W, const void* q,
+                              const void* k_new, const void* v_new, void* out, void* stream) {
+  pst_status st = need_device(p);
+  if (st != PST_OK) return st;
+  if (!tokens || W < 1 || !q || !k_new || !v_new || !out) return fail(PST_ERR_INVALID, "bad argument");
+  if (misaligned16(q) || misaligned16(out)) return fail(PST_ERR_INVALID, "q and out must be 16-byte aligned");
+  auto it = p->seqs.find(seq_id);
+  if (it == p->seqs.end()) return fail(PST_ERR_NOT_FOUND, "unknown sequence %lld", (long long)seq_id);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  Seq& sq = it->second;
+  const int64_t p0 = sq.length;
+  std::vector<ScatterOp> ops;
+  st = append_block(p, seq_id, sq, tokens, W, &ops);
+  if (st != PST_OK) return st;
+  st = scatter_layers(p, ops, k_new, v_new, W, s);
+  if (st != PST_OK) return st;
+  return prefill_attention(p, 0, sq, p0, W, q, out, s);
+}
+
+pst_status pst_extend(pst_pool* p, int64_t seq_id, const int32_t* tokens, int64_t W) {
+  if (!p || !tokens || W < 1) return fail(PST_ERR_INVALID, "bad argument");
+  auto it = p->seqs.find(seq_id);
+  if (it == p->seqs.end()) return fail(PST_ERR_NOT_FOUND, "unknown sequence %lld", (long long)seq_id);
+  std::vector<ScatterOp> ops;
+  return append_block(p, seq_id, it->second, tokens, W, &ops);
+}
+
+pst_status pst_prefill_attend_layer(pst_pool* p, int32_t layer, int64_t seq_id, int64_t p0, int64_t W, const void* q,
+                                    void* out, void* stream) {
+  pst_status st = need_device(p);
+  if (st != PST_OK) return st;
+  if (layer < 0 || layer >= p->n_layers) return fail(PST_ERR_INVALID, "layer %d outside [0, %d)", layer, p->n_layers);
+  if (W < 1 || p0 < 0 || !q || !out) return fail(PST_ERR_INVALID, "bad argument");
+  if (misaligned16(q) || misaligned16(out)) return fail(PST_ERR_INVALID, "q and out must be 16-byte aligned");
+  auto it = p->seqs.find(seq_id);
+  if (it == p->seqs.end()) return fail(PST_ERR_NOT_FOUND, "unknown sequence %lld", (long long)seq_id);
+  if (p0 + W > it->second.length)
+    return fail(PST_ERR_INVALID, "rows [%lld, %lld) past the sequence's %lld tokens", (long long)p0,
+                (long long)(p0 + W), (long long)it->second.length);
+  return prefill_attention(p, layer, it->second, p0, W, q, out, static_cast<cudaStream_t>(stream));
+}
+
 pst_status pst_gather_kv(const pst_pool* p, int64_t seq_id, void* k_out, void* v_out, void* stream) {
   pst_status st = need_device(p);
   if (st != PST_OK) return st;
@@ -1393,7 +1460,59 @@ pst_status pst_gather_kv(const pst_pool* p, int64_t seq_id, void* k_out, void* v
     ops.push_back({n.chunk, pos, 0, n.n_tokens, 0});
     pos += n.n_tokens;
   }
-  return run_scatter(const_cast<pst_pool*>(p), ops, k_out, v_out, static_cast<cudaStream_t>(stream), true);
+  return scatter_layers(const_cast<pst_pool*>(p), ops, k_out, v_out, it->second.length, static_cast<cudaStream_t>(stream),
+                        true);
+}
+
+pst_status pst_write_kv(pst_pool* p, int32_t layer, int64_t seq_id, int64_t n, const void* k, const void* v,
+                        void* stream) {
+  pst_status st = need_device(p);
+  if (st != PST_OK) return st;
+  if (layer < 0 || layer >= p->n_layers) return fail(PST_ERR_INVALID, "layer %d outside [0, %d)", layer, p->n_layers);
+  if (!k || !v || n < 1) return fail(PST_ERR_INVALID, "bad argument");
+  auto it = p->seqs.find(seq_id);
+  if (it == p->seqs.end()) return fail(PST_ERR_NOT_FOUND, "unknown sequence %lld", (long long)seq_id);
+  const Seq& sq = it->second;
+  if (n > sq.length)
+    return fail(PST_ERR_INVALID, "%lld rows for a sequence of %lld tokens", (long long)n, (long long)sq.length);
+  // the last n rows: every node but the leaf is full, so node i holds
+  // positions [i C, i C + n_tokens); each op runs to its chunk's last row
+  // (the chunk's device length is set from it)
+  const int64_t pos0 = sq.length - n;
+  std::vector<ScatterOp> ops;
+  for (int64_t i = pos0 / p->C; i < static_cast<int64_t>(sq.path.size()); ++i) {
+    const Node& nd = p->nodes[sq.path[i]];
+    if (nd.refs > 1)
+      return fail(PST_ERR_STATE,
+                  "chunk %lld of the sequence is shared by %d sequences; shared rows are written once, by the "
+                  "insert that created them",
+                  (long long)i, nd.refs);
+    const int32_t r0 = static_cast<int32_t>(std::max<int64_t>(pos0, i * p->C) - i * p->C);
+    // a chunk written from its first row also clears the rest of it, as on insert
+    ops.push_back({nd.chunk, static_cast<int32_t>(i * p->C + r0 - pos0), r0, nd.n_tokens, r0 == 0 ? 1 : 0});
+  }
+  return run_scatter(p, ops, k, v, static_cast<cudaStream_t>(stream), false, layer);
+}
+
+pst_status pst_write_kv_last(pst_pool* p, int32_t layer, int64_t n, const int64_t* seq_ids, const void* k,
+                             const void* v, void* stream) {
+  pst_status st = need_device(p);
+  if (st != PST_OK) return st;
+  if (layer < 0 || layer >= p->n_layers) return fail(PST_ERR_INVALID, "layer %d outside [0, %d)", layer, p->n_layers);
+  if (n < 0 || (n > 0 && (!seq_ids || !k || !v))) return fail(PST_ERR_INVALID, "bad argument");
+  std::vector<ScatterOp> ops(n);
+  for (int64_t x = 0; x < n; ++x) {
+    auto it = p->seqs.find(seq_ids[x]);
+    if (it == p->seqs.end()) return fail(PST_ERR_NOT_FOUND, "unknown sequence %lld", (long long)seq_ids[x]);
+    const Node& nd = p->nodes[it->second.path.back()];
+    if (nd.refs > 1)
+      return fail(PST_ERR_STATE, "the last token of sequence %lld lies in a chunk shared with %d sequences",
+                  (long long)seq_ids[x], nd.refs);
+    const int32_t r = nd.n_tokens - 1;
+    // as a decode append: a chunk's first row also clears the rest of it
+    ops[x] = {nd.chunk, static_cast<int32_t>(x), r, r + 1, r == 0 ? 1 : 0};
+  }
+  return run_scatter(p, ops, k, v, static_cast<cudaStream_t>(stream), false, layer);
 }
 
 pst_status pst_export_tables(const pst_pool* p, int32_t* shared_rows, int64_t shared_cap, int64_t* n_shared,

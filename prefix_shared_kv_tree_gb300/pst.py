@@ -29,7 +29,7 @@ MIN_SHARE_NEVER = 2**31 - 1
 class pst_config(Structure):
     _fields_ = [("n_q_heads", c_int32), ("n_kv_heads", c_int32), ("head_dim", c_int32), ("chunk_size", c_int32),
                 ("max_chunks", c_int64), ("dtype", c_int32), ("min_share", c_int32), ("max_seqs", c_int32),
-                ("flags", c_int32)]
+                ("flags", c_int32), ("n_layers", c_int32)]
 
 
 class pst_stats_t(Structure):
@@ -67,6 +67,11 @@ SIGNATURES = {
     "pst_decode_attention_graph": (c_int, [_P, _P, _P, _P]),
     "pst_prefill_attend": (c_int, [_P, c_int64, _P, c_int64, _P, _P, _P, _P, _P]),
     "pst_gather_kv": (c_int, [_P, c_int64, _P, _P, _P]),
+    "pst_extend": (c_int, [_P, c_int64, _P, c_int64]),
+    "pst_write_kv": (c_int, [_P, c_int32, c_int64, c_int64, _P, _P, _P]),
+    "pst_write_kv_last": (c_int, [_P, c_int32, c_int64, _P, _P, _P, _P]),
+    "pst_decode_attention_layer": (c_int, [_P, c_int32, _P, _P, _P]),
+    "pst_prefill_attend_layer": (c_int, [_P, c_int32, c_int64, c_int64, c_int64, _P, _P, _P]),
     "pst_export_tables": (c_int, [_P, _P, c_int64, _I64P, _P, c_int64, _I64P, _P, c_int64, _I64P]),
     "pst_stats": (c_int, [_P, POINTER(pst_stats_t)]),
     "pst_set_profiling": (c_int, [_P, c_int]),
@@ -127,9 +132,10 @@ class Pool:
     """A pst_pool handle.  device=-1 makes a host-only pool (tree and tables only)."""
 
     def __init__(self, n_q_heads: int, n_kv_heads: int, head_dim: int, chunk_size: int, max_chunks: int,
-                 dtype: str = "f16", min_share: int = 0, max_seqs: int = 0, flags: int = 0, device: int = 0):
+                 dtype: str = "f16", min_share: int = 0, max_seqs: int = 0, flags: int = 0, device: int = 0,
+                 n_layers: int = 0):
         self.cfg = pst_config(n_q_heads, n_kv_heads, head_dim, chunk_size, max_chunks, DTYPE_CODES[dtype],
-                              min_share, max_seqs, flags)
+                              min_share, max_seqs, flags, n_layers)
         self.dtype = dtype
         self.device = device
         h = c_void_p()
@@ -213,6 +219,28 @@ class Pool:
 
     def gather_kv(self, seq_id: int, k_out, v_out, stream=None) -> None:
         check(lib.pst_gather_kv(self.h, seq_id, _ptr(k_out), _ptr(v_out), _stream(stream)))
+
+    # ---- one layer at a time (pools with n_layers > 1)
+    def extend(self, seq_id: int, tokens) -> None:
+        """pst_extend: append a block of tokens to the tree only."""
+        t = _tokens(tokens)
+        check(lib.pst_extend(self.h, seq_id, _ptr(t), len(t)))
+
+    def write_kv(self, layer: int, seq_id: int, k, v, stream=None) -> None:
+        """pst_write_kv: layer `layer`'s K/V of the sequence's last k.shape[0] tokens."""
+        check(lib.pst_write_kv(self.h, layer, seq_id, k.shape[0], _ptr(k), _ptr(v), _stream(stream)))
+
+    def write_kv_last(self, layer: int, seq_ids, k, v, stream=None) -> None:
+        """pst_write_kv_last: layer `layer`'s K/V of each sequence's last token."""
+        ids = np.ascontiguousarray(np.asarray(seq_ids, dtype=np.int64))
+        check(lib.pst_write_kv_last(self.h, layer, len(ids), _ptr(ids), _ptr(k), _ptr(v), _stream(stream)))
+
+    def decode_attention_layer(self, layer: int, q, out, stream=None) -> None:
+        check(lib.pst_decode_attention_layer(self.h, layer, _ptr(q), _ptr(out), _stream(stream)))
+
+    def prefill_attend_layer(self, layer: int, seq_id: int, p0: int, q, out, stream=None) -> None:
+        check(lib.pst_prefill_attend_layer(self.h, layer, seq_id, p0, q.shape[0], _ptr(q), _ptr(out),
+                                           _stream(stream)))
 
     # ---- introspection
     def export_tables(self):

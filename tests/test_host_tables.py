@@ -159,7 +159,8 @@ def test_error_statuses(pst):
 
 
 @pytest.mark.parametrize("kw", [dict(n_q_heads=3, n_kv_heads=2), dict(head_dim=96), dict(chunk_size=48),
-                                dict(n_q_heads=32, n_kv_heads=2), dict(max_chunks=0), dict(dtype=7)])
+                                dict(n_q_heads=32, n_kv_heads=2), dict(max_chunks=0), dict(dtype=7),
+                                dict(n_layers=-1), dict(n_layers=1025)])
 def test_bad_configs_rejected(pst, kw):
     cfg = dict(n_q_heads=4, n_kv_heads=2, head_dim=64, chunk_size=32, max_chunks=16, dtype=0, min_share=0,
                max_seqs=0, flags=0)
@@ -186,3 +187,38 @@ def test_table_builds_are_lazy(pst):
     pool.append(a, 9)                   # 65th token opens a chunk: structural
     pool.batch_order()
     assert pool.stats()["rebuild_count"] == n0 + 1
+
+
+@pytest.mark.parametrize("c", [16, 32, 128])
+def test_extend_block_equals_token_appends(pst, c):
+    """pst_extend (a chunked-prefill block added to the tree only) leaves the
+    same tree and tables as appending its tokens one by one (Knowl 1: the
+    leaf fills first, then new chunks of the sequence's own)."""
+    rng = np.random.default_rng(300 + c)
+    pool = _pool(pst, c)
+    tree = PrefixTree(c)
+    base = list(rng.integers(0, 4, 2 * c + 3))
+    ids = []
+    for tail in (0, 5, c):
+        toks = base + list(rng.integers(0, 4, tail))
+        sid, m = pool.insert(toks)
+        assert (sid, m) == tree.insert(toks)
+        ids.append(sid)
+    for sid, w in zip(ids, (1, c - 3, 3 * c + 1)):
+        block = [int(x) for x in rng.integers(0, 4, w)]
+        pool.extend(sid, block)
+        for t in block:
+            tree.append(sid, t)
+        _same(pool, tree)
+    for sid in ids:
+        assert pool.seq_length(sid) == tree.lengths[sid]
+    with pytest.raises(pst.PstError) as e:
+        pool.extend(12345, [1])
+    assert e.value.status == pst.PST_ERR_NOT_FOUND
+    tight = pst.Pool(1, 1, 64, c, 4, "f16", 0, 0, device=-1)
+    sid, _ = tight.insert([1] * c)
+    before = (tight.export_tables(), tight.stats()["used_chunks"], tight.seq_length(sid))
+    with pytest.raises(pst.PstError) as e:
+        tight.extend(sid, [2] * (4 * c))  # needs 4 new chunks, 3 free
+    assert e.value.status == pst.PST_ERR_OOM
+    assert (tight.export_tables(), tight.stats()["used_chunks"], tight.seq_length(sid)) == before

@@ -1,0 +1,166 @@
+"""Multi-layer pools: the K/V of n_layers decoder layers under one prefix tree.
+
+The tree and the chunk tables depend on token ids only, so every layer shares
+them (ChunkAttention, Knowl 5: the context is built once per step, behind the
+layers' earlier kernels); layer l's attention reads layer l's K/V.  Checked
+against the fp64 oracle layer by layer: decode after an insert that writes all
+layers at once; a decode loop whose appends add each token to the tree first
+and then write its K/V layer by layer; a chunked prefill written and attended
+layer by layer (Chunked Prefill, sections 1-2); byte-exact read-back of all
+layers; and the refusals (rows in a shared chunk, a layer out of range).
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle import attention as A
+from prefix_shared_kv_tree_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"f16": 2e-3, "bf16": 2e-3, "f32": 1e-5}
+ULP_BITS = {"f16": 10, "bf16": 7, "f32": 23}
+N_LAYERS = 3
+
+
+@pytest.fixture(scope="module")
+def pst():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from prefix_shared_kv_tree_gb300 import build
+    build.build_library()
+    from prefix_shared_kv_tree_gb300 import pst as mod
+    return mod
+
+
+def _f64(t):
+    return t.detach().float().cpu().double().numpy()
+
+
+def _check(got, want, dtype, what):
+    """Parity bound: the dtype's tolerance plus half an output ulp at |oracle|."""
+    got = _f64(got)
+    mag = np.maximum(np.abs(want), 1e-30)
+    bound = TOL[dtype] + 0.5 * 2.0 ** (np.floor(np.log2(mag)) - ULP_BITS[dtype])
+    assert np.isfinite(got).all(), f"{what}: non-finite output"
+    err = np.abs(got - want)
+    assert (err <= bound).all(), f"{what}: max err {err.max():.3e}"
+
+
+# dtype, Hq, Hkv, c: tensor-core chunk-first at c = 64 and (two tiles per chunk)
+# c = 128; fp32 on the CUDA-core kernel for both phases
+CASES = [("bf16", 8, 2, 64), ("f16", 4, 4, 128), ("f32", 2, 1, 32)]
+
+
+@pytest.mark.parametrize("dtype,hq,hkv,c", CASES)
+def test_layers_decode_loop_and_prefill(pst, dtype, hq, hkv, c):
+    L = N_LAYERS
+    d = 64 if dtype == "f32" else 128
+    dt = W.DTYPES[dtype]
+    g = torch.Generator().manual_seed(40 + c)
+    pool = pst.Pool(hq, hkv, d, c, 512, dtype, 0, 0, 0, device=0, n_layers=L)
+
+    # a shared root of 3 full chunks + 10 tokens, four sequences with private tails
+    root_n = 3 * c + 10
+    root_t = torch.randint(0, 50, (root_n,), generator=g, dtype=torch.int32)
+    root_k = torch.randn(L, root_n, hkv, d, generator=g).to(dt)
+    root_v = torch.randn(L, root_n, hkv, d, generator=g).to(dt)
+    kv = {}  # sequence id -> its K, V on the CPU, [L][n][Hkv][d]
+    for s in range(4):
+        tail = c // 2 + 7 * s
+        t = torch.randint(0, 50, (tail,), generator=g, dtype=torch.int32)
+        t[0] = 1000 + s
+        k = torch.cat([root_k, torch.randn(L, tail, hkv, d, generator=g).to(dt)], dim=1)
+        v = torch.cat([root_v, torch.randn(L, tail, hkv, d, generator=g).to(dt)], dim=1)
+        sid, m = pool.insert(torch.cat([root_t, t]), k.cuda(), v.cuda())
+        assert m == (0 if s == 0 else 3 * c)
+        kv[sid] = (k, v)
+
+    def check_decode(what):
+        order = pool.batch_order()
+        for layer in range(L):
+            q = torch.randn(len(order), hq, d, generator=g).to(dt).cuda()
+            out = torch.empty(len(order), hq, d, dtype=dt, device="cuda")
+            pool.decode_attention_layer(layer, q, out)
+            if layer == 0:  # the layer-free entry point reads layer 0
+                out0 = torch.empty_like(out)
+                pool.decode_attention(q, out0)
+                torch.cuda.synchronize()
+                assert torch.equal(out0, out), what
+            torch.cuda.synchronize()
+            want = A.decode_attention([(_f64(kv[s][0][layer]), _f64(kv[s][1][layer])) for s in order], _f64(q))
+            _check(out, want, dtype, f"{what}, layer {layer}")
+        assert pool.check_device() == 0
+
+    check_decode("after insert")
+
+    # decode loop: each step adds the token to the tree (no K/V), then every
+    # layer writes its row of the token and attends; every sequence crosses a
+    # chunk boundary on the way
+    for step in range(c + 3):
+        ids = sorted(kv)
+        pool.append_batch(ids, [7] * len(ids))
+        kn = torch.randn(L, len(ids), hkv, d, generator=g).to(dt)
+        vn = torch.randn(L, len(ids), hkv, d, generator=g).to(dt)
+        for layer in range(L):
+            pool.write_kv_last(layer, ids, kn[layer].cuda(), vn[layer].cuda())
+        for i, sid in enumerate(ids):
+            kv[sid] = (torch.cat([kv[sid][0], kn[:, i:i + 1]], dim=1), torch.cat([kv[sid][1], vn[:, i:i + 1]], dim=1))
+        if step == 9:
+            victim = ids[1]
+            pool.remove(victim)
+            del kv[victim]
+        if step % 4 == 0 or step == c + 2:
+            check_decode(f"decode step {step}")
+
+    # read-back of every layer, byte-exact
+    sid0 = sorted(kv)[0]
+    n0 = pool.seq_length(sid0)
+    ko = torch.empty(L, n0, hkv, d, dtype=dt, device="cuda")
+    vo = torch.empty_like(ko)
+    pool.gather_kv(sid0, ko, vo)
+    torch.cuda.synchronize()
+    assert torch.equal(ko.cpu(), kv[sid0][0]) and torch.equal(vo.cpu(), kv[sid0][1])
+
+    # chunked prefill layer by layer: a new sequence matches two root chunks
+    # (no K/V to write), then each block joins the tree and, per layer, gets
+    # its K/V written and its rows attended
+    sid, m = pool.insert(root_t[:2 * c])
+    assert m == 2 * c
+    pk, pv = root_k[:, :2 * c], root_v[:, :2 * c]
+    pos = 2 * c
+    for w in (c + 5, 1, 2 * c - 3):
+        toks = torch.randint(0, 50, (w,), generator=g, dtype=torch.int32)
+        kb = torch.randn(L, w, hkv, d, generator=g).to(dt)
+        vb = torch.randn(L, w, hkv, d, generator=g).to(dt)
+        pool.extend(sid, toks)
+        assert pool.seq_length(sid) == pos + w
+        for layer in range(L):
+            pool.write_kv(layer, sid, kb[layer].cuda(), vb[layer].cuda())
+            q = torch.randn(w, hq, d, generator=g).to(dt)
+            out = torch.empty(w, hq, d, dtype=dt, device="cuda")
+            pool.prefill_attend_layer(layer, sid, pos, q.cuda(), out)
+            torch.cuda.synchronize()
+            want = A.prefill_attention(_f64(torch.cat([pk[layer], kb[layer]])), _f64(torch.cat([pv[layer], vb[layer]])),
+                                       _f64(q), pos)
+            _check(out, want, dtype, f"prefill block at {pos}, layer {layer}")
+        pk, pv = torch.cat([pk, kb], dim=1), torch.cat([pv, vb], dim=1)
+        pos += w
+    assert pool.check_device() == 0
+
+    # refusals: rows of shared chunks, layers out of range
+    n = pool.seq_length(sid)
+    junk = torch.zeros(n, hkv, d, dtype=dt, device="cuda")
+    with pytest.raises(pst.PstError) as e:
+        pool.write_kv(0, sid, junk, junk)  # its first two chunks are the shared root's
+    assert e.value.status == pst.PST_ERR_STATE
+    q = torch.zeros(len(pool.batch_order()), hq, d, dtype=dt, device="cuda")
+    for bad in (-1, L):
+        with pytest.raises(pst.PstError) as e:
+            pool.decode_attention_layer(bad, q, torch.empty_like(q))
+        assert e.value.status == pst.PST_ERR_INVALID
+        with pytest.raises(pst.PstError) as e:
+            pool.write_kv_last(bad, [sid], junk[:1], junk[:1])
+        assert e.value.status == pst.PST_ERR_INVALID
+    torch.cuda.synchronize()
+    assert pool.check_device() == 0
