@@ -252,6 +252,12 @@ pst_status pst_write_kv_last(pst_pool* pool, int32_t layer, int64_t n, const int
 pst_status pst_decode_attention_layer(pst_pool* pool, int32_t layer, const void* q, void* out,
                                       void* stream);
 
+/* pst_decode_attention_graph on layer `layer`: each layer keeps its own
+ * captured step (a model's decode loop calls every layer once per step, each
+ * with its own q / out buffers), captured again after a structural change. */
+pst_status pst_decode_attention_graph_layer(pst_pool* pool, int32_t layer, const void* q, void* out,
+                                            void* stream);
+
 /* Causal attention of the W query rows at positions [p0, p0 + W) of sequence
  * seq_id over its keys [0, p0 + t] in layer `layer` (Chunked Prefill, sections
  * 1-2); appends nothing.  p0 + W <= the sequence's length; q, out: device

@@ -169,14 +169,18 @@ struct pst_pool {
   cudaEvent_t pev[6] = {};
   bool pran[3] = {false, false, false};
   int32_t last_launches = 0;
-  // pst_decode_attention_graph: the captured step, valid for one table
-  // version and one (q, out) pair
+  // pst_decode_attention_graph(_layer): the capture stream, and one captured
+  // decode step per layer, replayed while the table version and the q / out
+  // pointers it was captured with still hold
   cudaStream_t cap_stream = nullptr;
-  cudaGraphExec_t g_exec = nullptr;
-  int64_t g_version = -1;
-  const void* g_q = nullptr;
-  void* g_out = nullptr;
-  int32_t g_launches = 0;
+  struct GraphCache {
+    cudaGraphExec_t exec = nullptr;
+    int64_t version = -1;
+    const void* q = nullptr;
+    void* out = nullptr;
+    int32_t launches = 0;
+  };
+  std::vector<GraphCache> graphs;
   int64_t graph_captures = 0;
 };
 
@@ -860,7 +864,8 @@ pst_status pst_pool_free(pst_pool* p) {
     cudaFree(p->d_out);
     if (p->h_stage) cudaFreeHost(p->h_stage);
     if (p->aux) cudaStreamDestroy(p->aux);
-    if (p->g_exec) cudaGraphExecDestroy(p->g_exec);
+    for (auto& gc : p->graphs)
+      if (gc.exec) cudaGraphExecDestroy(gc.exec);
     if (p->cap_stream) cudaStreamDestroy(p->cap_stream);
     if (p->ev_fork) cudaEventDestroy(p->ev_fork);
     if (p->ev_join) cudaEventDestroy(p->ev_join);
@@ -1176,12 +1181,9 @@ pst_status pst_decode_attention_layer(pst_pool* p, int32_t layer, const void* q,
   return decode_impl(p, layer, q, out, static_cast<cudaStream_t>(stream));
 }
 
-pst_status pst_decode_attention_graph(pst_pool* p, const void* q, void* out, void* stream) {
-  pst_status st = need_device(p);
-  if (st != PST_OK) return st;
-  const cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (p->profiling) return decode_impl(p, 0, q, out, s);  // per-phase events are not captured
-  st = ensure_tables(p);
+static pst_status decode_graph_impl(pst_pool* p, int32_t layer, const void* q, void* out, cudaStream_t s) {
+  if (p->profiling) return decode_impl(p, layer, q, out, s);  // per-phase events are not captured
+  pst_status st = ensure_tables(p);
   if (st != PST_OK) return st;
   p->pran[0] = p->pran[1] = p->pran[2] = false;
   const int32_t B = static_cast<int32_t>(p->batch.size());
@@ -1194,14 +1196,16 @@ pst_status pst_decode_attention_graph(pst_pool* p, const void* q, void* out, voi
   st = sync_device_tables(p, s);  // on the caller's stream, before the graph
   if (st != PST_OK) return st;
   CUDA_TRY(clear_sched(p, s));  // the graph holds no counter reset: the previous step's merge cleared it
-  if (!p->g_exec || p->g_version != p->version || p->g_q != q || p->g_out != out) {
+  if (p->graphs.size() < static_cast<size_t>(p->n_layers)) p->graphs.resize(p->n_layers);
+  auto& gc = p->graphs[layer];
+  if (!gc.exec || gc.version != p->version || gc.q != q || gc.out != out) {
     if (!p->cap_stream) CUDA_TRY(cudaStreamCreateWithFlags(&p->cap_stream, cudaStreamNonBlocking));
-    if (p->g_exec) {
-      cudaGraphExecDestroy(p->g_exec);
-      p->g_exec = nullptr;
+    if (gc.exec) {
+      cudaGraphExecDestroy(gc.exec);
+      gc.exec = nullptr;
     }
     CUDA_TRY(cudaStreamBeginCapture(p->cap_stream, cudaStreamCaptureModeRelaxed));
-    const pst_status ls = launch_step(p, 0, q, out, p->cap_stream);
+    const pst_status ls = launch_step(p, layer, q, out, p->cap_stream);
     cudaGraph_t graph = nullptr;
     const cudaError_t ce = cudaStreamEndCapture(p->cap_stream, &graph);
     if (ls != PST_OK) {
@@ -1209,21 +1213,34 @@ pst_status pst_decode_attention_graph(pst_pool* p, const void* q, void* out, voi
       return ls;
     }
     if (ce != cudaSuccess) return fail(PST_ERR_CUDA, "decode graph capture: %s", cudaGetErrorString(ce));
-    const cudaError_t ie = cudaGraphInstantiate(&p->g_exec, graph, 0);
+    const cudaError_t ie = cudaGraphInstantiate(&gc.exec, graph, 0);
     cudaGraphDestroy(graph);
     if (ie != cudaSuccess) {
-      p->g_exec = nullptr;
+      gc.exec = nullptr;
       return fail(PST_ERR_CUDA, "decode graph instantiate: %s", cudaGetErrorString(ie));
     }
-    p->g_version = p->version;
-    p->g_q = q;
-    p->g_out = out;
-    p->g_launches = p->last_launches;
+    gc.version = p->version;
+    gc.q = q;
+    gc.out = out;
+    gc.launches = p->last_launches;
     ++p->graph_captures;
   }
-  CUDA_TRY(cudaGraphLaunch(p->g_exec, s));
-  p->last_launches = p->g_launches;
+  CUDA_TRY(cudaGraphLaunch(gc.exec, s));
+  p->last_launches = gc.launches;
   return PST_OK;
+}
+
+pst_status pst_decode_attention_graph(pst_pool* p, const void* q, void* out, void* stream) {
+  pst_status st = need_device(p);
+  if (st != PST_OK) return st;
+  return decode_graph_impl(p, 0, q, out, static_cast<cudaStream_t>(stream));
+}
+
+pst_status pst_decode_attention_graph_layer(pst_pool* p, int32_t layer, const void* q, void* out, void* stream) {
+  pst_status st = need_device(p);
+  if (st != PST_OK) return st;
+  if (layer < 0 || layer >= p->n_layers) return fail(PST_ERR_INVALID, "layer %d outside [0, %d)", layer, p->n_layers);
+  return decode_graph_impl(p, layer, q, out, static_cast<cudaStream_t>(stream));
 }
 
 // Decode attention without any allocation: the partial rows and the work

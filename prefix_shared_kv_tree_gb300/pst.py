@@ -71,6 +71,7 @@ SIGNATURES = {
     "pst_write_kv": (c_int, [_P, c_int32, c_int64, c_int64, _P, _P, _P]),
     "pst_write_kv_last": (c_int, [_P, c_int32, c_int64, _P, _P, _P, _P]),
     "pst_decode_attention_layer": (c_int, [_P, c_int32, _P, _P, _P]),
+    "pst_decode_attention_graph_layer": (c_int, [_P, c_int32, _P, _P, _P]),
     "pst_prefill_attend_layer": (c_int, [_P, c_int32, c_int64, c_int64, c_int64, _P, _P, _P]),
     "pst_export_tables": (c_int, [_P, _P, c_int64, _I64P, _P, c_int64, _I64P, _P, c_int64, _I64P]),
     "pst_stats": (c_int, [_P, POINTER(pst_stats_t)]),
@@ -237,6 +238,10 @@ class Pool:
 
     def decode_attention_layer(self, layer: int, q, out, stream=None) -> None:
         check(lib.pst_decode_attention_layer(self.h, layer, _ptr(q), _ptr(out), _stream(stream)))
+
+    def decode_attention_graph_layer(self, layer: int, q, out, stream=None) -> None:
+        """pst_decode_attention_graph_layer: one captured step per layer."""
+        check(lib.pst_decode_attention_graph_layer(self.h, layer, _ptr(q), _ptr(out), _stream(stream)))
 
     def prefill_attend_layer(self, layer: int, seq_id: int, p0: int, q, out, stream=None) -> None:
         check(lib.pst_prefill_attend_layer(self.h, layer, seq_id, p0, q.shape[0], _ptr(q), _ptr(out),

@@ -5,7 +5,8 @@ them (ChunkAttention, Knowl 5: the context is built once per step, behind the
 layers' earlier kernels); layer l's attention reads layer l's K/V.  Checked
 against the fp64 oracle layer by layer: decode after an insert that writes all
 layers at once; a decode loop whose appends add each token to the tree first
-and then write its K/V layer by layer; a chunked prefill written and attended
+and then write its K/V layer by layer, each layer replaying its own captured
+graph (checked against the regular entry point); a chunked prefill written and attended
 layer by layer (Chunked Prefill, sections 1-2); byte-exact read-back of all
 layers; and the refusals (rows in a shared chunk, a layer out of range).
 """
@@ -95,8 +96,16 @@ def test_layers_decode_loop_and_prefill(pst, dtype, hq, hkv, c):
     check_decode("after insert")
 
     # decode loop: each step adds the token to the tree (no K/V), then every
-    # layer writes its row of the token and attends; every sequence crosses a
-    # chunk boundary on the way
+    # layer writes its row of the token and attends, from its own captured
+    # graph with its own q / out buffers; every sequence crosses a chunk
+    # boundary on the way
+    def buffers():
+        b = len(pool.batch_order())
+        qs = [torch.empty(b, hq, d, dtype=dt, device="cuda") for _ in range(L)]
+        return qs, [torch.empty_like(x) for x in qs], torch.empty_like(qs[0])
+
+    qg, og, ref = buffers()
+    seen = set()
     for step in range(c + 3):
         ids = sorted(kv)
         pool.append_batch(ids, [7] * len(ids))
@@ -106,12 +115,26 @@ def test_layers_decode_loop_and_prefill(pst, dtype, hq, hkv, c):
             pool.write_kv_last(layer, ids, kn[layer].cuda(), vn[layer].cuda())
         for i, sid in enumerate(ids):
             kv[sid] = (torch.cat([kv[sid][0], kn[:, i:i + 1]], dim=1), torch.cat([kv[sid][1], vn[:, i:i + 1]], dim=1))
-        if step == 9:
+        if step == 9:  # a departure: the batch shrinks, so new q / out buffers
             victim = ids[1]
             pool.remove(victim)
             del kv[victim]
+            qg, og, ref = buffers()
+        for layer in range(L):
+            qg[layer].copy_(torch.randn(qg[layer].shape, generator=g).to(dt))
+            og[layer].fill_(float("nan"))
+            pool.decode_attention_graph_layer(layer, qg[layer], og[layer])
+            seen.add((pool.stats()["table_version"], layer, qg[layer].data_ptr(), og[layer].data_ptr()))
+            pool.decode_attention_layer(layer, qg[layer], ref)
+            torch.cuda.synchronize()
+            assert torch.isfinite(og[layer].float()).all(), (step, layer)
+            err = (og[layer].float() - ref.float()).abs().max().item()
+            assert err <= TOL[dtype], (step, layer, err)
         if step % 4 == 0 or step == c + 2:
             check_decode(f"decode step {step}")
+    st = pool.stats()
+    assert st["graph_captures"] == len(seen), (st["graph_captures"], len(seen))
+    assert st["graph_captures"] < L * (c + 3) // 2  # most steps replayed their layer's graph
 
     # read-back of every layer, byte-exact
     sid0 = sorted(kv)[0]
