@@ -243,7 +243,7 @@ pst_status pst_write_kv(pst_pool* pool, int32_t layer, int64_t seq_id, int64_t n
 /* Write layer `layer`'s K/V of the last token of each of n sequences (host
  * seq_ids int64[n]; device k, v [n][Hkv][d]): the per-layer half of a decode
  * append made with k = v = NULL.  PST_ERR_STATE if a last token lies in a
- * shared chunk.  One kernel launch. */
+ * shared chunk, PST_ERR_INVALID on a repeated id.  One kernel launch. */
 pst_status pst_write_kv_last(pst_pool* pool, int32_t layer, int64_t n, const int64_t* seq_ids,
                              const void* k, const void* v, void* stream);
 

@@ -1517,6 +1517,10 @@ pst_status pst_write_kv_last(pst_pool* p, int32_t layer, int64_t n, const int64_
   if (st != PST_OK) return st;
   if (layer < 0 || layer >= p->n_layers) return fail(PST_ERR_INVALID, "layer %d outside [0, %d)", layer, p->n_layers);
   if (n < 0 || (n > 0 && (!seq_ids || !k || !v))) return fail(PST_ERR_INVALID, "bad argument");
+  std::vector<int64_t> sorted(seq_ids, seq_ids + n);
+  std::sort(sorted.begin(), sorted.end());
+  if (std::adjacent_find(sorted.begin(), sorted.end()) != sorted.end())
+    return fail(PST_ERR_INVALID, "duplicate sequence id in batch write");  // one launch: rows must not collide
   std::vector<ScatterOp> ops(n);
   for (int64_t x = 0; x < n; ++x) {
     auto it = p->seqs.find(seq_ids[x]);

@@ -185,5 +185,8 @@ def test_layers_decode_loop_and_prefill(pst, dtype, hq, hkv, c):
         with pytest.raises(pst.PstError) as e:
             pool.write_kv_last(bad, [sid], junk[:1], junk[:1])
         assert e.value.status == pst.PST_ERR_INVALID
+    with pytest.raises(pst.PstError) as e:  # one launch: two rows for one sequence would collide
+        pool.write_kv_last(0, [sid, sid], junk[:2], junk[:2])
+    assert e.value.status == pst.PST_ERR_INVALID
     torch.cuda.synchronize()
     assert pool.check_device() == 0

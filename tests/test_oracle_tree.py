@@ -87,7 +87,7 @@ def test_capacity_multiplier_limit():
         prev = ratio
 
 
-@pytest.mark.parametrize("c", [1, 16, 32, 64])
+@pytest.mark.parametrize("c", [1, 16, 32, 64, 128])
 def test_fragmentation_bound(c):
     for n in range(1, 400):
         w = T.wasted_slots(n, c)
