@@ -299,10 +299,25 @@ pst_status pst_phase_times(pst_pool* pool, float* ms3);
 /* Kernel launches issued by the last pst_decode_attention call. */
 pst_status pst_last_launch_count(const pst_pool* pool, int32_t* n);
 
+/* Bits of the device error word. */
+enum {
+  PST_DEVICE_WAIT_TIMEOUT = 1, /* a bounded wait ran out; the kernel stopped early */
+  PST_DEVICE_BAD_INDEX = 2     /* an index check failed; the access was skipped */
+};
+
 /* Read and clear the device error word written by kernels whose bounded
  * waits timed out or whose index checks failed (synchronises the device).
- * *code == 0 means no error. */
+ * *code == 0 means no error, else an OR of PST_DEVICE_* bits. */
 pst_status pst_check_device(pst_pool* pool, int32_t* code);
+
+/* Self-test of the kernels' bounded waits (failure detection without a GPU
+ * fault): on `device`, one warp waits through the attention kernels' own
+ * mbarrier-wait routine on a barrier that nothing arrives on.  The wait gives
+ * up after its time limit (2 s), so the call takes about that long.  On return
+ * *err_code holds the device error word the kernel left (PST_DEVICE_WAIT_TIMEOUT
+ * is expected) and *lanes_gave_up the lanes whose wait returned unfinished
+ * (32 expected); the context stays usable. */
+pst_status pst_selftest_bounded_wait(int device, int32_t* err_code, int32_t* lanes_gave_up);
 
 /* Thread-local message of the last failing call on this thread ("" if none). */
 const char* pst_last_error(void);

@@ -26,7 +26,7 @@ NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-
 CXX_FLAGS = ["-O2", "-std=c++17", "-fPIC", "-Wall", "-I", INCLUDE, "-I", CSRC, "-I", os.path.join(CUDA_HOME, "include")]
 
 CU_SOURCES = ["kernels_misc.cu", "simt_f16.cu", "simt_bf16.cu", "simt_f32.cu", "simt_f16_small.cu", "simt_bf16_small.cu",
-              "simt_f32_small.cu", "kernels_tc.cu", "static_scratch.cu"]
+              "simt_f32_small.cu", "kernels_tc.cu", "static_scratch.cu", "selftest.cu"]
 CPP_SOURCES = ["pool.cpp"]
 
 

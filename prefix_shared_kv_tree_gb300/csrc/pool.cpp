@@ -34,6 +34,12 @@
 
 using namespace pst;
 
+namespace pst {
+// selftest.cu: one warp waits on an mbarrier nothing arrives on, through the
+// kernels' bounded-wait helper; returns the error word and how many lanes gave up.
+cudaError_t run_bounded_wait_selftest(int device, int32_t* err_word, int32_t* lanes_gave_up);
+}  // namespace pst
+
 namespace {
 
 thread_local std::string g_last_error;
@@ -1596,6 +1602,13 @@ pst_status pst_phase_times(pst_pool* p, float* ms3) {
     CUDA_TRY(cudaEventSynchronize(p->pev[2 * i + 1]));
     CUDA_TRY(cudaEventElapsedTime(&ms3[i], p->pev[2 * i], p->pev[2 * i + 1]));
   }
+  return PST_OK;
+}
+
+pst_status pst_selftest_bounded_wait(int device, int32_t* err_code, int32_t* lanes_gave_up) {
+  if (device < 0 || !err_code || !lanes_gave_up) return fail(PST_ERR_INVALID, "bad argument");
+  const cudaError_t e = run_bounded_wait_selftest(device, err_code, lanes_gave_up);
+  if (e != cudaSuccess) return fail(PST_ERR_CUDA, "bounded-wait self-test: %s", cudaGetErrorString(e));
   return PST_OK;
 }
 

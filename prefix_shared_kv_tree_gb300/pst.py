@@ -78,6 +78,7 @@ SIGNATURES = {
     "pst_set_profiling": (c_int, [_P, c_int]),
     "pst_phase_times": (c_int, [_P, POINTER(c_float)]),
     "pst_last_launch_count": (c_int, [_P, _I32P]),
+    "pst_selftest_bounded_wait": (c_int, [c_int, _I32P, _I32P]),
     "pst_check_device": (c_int, [_P, _I32P]),
     "pst_last_error": (c_char_p, []),
     "pst_version": (c_char_p, []),
@@ -96,6 +97,17 @@ def _load() -> ctypes.CDLL:
 
 
 lib = _load()
+
+
+PST_DEVICE_WAIT_TIMEOUT = 1
+PST_DEVICE_BAD_INDEX = 2
+
+
+def selftest_bounded_wait(device: int = 0):
+    """pst_selftest_bounded_wait: (device error word, lanes whose wait gave up)."""
+    code, lanes = c_int32(), c_int32()
+    check(lib.pst_selftest_bounded_wait(device, byref(code), byref(lanes)))
+    return code.value, lanes.value
 
 
 def check(status: int) -> None:
