@@ -222,3 +222,29 @@ def test_extend_block_equals_token_appends(pst, c):
         tight.extend(sid, [2] * (4 * c))  # needs 4 new chunks, 3 free
     assert e.value.status == pst.PST_ERR_OOM
     assert (tight.export_tables(), tight.stats()["used_chunks"], tight.seq_length(sid)) == before
+
+
+def test_layered_calls_on_a_host_only_pool(pst):
+    """A host-only pool runs the tree for any number of layers (tree-only
+    calls work), refuses every call that needs device K/V with
+    PST_ERR_STATE, and the bounded-wait self-test refuses a negative device."""
+    pool = pst.Pool(4, 2, 64, 32, 64, "f16", 0, 0, device=-1, n_layers=3)
+    h = pool.h
+    tree = PrefixTree(32)
+    toks = list(range(70))
+    assert pool.insert(toks) == tree.insert(toks)
+    pool.extend(0, [5] * 40)
+    for t in [5] * 40:
+        tree.append(0, t)
+    _same(pool, tree)
+    ids = np.zeros(1, dtype=np.int64)
+    for st in (pst.lib.pst_write_kv(h, 0, 0, 1, None, None, None),
+               pst.lib.pst_write_kv_last(h, 0, 1, ids.ctypes.data, None, None, None),
+               pst.lib.pst_decode_attention_layer(h, 0, None, None, None),
+               pst.lib.pst_decode_attention_graph_layer(h, 0, None, None, None),
+               pst.lib.pst_prefill_attend_layer(h, 0, 0, 0, 1, None, None, None)):
+        assert st == pst.PST_ERR_STATE
+    with pytest.raises(pst.PstError) as e:
+        pst.selftest_bounded_wait(-1)
+    assert e.value.status == pst.PST_ERR_INVALID
+    pool.close()
