@@ -25,6 +25,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <functional>
 #include <string>
 #include <unordered_map>
 #include <vector>
@@ -89,6 +90,29 @@ struct Seq {
 
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+struct Stream {  // a run of tiles for the CUDA-core kernel: chunks of one list, one KV head, one group
+  int32_t chunk_off, n, kv, group;
+};
+
+// Partial results, one entry per (batch row, KV head) pair and item that
+// covers it.  The rows of one pair end up contiguous in entry order (slot e of
+// the pair holds heads kv*g .. kv*g+g-1 at rows e*g ..), so the merge reads
+// one contiguous block per pair.  An entry points back at its producer: a
+// tensor-core row-index slot (rows of head 0 at tc_rows[pos]) or a CUDA-core
+// item (x).
+struct Entry {
+  int32_t key;  // u * Hkv + kv
+  int32_t pos;  // >= 0: index into tc_rows of head 0; < 0: -1 - CUDA-core item index
+};
+
+// The table builder's large work arrays, kept by the pool between builds so a
+// rebuild reuses their memory instead of allocating (and first touching) it.
+struct BuildScratch {
+  std::vector<int32_t> chunks, tc_items, simt_items, tc_rows, sorted, moff, fill;
+  std::vector<Entry> ents;
+  std::vector<Stream> streams, units, ordered;
+};
+
 }  // namespace
 
 struct pst_pool {
@@ -145,6 +169,9 @@ struct pst_pool {
   std::vector<int32_t> canon_shared;   // 4 per row
   std::vector<int32_t> canon_entries;  // 2 per entry
   std::vector<int64_t> canon_offsets;  // B + 1
+  BuildScratch scratch;                // the table builder's work arrays, reused between builds
+  bool canon_valid = false;            // built on demand by pst_export_tables from the last rebuild's
+  std::vector<int32_t> tab_ni, tab_nj, tab_preorder;  // batch ranges and node preorder
 
   // ---- device
   uint8_t* d_pool = nullptr;
@@ -299,9 +326,6 @@ pst_status scatter_layers(pst_pool* p, const std::vector<ScatterOp>& ops, const 
 }
 
 // ================================================================ tables
-struct Stream {  // a run of tiles for the CUDA-core kernel: chunks of one list, one KV head, one group
-  int32_t chunk_off, n, kv, group;
-};
 
 pst_status upload(pst_pool* p, int32_t** dbuf, size_t* dcap, const std::vector<int32_t>& src, cudaStream_t s) {
   const size_t n = src.size();
@@ -390,24 +414,9 @@ pst_status rebuild(pst_pool* p) {
   const int32_t B = static_cast<int32_t>(p->batch.size());
   auto shared = [&](int32_t id) { return nj[id] - ni[id] >= min_share; };
 
-  // canonical tables
-  p->canon_shared.clear();
-  p->canon_entries.clear();
-  p->canon_offsets.assign(1, 0);
+  // canonical tables: only counted here (pst_export_tables builds them)
   int64_t n_shared = 0;
-  for (int32_t id : preorder) {
-    if (!shared(id)) continue;
-    const Node& n = p->nodes[id];
-    p->canon_shared.insert(p->canon_shared.end(), {n.depth, ni[id], nj[id], n.n_tokens});
-    ++n_shared;
-  }
-  for (int64_t sid : p->batch) {
-    for (int32_t id : p->seqs[sid].path) {
-      p->canon_entries.push_back(p->nodes[id].depth);
-      p->canon_entries.push_back(shared(id) ? 1 : 0);
-    }
-    p->canon_offsets.push_back(static_cast<int64_t>(p->canon_entries.size() / 2));
-  }
+  for (int32_t id : preorder) n_shared += shared(id) ? 1 : 0;
   p->shared_chunks = n_shared;
 
   // runs of shared chunks with an identical batch range
@@ -425,21 +434,20 @@ pst_status rebuild(pst_pool* p) {
     runs[run_of[id]].push_back(id);
   }
 
-  std::vector<int32_t> chunks;
-  std::vector<int32_t> tc_items, simt_items, warp_items;
-  // Partial results, one entry per (batch row, KV head) pair and item that
-  // covers it.  The rows of one pair end up contiguous in entry order (slot
-  // e of the pair holds heads kv*g .. kv*g+g-1 at rows e*g ..), so the merge
-  // reads one contiguous block per pair.  An entry points back at its
-  // producer: a tensor-core row-index slot (rows of head 0 at tc_rows[pos]) or
-  // a CUDA-core item (x).
-  struct Entry {
-    int32_t key;  // u * Hkv + kv
-    int32_t pos;  // >= 0: index into tc_rows of head 0; < 0: -1 - CUDA-core item index
-  };
-  std::vector<Entry> ents;
-  std::vector<int32_t> tc_rows;  // tensor-core item row -> partial row
-  std::vector<Stream> streams;
+  BuildScratch& sc = p->scratch;
+  auto& chunks = sc.chunks;
+  auto& tc_items = sc.tc_items;
+  auto& simt_items = sc.simt_items;
+  auto& ents = sc.ents;      // partial-result entries (see Entry)
+  auto& tc_rows = sc.tc_rows;  // tensor-core item row -> partial row
+  auto& streams = sc.streams;
+  chunks.clear();
+  tc_items.clear();
+  simt_items.clear();
+  ents.clear();
+  tc_rows.clear();
+  streams.clear();
+  std::vector<int32_t> warp_items;
 
   // ---- phase 1: chunk-first over the runs.  The tensor-core kernel takes a
   // chunk as tiles of 64 keys (two for 128-token chunks): its costs and item
@@ -572,19 +580,29 @@ pst_status rebuild(pst_pool* p) {
     std::vector<int32_t> order(n);
     for (int32_t x = 0; x < n; ++x) order[x] = x;
     std::stable_sort(order.begin(), order.end(), [&](int32_t a, int32_t b) { return cost[a] > cost[b]; });
-    std::vector<double> load(k, 0.0);
-    std::vector<std::vector<int32_t>> per(k);
+    // each item to the least-loaded CTA, the lowest index among equals: a
+    // min-heap on (load, CTA)
+    std::vector<std::pair<double, int32_t>> heap(k);
+    for (int32_t c = 0; c < k; ++c) heap[c] = {0.0, c};
+    std::vector<int32_t> cta_of(n), count(k + 1, 0);
     for (int32_t x : order) {
-      const int32_t c = static_cast<int32_t>(std::min_element(load.begin(), load.end()) - load.begin());
-      load[c] += cost[x];
-      per[c].push_back(x);
+      std::pop_heap(heap.begin(), heap.end(), std::greater<>());
+      auto& top = heap.back();
+      cta_of[x] = top.second;
+      ++count[top.second + 1];
+      top.first += cost[x];
+      std::push_heap(heap.begin(), heap.end(), std::greater<>());
     }
-    std::vector<int32_t> sorted;
-    sorted.reserve(tc_items.size());
-    for (int32_t c = 0; c < k; ++c) {
-      for (int32_t x : per[c]) sorted.insert(sorted.end(), tc_items.begin() + 8 * x, tc_items.begin() + 8 * x + 8);
-      tc_cta_off.push_back(static_cast<int32_t>(sorted.size() / 8));
+    // items grouped by CTA, each CTA's in assignment order
+    for (int32_t c = 0; c < k; ++c) count[c + 1] += count[c];
+    auto& sorted = sc.sorted;
+    sorted.resize(tc_items.size());
+    std::vector<int32_t> fill_at(count.begin(), count.end() - 1);
+    for (int32_t x : order) {
+      const int32_t at = fill_at[cta_of[x]]++;
+      std::copy(tc_items.begin() + 8 * x, tc_items.begin() + 8 * x + 8, sorted.begin() + 8 * at);
     }
+    for (int32_t c = 0; c < k; ++c) tc_cta_off.push_back(count[c + 1]);
     tc_items.swap(sorted);
     p->n_tc_ctas = k;
   }
@@ -611,19 +629,45 @@ pst_status rebuild(pst_pool* p) {
                          : static_cast<int32_t>(std::max<int64_t>(
                                1, static_cast<int64_t>(static_cast<double>(T) * std::sqrt(static_cast<double>(g)) /
                                                        (p->simt_unit_div * W)))));
-    std::vector<Stream> units;
+    // the units, largest first and in stream order among equals: a stable
+    // bucket pass (a unit has 1 .. unit <= kSimtInline chunks)
+    std::vector<int32_t> of_len(kSimtInline + 2, 0);
+    for (const auto& st : streams) {
+      of_len[std::min(unit, st.n) + 1] += st.n / unit;
+      if (st.n % unit) ++of_len[st.n % unit + 1];
+    }
+    std::vector<int32_t> at(kSimtInline + 1, 0);  // first slot of each length, longest first
+    for (int32_t len = kSimtInline, pos = 0; len >= 1; --len) {
+      at[len] = pos;
+      pos += of_len[len + 1];
+    }
+    auto& units = sc.units;
+    units.resize(static_cast<size_t>(at[1] + of_len[2]));
     for (const auto& st : streams)
-      for (int32_t a = 0; a < st.n; a += unit) units.push_back({st.chunk_off + a, std::min(unit, st.n - a), st.kv, st.group});
-    std::stable_sort(units.begin(), units.end(), [](const Stream& x, const Stream& y) { return x.n > y.n; });
+      for (int32_t a = 0; a < st.n; a += unit) {
+        const int32_t len = std::min(unit, st.n - a);
+        units[at[len]++] = {st.chunk_off + a, len, st.kv, st.group};
+      }
     int64_t tail = 0;
     size_t cut = units.size();
     while (cut > 0 && static_cast<double>(tail) < p->simt_tail * W) tail += units[--cut].n;
-    std::vector<Stream> ordered(units.begin(), units.begin() + cut);
+    auto& ordered = sc.ordered;
+    ordered.assign(units.begin(), units.begin() + cut);
     for (size_t x = cut; x < units.size(); ++x)
       for (int32_t a = 0; a < units[x].n; ++a) ordered.push_back({units[x].chunk_off + a, 1, units[x].kv, units[x].group});
-    for (const auto& un : ordered) {
-      ents.push_back({un.group * Hkv + un.kv, -1 - static_cast<int32_t>(simt_items.size() / 8)});
-      push_simt_item(simt_items, chunks, un.chunk_off, un.n, un.kv, un.group, 0);
+    // one entry and one 8-word item per unit, written in place
+    const size_t e0 = ents.size(), i0 = simt_items.size() / 8;
+    ents.resize(e0 + ordered.size());
+    simt_items.resize(8 * (i0 + ordered.size()));
+    for (size_t x = 0; x < ordered.size(); ++x) {
+      const Stream& un = ordered[x];
+      ents[e0 + x] = {un.group * Hkv + un.kv, -1 - static_cast<int32_t>(i0 + x)};
+      int32_t* it = simt_items.data() + 8 * (i0 + x);
+      for (int32_t c = 0; c < kSimtInline; ++c) it[c] = c < un.n ? chunks[un.chunk_off + c] : 0;
+      it[4] = un.n;
+      it[5] = un.kv;
+      it[6] = un.group;
+      it[7] = 0;
     }
     warp_items.assign(1, 0);
   }
@@ -632,7 +676,8 @@ pst_status rebuild(pst_pool* p) {
 
   // ---- merge CSR per (batch row, KV head): entry slots in emission order,
   // and each producer told its rows
-  std::vector<int32_t> moff(static_cast<size_t>(B) * Hkv + 1, 0);
+  auto& moff = sc.moff;
+  moff.assign(static_cast<size_t>(B) * Hkv + 1, 0);
   for (const auto& e : ents) moff[e.key + 1]++;
   for (size_t x = 1; x < moff.size(); ++x) moff[x] += moff[x - 1];
   {
@@ -646,7 +691,8 @@ pst_status rebuild(pst_pool* p) {
     if (p->merge_cap_forced >= 0) p->merge_cap = std::min(p->merge_cap, p->merge_cap_forced);
   }
   {
-    std::vector<int32_t> fill(moff.begin(), moff.end() - 1);
+    auto& fill = sc.fill;
+    fill.assign(moff.begin(), moff.end() - 1);
     for (const auto& e : ents) {
       const int32_t slot = fill[e.key]++;
       if (e.pos >= 0) {
@@ -678,6 +724,10 @@ pst_status rebuild(pst_pool* p) {
   t.insert(t.end(), tc_rows.begin(), tc_rows.end());
   if (t.empty()) t.push_back(0);
 
+  p->tab_ni.swap(ni);
+  p->tab_nj.swap(nj);
+  p->tab_preorder.swap(preorder);
+  p->canon_valid = false;
   p->rebuild_count++;
   p->dirty = false;
   p->tab_uploaded = false;
@@ -1542,12 +1592,39 @@ pst_status pst_write_kv_last(pst_pool* p, int32_t layer, int64_t n, const int64_
   return run_scatter(p, ops, k, v, static_cast<cudaStream_t>(stream), false, layer);
 }
 
+// Canonical (chunk-id free) tables of the last rebuild: per shared chunk in
+// preorder (depth, i, j, tokens), per sequence in batch order its path's
+// (depth, shared) entries.
+static void build_canonical(pst_pool* p) {
+  if (p->canon_valid) return;
+  const auto& ni = p->tab_ni;
+  const auto& nj = p->tab_nj;
+  auto shared = [&](int32_t id) { return nj[id] - ni[id] >= p->cfg.min_share; };
+  p->canon_shared.clear();
+  p->canon_entries.clear();
+  p->canon_offsets.assign(1, 0);
+  for (int32_t id : p->tab_preorder) {
+    if (!shared(id)) continue;
+    const Node& n = p->nodes[id];
+    p->canon_shared.insert(p->canon_shared.end(), {n.depth, ni[id], nj[id], n.n_tokens});
+  }
+  for (int64_t sid : p->batch) {
+    for (int32_t id : p->seqs[sid].path) {
+      p->canon_entries.push_back(p->nodes[id].depth);
+      p->canon_entries.push_back(shared(id) ? 1 : 0);
+    }
+    p->canon_offsets.push_back(static_cast<int64_t>(p->canon_entries.size() / 2));
+  }
+  p->canon_valid = true;
+}
+
 pst_status pst_export_tables(const pst_pool* p, int32_t* shared_rows, int64_t shared_cap, int64_t* n_shared,
                              int32_t* seq_entries, int64_t entries_cap, int64_t* n_entries, int64_t* seq_offsets,
                              int64_t offsets_cap, int64_t* B) {
   if (!p || !n_shared || !n_entries || !B) return fail(PST_ERR_INVALID, "null count pointer");
   pst_status st = ensure_tables(p);
   if (st != PST_OK) return st;
+  build_canonical(const_cast<pst_pool*>(p));
   *n_shared = static_cast<int64_t>(p->canon_shared.size() / 4);
   *n_entries = static_cast<int64_t>(p->canon_entries.size() / 2);
   *B = static_cast<int64_t>(p->batch.size());
