@@ -29,7 +29,8 @@
  *   - "device" pointers are CUDA device memory on the pool's device; "host"
  *     pointers are ordinary host memory.  The caller owns every buffer it
  *     passes; the library never frees or retains caller pointers.
- *   - Tensors are dense, row-major, in the pool dtype (pst_config.dtype).
+ *   - Tensors are dense, row-major, in the pool dtype (pst_config.dtype);
+ *     attention outputs are fp32 instead when the pool has PST_FLAG_F32_OUT.
  *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Device work
  *     is enqueued asynchronously on it; host-side tree changes happen before
  *     the call returns.  All calls on one pool must be issued from one host
@@ -62,8 +63,11 @@ typedef enum { PST_F16 = 0, PST_BF16 = 1, PST_F32 = 2 } pst_dtype;
 /* pst_config.flags */
 enum {
   PST_FLAG_NO_TENSOR_CORES = 1,  /* run the chunk-first phase on the CUDA-core kernel too */
-  PST_FLAG_CONCURRENT_PHASES = 2 /* run the two phases at once on disjoint SMs (fork/join over an
-                                    internal stream) instead of back to back */
+  PST_FLAG_CONCURRENT_PHASES = 2, /* run the two phases at once on disjoint SMs (fork/join over an
+                                     internal stream) instead of back to back */
+  PST_FLAG_F32_OUT = 4            /* every attention call writes `out` as fp32 rows (the value the
+                                     kernels would otherwise round to the pool dtype, round to
+                                     nearest even); q and K/V stay in the pool dtype */
 };
 
 typedef struct {
@@ -71,8 +75,9 @@ typedef struct {
   int32_t n_kv_heads;  /* Hkv >= 1, divides Hq, Hq/Hkv in {1,2,4,8} */
   int32_t head_dim;    /* d in {64, 128} */
   int32_t chunk_size;  /* c in {16, 32, 64, 128}; the chunk-first phase runs on the
-                          tensor cores (tcgen05) for 16-bit K/V at c = 64, on the
-                          CUDA-core kernel otherwise */
+                          tensor cores (tcgen05) for 16-bit K/V at c = 64 and 128
+                          (a 128-token chunk as two 64-key tiles), on the CUDA-core
+                          kernel otherwise */
   int64_t max_chunks;  /* pool capacity in chunks (>= 1) */
   int32_t dtype;       /* pst_dtype */
   int32_t min_share;   /* chunk-first threshold: a chunk covered by >= min_share live
@@ -160,7 +165,7 @@ pst_status pst_seq_length(const pst_pool* pool, int64_t seq_id, int64_t* n_token
  * q, out: device [B][Hq][d], B = live count.  Rebuilds and uploads the chunk
  * tables first if the tree changed (Knowl 5).  q and out must start on a
  * 16-byte boundary (PST_ERR_INVALID otherwise).  Chunk-first partials run on the
- * tensor cores (tcgen05) for f16/bf16 with c = 64, sequence-first partials on
+ * tensor cores (tcgen05) for f16/bf16 with c = 64 or 128, sequence-first partials on
  * warp-level tensor-core products (f16/bf16) or the CUDA cores (f32), then a
  * merge kernel combines the partial rows (attn_reduce) and writes out. */
 pst_status pst_decode_attention(pst_pool* pool, const void* q, void* out, void* stream);
@@ -179,19 +184,24 @@ pst_status pst_decode_attention_host(pst_pool* pool, const void* q_host, void* o
  * front, or a latency-critical loop where cudaMalloc / cudaFree would
  * synchronise the device.  Same inputs, outputs and result as
  * pst_decode_attention, but the partial rows live in a fixed 32 MiB device
- * area that the library defines at file scope: every GPU that loads the
- * library holds that area until the process exits.
- *   - The first call on a device looks up the area's device address (once per
- *     device); make that first call before any stream capture.
+ * area that the library defines at file scope.  The area is committed on a
+ * device when the first pool is created there (pst_pool_create looks up its
+ * device address, which loads the module that holds it) and stays until the
+ * process exits; this call itself never loads a module or allocates.
+ *   - It takes no per-phase timings (pst_set_profiling does not apply; after
+ *     it, pst_phase_times reports nothing) and always launches the phases
+ *     overlapped on `stream`, ignoring PST_FLAG_CONCURRENT_PHASES.
  *   - Needs the chunk tables already on the device: after a structural change
  *     (insert, remove, a new chunk on append) call pst_decode_attention once
  *     first; otherwise returns PST_ERR_STATE.  It never rebuilds or uploads.
  *   - A batch needing more than 32 MiB of scratch (about
  *     partial_rows * (d + 2) * 4 bytes, see pst_stats) returns
  *     PST_ERR_INVALID.
- *   - All calls share the one area (it keeps the last call's contents; every
- *     partial row is written before it is read, so nothing needs clearing):
- *     calls whose GPU work overlaps -- on different streams or from different
+ *   - All calls share the one area, which keeps the last call's contents.
+ *     Its first 4 bytes are the work-claim counter, which must start at zero:
+ *     every call clears it with a 4-byte cudaMemsetAsync on `stream`; every
+ *     partial row is written before it is read, so nothing else is cleared.
+ *     Calls whose GPU work overlaps -- on different streams or from different
  *     pools -- race with each other.
  * Calls no cudaMalloc, cudaFree or other allocating routine. */
 pst_status pst_decode_attention_noalloc(pst_pool* pool, const void* q, void* out, void* stream);
@@ -293,7 +303,9 @@ pst_status pst_set_profiling(pst_pool* pool, int enable);
  * ms[1] sequence-first kernel (0 when a kernel did not run), ms[2] the whole
  * call from its first kernel to the end of the merge.  Waits for those
  * events.  (The per-kernel events sit between the kernels and may keep them
- * from overlapping; time the whole call without profiling.) */
+ * from overlapping; time the whole call without profiling.)  After a
+ * profiled prefill call: the attention kernel alone, in ms[0] (tensor-core
+ * kernel) or ms[1] (CUDA-core kernel). */
 pst_status pst_phase_times(pst_pool* pool, float* ms3);
 
 /* Kernel launches issued by the last pst_decode_attention call. */

@@ -63,6 +63,48 @@ __device__ __forceinline__ uint32_t pack2_16(float a, float b) {
   }
 }
 
+// The low / high 16-bit value packed in w (as pack2_16 wrote them),
+// converted exactly to fp32.
+template <typename T>
+__device__ __forceinline__ float lo16(uint32_t w) {
+  if constexpr (std::is_same<T, __half>::value) {
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(w & 0xffffu)));
+  } else {
+    return __uint_as_float(w << 16);
+  }
+}
+template <typename T>
+__device__ __forceinline__ float hi16(uint32_t w) {
+  if constexpr (std::is_same<T, __half>::value) {
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(w >> 16)));
+  } else {
+    return __uint_as_float(w & 0xffff0000u);
+  }
+}
+// Sum of both: the row sum of two rounded probabilities.
+template <typename T>
+__device__ __forceinline__ float sum2_16(uint32_t w) {
+  return lo16<T>(w) + hi16<T>(w);
+}
+
+// Element `elem` of an output tensor whose elements are T, or fp32 when
+// out_f32 is set (the value before the final rounding to T).
+template <typename T>
+__device__ __forceinline__ void store_out1(void* out, size_t elem, float x, int out_f32) {
+  if (out_f32) static_cast<float*>(out)[elem] = x;
+  else static_cast<T*>(out)[elem] = from_float<T>(x);
+}
+
+// Four consecutive output elements from elem (a multiple of 4).
+template <typename T>
+__device__ __forceinline__ void store_out4(void* out, size_t elem, float a, float b, float c, float d, int out_f32) {
+  if (out_f32 || sizeof(T) == 4) {
+    *reinterpret_cast<float4*>(static_cast<float*>(out) + elem) = make_float4(a, b, c, d);
+  } else {
+    *reinterpret_cast<uint2*>(static_cast<T*>(out) + elem) = make_uint2(pack2_16<T>(a, b), pack2_16<T>(c, d));
+  }
+}
+
 __device__ __forceinline__ float warp_max(float x) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
@@ -173,15 +215,9 @@ __device__ __forceinline__ void merge_task(const AttnParams& p, int key, int e0,
   for (int i = 0; i < NI; ++i) {
     const float inv = 1.f / __shfl_sync(0xffffffffu, nn, hg_i[i]);
     const int f = lane + 32 * i;
-    if (f < F4) {
-      T* out = static_cast<T*>(p.out) + (static_cast<size_t>(key) * G + f / RF) * D + (f % RF) * 4;
-      if constexpr (sizeof(T) == 2) {
-        *reinterpret_cast<uint2*>(out) =
-            make_uint2(pack2_16<T>(acc[i].x * inv, acc[i].y * inv), pack2_16<T>(acc[i].z * inv, acc[i].w * inv));
-      } else {
-        *reinterpret_cast<float4*>(out) = make_float4(acc[i].x * inv, acc[i].y * inv, acc[i].z * inv, acc[i].w * inv);
-      }
-    }
+    if (f < F4)
+      store_out4<T>(p.out, (static_cast<size_t>(key) * G + f / RF) * D + (f % RF) * 4, acc[i].x * inv, acc[i].y * inv,
+                    acc[i].z * inv, acc[i].w * inv, p.out_f32);
   }
 }
 
@@ -235,15 +271,9 @@ __device__ __forceinline__ void merge_task_staged(const AttnParams& p, int key, 
   for (int i = 0; i < NI; ++i) {
     const float inv = 1.f / __shfl_sync(0xffffffffu, nn, hg_i[i]);
     const int f = lane + 32 * i;
-    if (f < F4) {
-      T* out = static_cast<T*>(p.out) + (static_cast<size_t>(key) * G + f / RF) * D + (f % RF) * 4;
-      if constexpr (sizeof(T) == 2) {
-        *reinterpret_cast<uint2*>(out) =
-            make_uint2(pack2_16<T>(acc[i].x * inv, acc[i].y * inv), pack2_16<T>(acc[i].z * inv, acc[i].w * inv));
-      } else {
-        *reinterpret_cast<float4*>(out) = make_float4(acc[i].x * inv, acc[i].y * inv, acc[i].z * inv, acc[i].w * inv);
-      }
-    }
+    if (f < F4)
+      store_out4<T>(p.out, (static_cast<size_t>(key) * G + f / RF) * D + (f % RF) * 4, acc[i].x * inv, acc[i].y * inv,
+                    acc[i].z * inv, acc[i].w * inv, p.out_f32);
   }
 }
 

@@ -86,12 +86,13 @@ constexpr int kSlotHeader = 64;
 // and the probabilities (G x C fp32); the tensor-core consumer (16-bit K/V)
 // keeps its query rows in registers and the probabilities as the transposed
 // C x 8 block of 16-bit values (one 16-byte row per key, columns past G
-// unused) that the P V product reads back.
+// unused) that the P V product reads back -- for bf16 two such blocks, P's
+// rounded value and the rounded remainder (see the consumer).
 struct SimtLayout {
   uint32_t stage, q, p, slot, slot_bytes, bars, total;
 };
 
-__host__ __device__ inline SimtLayout simt_layout(int C, int D, int G, int S, int es) {
+__host__ __device__ inline SimtLayout simt_layout(int C, int D, int G, int S, int es, bool p_split) {
   SimtLayout L;
   L.stage = static_cast<uint32_t>(simt_stage_bytes(C, D, es));
   size_t off = static_cast<size_t>(S) * L.stage;
@@ -99,7 +100,7 @@ __host__ __device__ inline SimtLayout simt_layout(int C, int D, int G, int S, in
   L.q = static_cast<uint32_t>(off);
   off += mma ? 0 : static_cast<size_t>(G) * D * 4;
   L.p = static_cast<uint32_t>(off);
-  off += mma ? static_cast<size_t>(C) * 16 : static_cast<size_t>(G) * C * 4;
+  off += mma ? static_cast<size_t>(C) * 16 * (p_split ? 2 : 1) : static_cast<size_t>(G) * C * 4;
   off = simt_align_up(off, 128);
   L.slot = static_cast<uint32_t>(off);
   L.slot_bytes = static_cast<uint32_t>(kSlotHeader + static_cast<size_t>(G) * D * es);
@@ -111,8 +112,8 @@ __host__ __device__ inline SimtLayout simt_layout(int C, int D, int G, int S, in
   return L;
 }
 
-__host__ __device__ inline size_t simt_warp_bytes(int C, int D, int G, int S, int es) {
-  return simt_layout(C, D, G, S, es).total;
+__host__ __device__ inline size_t simt_warp_bytes(int C, int D, int G, int S, int es, bool p_split) {
+  return simt_layout(C, D, G, S, es, p_split).total;
 }
 
 // A work item as loaded: the two raw 16-byte halves of the SimtItem and
@@ -179,7 +180,11 @@ __global__ void __launch_bounds__(32 * (simt_max_warps(G, sizeof(T)) + 1), 1) at
   static_assert(!kMma || (G <= 8 && C % 16 == 0 && KPR % 16 == 0 && VPR % 16 == 0), "mma shape");
   const int S = p.stages;
   const int NW = p.warps_per_cta;  // consumer warps; warp NW produces
-  const SimtLayout L = simt_layout(C, D, G, S, ES);
+  // bf16 probabilities go to the tensor cores as two bf16 terms, the rounded
+  // value and the rounded remainder: 16 significant bits instead of 8, so a
+  // row dominated by a few keys keeps its accuracy
+  constexpr bool kPSplit = std::is_same<T, __nv_bfloat16>::value;
+  const SimtLayout L = simt_layout(C, D, G, S, ES, kPSplit);
 
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ int s_abort;
@@ -615,11 +620,23 @@ __global__ void __launch_bounds__(32 * (simt_max_warps(G, sizeof(T)) + 1), 1) at
             const float e1 = ptx::ex2(fmaf(sacc[t][1], sl2, -mu1));
             const float e2 = ptx::ex2(fmaf(sacc[t][2], sl2, -mu0));
             const float e3 = ptx::ex2(fmaf(sacc[t][3], sl2, -mu1));
-            ps0 += e0 + e2;
-            ps1 += e1 + e3;
-            // P^T row of key t*16 + lg (+8): query columns 2 lq, 2 lq + 1
-            *reinterpret_cast<uint32_t*>(pbuf_b + (t * 16 + lg) * 16 + lq * 4) = pack2_16<T>(e0, e1);
-            *reinterpret_cast<uint32_t*>(pbuf_b + (t * 16 + lg + 8) * 16 + lq * 4) = pack2_16<T>(e2, e3);
+            // P^T row of key t*16 + lg (+8): query columns 2 lq, 2 lq + 1.
+            // The row sums add the rounded probabilities the product reads,
+            // so o / n stays a weighted mean of V rows.
+            const uint32_t w01 = pack2_16<T>(e0, e1), w23 = pack2_16<T>(e2, e3);
+            *reinterpret_cast<uint32_t*>(pbuf_b + (t * 16 + lg) * 16 + lq * 4) = w01;
+            *reinterpret_cast<uint32_t*>(pbuf_b + (t * 16 + lg + 8) * 16 + lq * 4) = w23;
+            if constexpr (kPSplit) {
+              const float h0 = lo16<T>(w01), h1 = hi16<T>(w01), h2 = lo16<T>(w23), h3 = hi16<T>(w23);
+              const uint32_t r01 = pack2_16<T>(e0 - h0, e1 - h1), r23 = pack2_16<T>(e2 - h2, e3 - h3);
+              *reinterpret_cast<uint32_t*>(pbuf_b + C * 16 + (t * 16 + lg) * 16 + lq * 4) = r01;
+              *reinterpret_cast<uint32_t*>(pbuf_b + C * 16 + (t * 16 + lg + 8) * 16 + lq * 4) = r23;
+              ps0 += (h0 + lo16<T>(r01)) + (h2 + lo16<T>(r23));
+              ps1 += (h1 + hi16<T>(r01)) + (h3 + hi16<T>(r23));
+            } else {
+              ps0 += lo16<T>(w01) + lo16<T>(w23);
+              ps1 += hi16<T>(w01) + hi16<T>(w23);
+            }
           }
           nl2[0] = nl2[0] * al0 + ps0;
           nl2[1] = nl2[1] * al1 + ps1;
@@ -633,20 +650,24 @@ __global__ void __launch_bounds__(32 * (simt_max_warps(G, sizeof(T)) + 1), 1) at
           __syncwarp();  // P^T is written
           // B fragments of P^T (keys x query columns), k-steps of 16 keys:
           // matrices of 8 key rows, transposed on load
-          uint32_t pf[MT][2];
-          if constexpr (MT == 1) {
-            ptx::ldsm_x2_trans(pb + (lane & 15) * 16, pf[0]);
-          } else {
+          uint32_t pf[MT][2], pfr[kPSplit ? MT : 1][2];  // P (rounded) and, for bf16, its rounded remainder
+          auto load_p = [&](uint32_t base, uint32_t (*dst)[2]) {
+            if constexpr (MT == 1) {
+              ptx::ldsm_x2_trans(base + (lane & 15) * 16, dst[0]);
+            } else {
 #pragma unroll
-            for (int t2 = 0; t2 < MT / 2; ++t2) {
-              uint32_t r[4];
-              ptx::ldsm_x4_trans(pb + (t2 * 32 + lane) * 16, r);
-              pf[2 * t2][0] = r[0];
-              pf[2 * t2][1] = r[1];
-              pf[2 * t2 + 1][0] = r[2];
-              pf[2 * t2 + 1][1] = r[3];
+              for (int t2 = 0; t2 < MT / 2; ++t2) {
+                uint32_t r[4];
+                ptx::ldsm_x4_trans(base + (t2 * 32 + lane) * 16, r);
+                dst[2 * t2][0] = r[0];
+                dst[2 * t2][1] = r[1];
+                dst[2 * t2 + 1][0] = r[2];
+                dst[2 * t2 + 1][1] = r[3];
+              }
             }
-          }
+          };
+          load_p(pb, pf);
+          if constexpr (kPSplit) load_p(pb + C * 16, pfr);
 
           // ---- O^T += V^T P^T over the V^T pieces (VPR feature rows of one
           // key block each: VKS k-steps of 16 keys from key vb * 16 VKS)
@@ -674,8 +695,11 @@ __global__ void __launch_bounds__(32 * (simt_max_warps(G, sizeof(T)) + 1), 1) at
             for (int ks = 0; ks < VKS; ++ks) {
               if (ks + 1 < VKS) load_v(ks + 1, af[(ks + 1) & 1]);
 #pragma unroll
-              for (int t = 0; t < VMT; ++t)
+              for (int t = 0; t < VMT; ++t) {
                 ptx::mma_16816<BF>(o[vg * VMT + t], af[ks & 1][t], pf[vb * VKS + ks][0], pf[vb * VKS + ks][1]);
+                if constexpr (kPSplit)
+                  ptx::mma_16816<BF>(o[vg * VMT + t], af[ks & 1][t], pfr[vb * VKS + ks][0], pfr[vb * VKS + ks][1]);
+              }
             }
             __syncwarp();  // every lane is done with the stage (and with P^T before the next chunk)
             ++consumed;
@@ -701,11 +725,11 @@ __global__ void __launch_bounds__(32 * (simt_max_warps(G, sizeof(T)) + 1), 1) at
           if (h < G) {
             if (p.final_mode) {
               const float inv = 1.f / nl2[j];
-              T* out = static_cast<T*>(p.out) + (static_cast<size_t>(grp) * p.Hq + kv * p.g + h) * D;
+              const size_t row = (static_cast<size_t>(grp) * p.Hq + kv * p.g + h) * D;
 #pragma unroll
               for (int t = 0; t < OMT; ++t) {
-                out[t * 16 + lg] = from_float<T>(o[t][j] * inv);
-                out[t * 16 + lg + 8] = from_float<T>(o[t][2 + j] * inv);
+                store_out1<T>(p.out, row + t * 16 + lg, o[t][j] * inv, p.out_f32);
+                store_out1<T>(p.out, row + t * 16 + lg + 8, o[t][2 + j] * inv, p.out_f32);
               }
             } else {
               const size_t row = static_cast<size_t>(part_base) + h;
@@ -878,9 +902,9 @@ __global__ void __launch_bounds__(32 * (simt_max_warps(G, sizeof(T)) + 1), 1) at
 #pragma unroll
         for (int h = 0; h < G; ++h) {
           const float inv = 1.f / warp_sum(nl[h]);
-          T* out = static_cast<T*>(p.out) + (static_cast<size_t>(grp) * p.Hq + kv * p.g + h) * D;
+          const size_t row = (static_cast<size_t>(grp) * p.Hq + kv * p.g + h) * D;
 #pragma unroll
-          for (int i = 0; i < DPL; ++i) out[lane + 32 * i] = from_float<T>((o[h][i].x + o[h][i].y) * inv);
+          for (int i = 0; i < DPL; ++i) store_out1<T>(p.out, row + lane + 32 * i, (o[h][i].x + o[h][i].y) * inv, p.out_f32);
         }
       } else {
 #pragma unroll
@@ -910,7 +934,8 @@ __global__ void __launch_bounds__(32 * (simt_max_warps(G, sizeof(T)) + 1), 1) at
 template <typename T, int D, int G, int C>
 cudaError_t launch_simt_t(const AttnParams& p, int grid, cudaStream_t s) {
   if (p.warps_per_cta < 1 || p.warps_per_cta > simt_max_warps(G, sizeof(T))) return cudaErrorInvalidValue;
-  const size_t smem = simt_warp_bytes(C, D, G, p.stages, sizeof(T)) * p.warps_per_cta;
+  const size_t smem = simt_warp_bytes(C, D, G, p.stages, sizeof(T), std::is_same<T, __nv_bfloat16>::value) *
+                     p.warps_per_cta;
   auto fn = attn_simt_kernel<T, D, G, C>;
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;

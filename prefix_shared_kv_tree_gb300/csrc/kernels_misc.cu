@@ -210,7 +210,7 @@ int attn_simt_max_warps(int dtype, int g) { return simt_max_warps(g, dtype_size(
 size_t attn_simt_piece_bytes(int dtype, int D, int C) { return simt_stage_bytes(C, D, dtype_size(dtype)); }
 
 size_t attn_simt_smem(int dtype, int D, int C, int g, int stages, int warps_per_cta) {
-  return simt_warp_bytes(C, D, g, stages, dtype_size(dtype)) * warps_per_cta;
+  return simt_warp_bytes(C, D, g, stages, dtype_size(dtype), dtype == kBF16) * warps_per_cta;
 }
 
 cudaError_t launch_attn_simt(int dtype, int D, int C, int g, const AttnParams& p, int grid, cudaStream_t s) {

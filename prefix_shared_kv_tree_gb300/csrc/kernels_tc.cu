@@ -25,8 +25,8 @@
 //   warp 6      : gathers the next item's query rows into the other half of a
 //                 double-buffered Q tile while the current item computes.
 //   warp 1      : allocates TMEM and issues S = Q K^T (M=128, N=64, K=D) into
-//                 three TMEM buffers, as far ahead of the softmax as they allow,
-//                 across item boundaries.
+//                 three TMEM buffers (two for bf16), as far ahead of the
+//                 softmax as they allow, across item boundaries.
 //   warp 7      : issues O += P V (M=128, N=D, K=64, A = P read from TMEM) into
 //                 the item's O buffer (double-buffered by item).
 //                 Both issuer warps run their loops whole; one elected lane
@@ -37,7 +37,8 @@
 //                 log2 units against a reference max that moves only when a
 //                 chunk's max passes it by more than 2^8 (then O and the row
 //                 sum are rescaled in TMEM), write the rounded probabilities P
-//                 into TMEM as the A operand of the PV product, and at the
+//                 into TMEM as the A operand of the PV product (for bf16 also
+//                 the rounded remainders, a second PV product), and at the
 //                 item's end stream O out of TMEM: the item's partial rows
 //                 (the merge kernel combines them) or, for a prefill block, the
 //                 normalised output rows.
@@ -61,7 +62,7 @@ namespace {
 constexpr int kC = 64;     // tokens per chunk
 constexpr int kBM = 128;   // stacked query rows per item
 constexpr int kNS = 5;     // K/V tile stages
-constexpr int kSB = 3;     // S buffers in TMEM: S runs kSB - 1 chunks ahead of the PV product
+constexpr int kSB = 3;     // S buffers in TMEM at most: S runs up to kSB - 1 chunks ahead of the PV product
 
 __host__ __device__ constexpr uint32_t tc_tile_bytes(int D) { return 2u * kC * D * 2u; }
 __host__ __device__ constexpr uint32_t tc_q_bytes(int D) { return kBM * D * 2u; }
@@ -91,15 +92,23 @@ __global__ void __launch_bounds__(256, 1) attn_tc_kernel(const AttnParams p) {
   constexpr uint32_t QB = tc_q_bytes(D);
   constexpr int DCH = D / 8;    // 16-byte chunks per row when the reduction runs over D
   constexpr int CCH = kC / 8;   // 16-byte chunks per row when the reduction runs over keys
-  constexpr uint32_t S_COL = 0;  // S buffers: columns [kC b, kC b + kC), b < kSB
-  // O of an item, double-buffered by item: [O_COL, O_COL + D), [O_COL + D, O_COL + 2D)
-  constexpr uint32_t O_COL = kSB * kC;
-  // P double buffer, the A operand of the PV product: a row's kC 16-bit
-  // probabilities packed two per column, [P_COL, P_COL + 32), [.. + 32, .. + 64)
-  constexpr uint32_t P_COL = O_COL + 2 * D;
-  constexpr uint32_t TMEM_COLS = (P_COL + kC) <= 256 ? 256u : 512u;
-  static_assert(P_COL + kC <= 512, "tensor memory columns");
   constexpr bool BF = std::is_same<T, __nv_bfloat16>::value;
+  // bf16 probabilities go to the PV product as two bf16 terms, the rounded
+  // value and the rounded remainder (16 significant bits instead of 8, so a
+  // row dominated by a few keys keeps its accuracy); their room in TMEM comes
+  // from one S buffer less
+  constexpr bool PSPLIT = BF;
+  constexpr int SB = PSPLIT ? 2 : kSB;               // S buffers in use
+  constexpr uint32_t PW = PSPLIT ? 64 : 32;          // TMEM columns of one P buffer
+  constexpr uint32_t S_COL = 0;  // S buffers: columns [kC b, kC b + kC), b < SB
+  // O of an item, double-buffered by item: [O_COL, O_COL + D), [O_COL + D, O_COL + 2D)
+  constexpr uint32_t O_COL = SB * kC;
+  // P double buffer, the A operand of the PV product: a row's kC 16-bit
+  // probabilities packed two per column, [P_COL + PW b, .. + 32) (and, split,
+  // the remainders in the next 32 columns)
+  constexpr uint32_t P_COL = O_COL + 2 * D;
+  constexpr uint32_t TMEM_COLS = (P_COL + 2 * PW) <= 256 ? 256u : 512u;
+  static_assert(P_COL + 2 * PW <= 512, "tensor memory columns");
   constexpr uint32_t ID_S = ptx::idesc_f16(kBM, kC, BF);
   constexpr uint32_t ID_O = ptx::idesc_f16(kBM, D, BF);
 
@@ -135,7 +144,7 @@ __global__ void __launch_bounds__(256, 1) attn_tc_kernel(const AttnParams p) {
       ptx::mbar_init(&full[s], 1);
       ptx::mbar_init(&empty[s], 1);
     }
-    for (int b = 0; b < kSB; ++b) {
+    for (int b = 0; b < SB; ++b) {
       ptx::mbar_init(&sfull[b], 1);
       ptx::mbar_init(&sfree[b], 128);
     }
@@ -241,10 +250,10 @@ __global__ void __launch_bounds__(256, 1) attn_tc_kernel(const AttnParams p) {
         return __all_sync(0xffffffffu, ptx::mbar_wait(bar, parity, abort_flag, p.err));
       };
       auto issue_s = [&](int t, int qb) -> bool {
-        const int s = t % kNS, b = t % kSB;
+        const int s = t % kNS, b = t % SB;
         if (!wait_all(&full[s], (t / kNS) & 1)) return false;
         if (lane == 0) *consumed_slot = t + 1;
-        if (t >= kSB && !wait_all(&sfree[b], ((t - kSB) / kSB) & 1)) return false;
+        if (t >= SB && !wait_all(&sfree[b], ((t - SB) / SB) & 1)) return false;
         ptx::tc_fence_after();
         // Descriptors of each K step = the tile's base descriptor + the step's
         // byte offset / 16 (the 14-bit start-address field never carries).
@@ -271,8 +280,14 @@ __global__ void __launch_bounds__(256, 1) attn_tc_kernel(const AttnParams p) {
         const uint64_t b0 = ptx::smem_desc_sw128(kv_addr + s * TILE + HALF, 1024);
 #pragma unroll
         for (int kk = 0; kk < kC / 16; ++kk)  // K step kk: keys [16kk, 16kk+16) = P columns [8kk, 8kk+8)
-          ptx::mma_f16_tmem_a_warp(tbase + O_COL + ob * D, tbase + P_COL + b * 32 + kk * 8, b0 + kk * 2, ID_O,
+          ptx::mma_f16_tmem_a_warp(tbase + O_COL + ob * D, tbase + P_COL + b * PW + kk * 8, b0 + kk * 2, ID_O,
                                    (c > 0 || kk > 0) ? 1u : 0u);
+        if constexpr (PSPLIT) {
+#pragma unroll
+          for (int kk = 0; kk < kC / 16; ++kk)  // the remainders: P columns 32 + [8kk, 8kk+8)
+            ptx::mma_f16_tmem_a_warp(tbase + O_COL + ob * D, tbase + P_COL + b * PW + 32 + kk * 8, b0 + kk * 2,
+                                     ID_O, 1u);
+        }
         ptx::mma_commit_warp(&pfree[b]);
         ptx::mma_commit_warp(&empty[s]);
         if (last) ptx::mma_commit_warp(&ofull[ob]);
@@ -353,8 +368,8 @@ __global__ void __launch_bounds__(256, 1) attn_tc_kernel(const AttnParams p) {
           }
         }
         const int lim = min(__shfl_sync(0xffffffffu, my_len, c & 31), key_limit - c * kC);
-        const int b = t & 1, sb = t % kSB;
-        if (!ptx::mbar_wait(&sfull[sb], (t / kSB) & 1, abort_flag, p.err)) {
+        const int b = t & 1, sb = t % SB;
+        if (!ptx::mbar_wait(&sfull[sb], (t / SB) & 1, abort_flag, p.err)) {
           ok = false;
           break;
         }
@@ -413,23 +428,38 @@ __global__ void __launch_bounds__(256, 1) attn_tc_kernel(const AttnParams p) {
           ok = false;
           break;
         }
-        // P = 2^(x * scale - m); the row sum is taken in fp32 before P is
-        // rounded to the operand type (two partial sums for a shorter chain).
+        // P = 2^(x * scale - m), rounded to the operand type (bf16: plus the
+        // rounded remainder); the row sum adds the rounded values the PV
+        // product reads (so o / n stays a weighted mean of V rows), in two
+        // partial sums for a shorter chain.
         const float neg_m = -m_use, sc = p.scale_log2;
         float ps0 = 0.f, ps1 = 0.f;
-        uint32_t pw[kC / 2];
+        uint32_t pw[kC / 2], pr[PSPLIT ? kC / 2 : 1];
 #pragma unroll
         for (int j = 0; j < CCH; ++j) {
           float e[8];
 #pragma unroll
           for (int q = 0; q < 8; ++q) e[q] = ptx::ex2(fmaf(x[8 * j + q], sc, neg_m));
-          ps0 += (e[0] + e[1]) + (e[2] + e[3]);
-          ps1 += (e[4] + e[5]) + (e[6] + e[7]);
 #pragma unroll
           for (int q = 0; q < 4; ++q) pw[4 * j + q] = pack2_plain<T>(e[2 * q], e[2 * q + 1]);
+          if constexpr (PSPLIT) {
+            float h[8];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              h[2 * q] = lo16<T>(pw[4 * j + q]);
+              h[2 * q + 1] = hi16<T>(pw[4 * j + q]);
+              pr[4 * j + q] = pack2_plain<T>(e[2 * q] - h[2 * q], e[2 * q + 1] - h[2 * q + 1]);
+            }
+            ps0 += (h[0] + h[1]) + (h[2] + h[3]) + sum2_16<T>(pr[4 * j]) + sum2_16<T>(pr[4 * j + 1]);
+            ps1 += (h[4] + h[5]) + (h[6] + h[7]) + sum2_16<T>(pr[4 * j + 2]) + sum2_16<T>(pr[4 * j + 3]);
+          } else {
+            ps0 += sum2_16<T>(pw[4 * j]) + sum2_16<T>(pw[4 * j + 1]);
+            ps1 += sum2_16<T>(pw[4 * j + 2]) + sum2_16<T>(pw[4 * j + 3]);
+          }
         }
         const float psum = ps0 + ps1;
-        ptx::tmem_st32(tl + P_COL + b * 32, pw);
+        ptx::tmem_st32(tl + P_COL + b * PW, pw);
+        if constexpr (PSPLIT) ptx::tmem_st32(tl + P_COL + b * PW + 32, pr);
         ptx::tmem_st_wait();
         ptx::tc_fence_before();  // orders the TMEM stores above before the PV product
         ptx::mbar_arrive(&pfull[b]);
@@ -443,7 +473,7 @@ __global__ void __launch_bounds__(256, 1) attn_tc_kernel(const AttnParams p) {
       if (!ok) break;
       ptx::tc_fence_after();
       const float inv = 1.f / l;
-      T* out = static_cast<T*>(p.out) + (static_cast<size_t>(grp) * p.Hq + w.kv * p.g + hg) * D;
+      const size_t out_row = (static_cast<size_t>(grp) * p.Hq + w.kv * p.g + hg) * D;
       float4* po = reinterpret_cast<float4*>(p.part_o + static_cast<size_t>(part_row) * D);
 #pragma unroll
       for (int cg = 0; cg < D / 32; ++cg) {
@@ -451,7 +481,14 @@ __global__ void __launch_bounds__(256, 1) attn_tc_kernel(const AttnParams p) {
         ptx::tmem_ld32(tl + O_COL + ob * D + 32 * cg, ov);
         ptx::tmem_ld_wait(ov);
         if (row_valid) {
-          if (p.final_mode) {
+          if (p.final_mode && p.out_f32) {
+            float4* o4 = reinterpret_cast<float4*>(static_cast<float*>(p.out) + out_row + 32 * cg);
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              o4[j] = make_float4(__uint_as_float(ov[4 * j]) * inv, __uint_as_float(ov[4 * j + 1]) * inv,
+                                  __uint_as_float(ov[4 * j + 2]) * inv, __uint_as_float(ov[4 * j + 3]) * inv);
+          } else if (p.final_mode) {
+            T* out = static_cast<T*>(p.out) + out_row;
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
               const float* o8 = reinterpret_cast<const float*>(ov) + 8 * j;

@@ -789,6 +789,7 @@ AttnParams base_params(const pst_pool* p, int32_t layer) {
   a.err = p->d_err;
   a.sched = p->d_sched;
   a.merge_cap = p->merge_cap;
+  a.out_f32 = (p->cfg.flags & PST_FLAG_F32_OUT) ? 1 : 0;
   return a;
 }
 
@@ -865,7 +866,8 @@ pst_status pst_pool_create(const pst_config* cfg, int device, pst_pool** out) {
     p->simt_wpc = std::max(1, std::min(attn_simt_max_warps(c.dtype, g), std::atoi(e)));
   if (const char* e = std::getenv("PST_SIMT_STAGES")) p->simt_stages = std::max(2, std::min(16, std::atoi(e)));
   if (const char* e = std::getenv("PST_SIMT_SMS")) p->simt_max_ctas = std::max(1, std::atoi(e));
-  while (attn_simt_smem(c.dtype, p->D, p->C, g, p->simt_stages, p->simt_wpc) > 220 * 1024) {
+  // dynamic shared memory per CTA: 227 KiB less the kernel's static part (under 1 KiB)
+  while (attn_simt_smem(c.dtype, p->D, p->C, g, p->simt_stages, p->simt_wpc) > 226 * 1024) {
     if (p->simt_stages > 2) p->simt_stages--;
     else p->simt_wpc--;
   }
@@ -897,6 +899,13 @@ pst_status pst_pool_create(const pst_config* cfg, int device, pst_pool** out) {
     if ((e = cudaEventCreateWithFlags(&p->ev_stage, cudaEventDisableTiming)) != cudaSuccess) return bail(e, "event");
     for (auto& ev : p->pev)
       if ((e = cudaEventCreate(&ev)) != cudaSuccess) return bail(e, "event");
+    // The fixed area of pst_decode_attention_noalloc belongs to a module of
+    // its own, which the CUDA runtime may load lazily, at the first use of one
+    // of its symbols.  Looking its address up here commits the area while
+    // this call allocates anyway, so the allocation-free call never triggers
+    // that load (and its allocation) itself.
+    void* scratch = nullptr;
+    if ((e = static_scratch_address(device, &scratch)) != cudaSuccess) return bail(e, "cudaGetSymbolAddress(scratch)");
     if ((e = cudaDeviceSynchronize()) != cudaSuccess) return bail(e, "cudaDeviceSynchronize");
   }
   *out = p;
@@ -1321,9 +1330,10 @@ pst_status pst_decode_attention_noalloc(pst_pool* p, const void* q, void* out, v
   if (need > kStaticScratchBytes)
     return fail(PST_ERR_INVALID, "this batch needs %zu bytes of scratch; the fixed area holds %zu", need,
                 kStaticScratchBytes);
-  void* base = nullptr;
+  void* base = nullptr;  // resolved by pst_pool_create: no module load happens here
   cudaError_t e = static_scratch_address(p->device, &base);
   if (e != cudaSuccess) return fail(PST_ERR_CUDA, "cudaGetSymbolAddress(scratch): %s", cudaGetErrorString(e));
+  p->pran[0] = p->pran[1] = p->pran[2] = false;  // no per-phase timings for this call
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* b8 = static_cast<uint8_t*>(base);
   AttnParams a = base_params(p, 0);
@@ -1349,6 +1359,7 @@ pst_status pst_decode_attention_host(pst_pool* p, const void* q_host, void* out_
   st = ensure_tables(p);
   if (st != PST_OK) return st;
   const size_t bytes = p->batch.size() * p->cfg.n_q_heads * p->D * p->es;
+  const size_t out_bytes = bytes / p->es * ((p->cfg.flags & PST_FLAG_F32_OUT) ? 4 : p->es);
   if (bytes == 0) return PST_OK;
   if (bytes > p->qo_cap) {
     CUDA_TRY(cudaStreamSynchronize(s));
@@ -1356,7 +1367,7 @@ pst_status pst_decode_attention_host(pst_pool* p, const void* q_host, void* out_
     cudaFree(p->d_out);
     p->d_q = p->d_out = nullptr;
     CUDA_TRY(cudaMalloc(&p->d_q, bytes));
-    CUDA_TRY(cudaMalloc(&p->d_out, bytes));
+    CUDA_TRY(cudaMalloc(&p->d_out, bytes / p->es * 4));  // room for fp32 rows
     p->qo_cap = bytes;
   }
   CUDA_TRY(cudaMemcpyAsync(p->d_q, q_host, bytes, cudaMemcpyHostToDevice, s));
@@ -1364,7 +1375,7 @@ pst_status pst_decode_attention_host(pst_pool* p, const void* q_host, void* out_
   // its CUDA graph until the tables change structurally
   st = pst_decode_attention_graph(p, p->d_q, p->d_out, stream);
   if (st != PST_OK) return st;
-  CUDA_TRY(cudaMemcpyAsync(out_host, p->d_out, bytes, cudaMemcpyDeviceToHost, s));
+  CUDA_TRY(cudaMemcpyAsync(out_host, p->d_out, out_bytes, cudaMemcpyDeviceToHost, s));
   CUDA_TRY(cudaStreamSynchronize(s));
   return PST_OK;
 }
@@ -1465,15 +1476,24 @@ static pst_status prefill_attention(pst_pool* p, int32_t layer, Seq& sq, int64_t
   a.n_items = n_items;
   cudaError_t e;
   a.warp_items = p->d_pre + off_warp;
+  // with profiling on, the attention kernel alone is timed: phase 0 for the
+  // tensor-core kernel, phase 1 for the CUDA-core kernel (pst_phase_times)
+  p->pran[0] = p->pran[1] = p->pran[2] = false;
+  if (!p->use_tc) CUDA_TRY(cudaMemsetAsync(p->d_sched, 0, sizeof(int32_t), s));
+  const int ph = p->use_tc ? 0 : 1;
+  if (p->profiling) CUDA_TRY(cudaEventRecord(p->pev[2 * ph], s));
   if (p->use_tc) {
     e = launch_attn_tc(p->cfg.dtype, p->D, p->C, a, n_items, s);
   } else {
-    CUDA_TRY(cudaMemsetAsync(p->d_sched, 0, sizeof(int32_t), s));
     (void)n_warps;
     e = launch_attn_simt(p->cfg.dtype, p->D, p->C, g, a, std::min<int32_t>(grid, p->n_sm), s);
     p->sched_zero = false;  // no merge follows to clear it
   }
   if (e != cudaSuccess) return fail(PST_ERR_CUDA, "prefill launch: %s", cudaGetErrorString(e));
+  if (p->profiling) {
+    CUDA_TRY(cudaEventRecord(p->pev[2 * ph + 1], s));
+    p->pran[ph] = true;
+  }
   return PST_OK;
 }
 

@@ -105,6 +105,9 @@ struct AttnParams {
   // 1: launched as a programmatic dependent of the previous kernel on the
   // stream (it may start while that kernel drains; it must not finish first)
   int32_t pdl;
+  // 1: `out` holds fp32 rows whatever the K/V type (the value before the
+  // final rounding to the K/V type; PST_FLAG_F32_OUT)
+  int32_t out_f32;
 };
 
 

@@ -23,6 +23,7 @@ PST_F16, PST_BF16, PST_F32 = 0, 1, 2
 DTYPE_CODES = {"f16": PST_F16, "bf16": PST_BF16, "f32": PST_F32}
 PST_FLAG_NO_TENSOR_CORES = 1
 PST_FLAG_CONCURRENT_PHASES = 2
+PST_FLAG_F32_OUT = 4
 MIN_SHARE_NEVER = 2**31 - 1
 
 

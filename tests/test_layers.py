@@ -10,17 +10,15 @@ graph (checked against the regular entry point); a chunked prefill written and a
 layer by layer (Chunked Prefill, sections 1-2); byte-exact read-back of all
 layers; and the refusals (rows in a shared chunk, a layer out of range).
 """
-import numpy as np
 import pytest
 import torch
 
 from oracle import attention as A
 from prefix_shared_kv_tree_gb300 import workloads as W
+from tests import parity_util as PU
 
 pytestmark = pytest.mark.gpu
 
-TOL = {"f16": 2e-3, "bf16": 2e-3, "f32": 1e-5}
-ULP_BITS = {"f16": 10, "bf16": 7, "f32": 23}
 N_LAYERS = 3
 
 
@@ -34,18 +32,7 @@ def pst():
     return mod
 
 
-def _f64(t):
-    return t.detach().float().cpu().double().numpy()
-
-
-def _check(got, want, dtype, what):
-    """Parity bound: the dtype's tolerance plus half an output ulp at |oracle|."""
-    got = _f64(got)
-    mag = np.maximum(np.abs(want), 1e-30)
-    bound = TOL[dtype] + 0.5 * 2.0 ** (np.floor(np.log2(mag)) - ULP_BITS[dtype])
-    assert np.isfinite(got).all(), f"{what}: non-finite output"
-    err = np.abs(got - want)
-    assert (err <= bound).all(), f"{what}: max err {err.max():.3e}"
+_f64 = PU.f64
 
 
 # dtype, Hq, Hkv, c: tensor-core chunk-first at c = 64 and (two tiles per chunk)
@@ -59,7 +46,8 @@ def test_layers_decode_loop_and_prefill(pst, dtype, hq, hkv, c):
     d = 64 if dtype == "f32" else 128
     dt = W.DTYPES[dtype]
     g = torch.Generator().manual_seed(40 + c)
-    pool = pst.Pool(hq, hkv, d, c, 512, dtype, 0, 0, 0, device=0, n_layers=L)
+    tw = PU.Twin(pst, hq, hkv, d, c, 512, dtype, n_layers=L)
+    pool = tw.native
 
     # a shared root of 3 full chunks + 10 tokens, four sequences with private tails
     root_n = 3 * c + 10
@@ -73,25 +61,23 @@ def test_layers_decode_loop_and_prefill(pst, dtype, hq, hkv, c):
         t[0] = 1000 + s
         k = torch.cat([root_k, torch.randn(L, tail, hkv, d, generator=g).to(dt)], dim=1)
         v = torch.cat([root_v, torch.randn(L, tail, hkv, d, generator=g).to(dt)], dim=1)
-        sid, m = pool.insert(torch.cat([root_t, t]), k.cuda(), v.cuda())
+        sid, m = tw.insert(torch.cat([root_t, t]), k.cuda(), v.cuda())
         assert m == (0 if s == 0 else 3 * c)
         kv[sid] = (k, v)
 
     def check_decode(what):
-        order = pool.batch_order()
+        order = tw.batch_order()
         for layer in range(L):
             q = torch.randn(len(order), hq, d, generator=g).to(dt).cuda()
-            out = torch.empty(len(order), hq, d, dtype=dt, device="cuda")
-            pool.decode_attention_layer(layer, q, out)
+            out, wide = tw.decode(q, "decode_attention_layer", layer)
             if layer == 0:  # the layer-free entry point reads layer 0
                 out0 = torch.empty_like(out)
                 pool.decode_attention(q, out0)
                 torch.cuda.synchronize()
                 assert torch.equal(out0, out), what
-            torch.cuda.synchronize()
             want = A.decode_attention([(_f64(kv[s][0][layer]), _f64(kv[s][1][layer])) for s in order], _f64(q))
-            _check(out, want, dtype, f"{what}, layer {layer}")
-        assert pool.check_device() == 0
+            PU.check(out, wide, want, dtype, f"layers {dtype} c{c}: {what}, layer {layer}")
+        assert tw.check_device() == 0
 
     check_decode("after insert")
 
@@ -100,7 +86,7 @@ def test_layers_decode_loop_and_prefill(pst, dtype, hq, hkv, c):
     # graph with its own q / out buffers; every sequence crosses a chunk
     # boundary on the way
     def buffers():
-        b = len(pool.batch_order())
+        b = len(tw.batch_order())
         qs = [torch.empty(b, hq, d, dtype=dt, device="cuda") for _ in range(L)]
         return qs, [torch.empty_like(x) for x in qs], torch.empty_like(qs[0])
 
@@ -108,16 +94,16 @@ def test_layers_decode_loop_and_prefill(pst, dtype, hq, hkv, c):
     seen = set()
     for step in range(c + 3):
         ids = sorted(kv)
-        pool.append_batch(ids, [7] * len(ids))
+        tw.append_batch(ids, [7] * len(ids))
         kn = torch.randn(L, len(ids), hkv, d, generator=g).to(dt)
         vn = torch.randn(L, len(ids), hkv, d, generator=g).to(dt)
         for layer in range(L):
-            pool.write_kv_last(layer, ids, kn[layer].cuda(), vn[layer].cuda())
+            tw.write_kv_last(layer, ids, kn[layer].cuda(), vn[layer].cuda())
         for i, sid in enumerate(ids):
             kv[sid] = (torch.cat([kv[sid][0], kn[:, i:i + 1]], dim=1), torch.cat([kv[sid][1], vn[:, i:i + 1]], dim=1))
         if step == 9:  # a departure: the batch shrinks, so new q / out buffers
             victim = ids[1]
-            pool.remove(victim)
+            tw.remove(victim)
             del kv[victim]
             qg, og, ref = buffers()
         for layer in range(L):
@@ -128,8 +114,8 @@ def test_layers_decode_loop_and_prefill(pst, dtype, hq, hkv, c):
             pool.decode_attention_layer(layer, qg[layer], ref)
             torch.cuda.synchronize()
             assert torch.isfinite(og[layer].float()).all(), (step, layer)
-            err = (og[layer].float() - ref.float()).abs().max().item()
-            assert err <= TOL[dtype], (step, layer, err)
+            # the same kernels on the same tables: the same bits
+            assert torch.equal(og[layer], ref), (step, layer)
         if step % 4 == 0 or step == c + 2:
             check_decode(f"decode step {step}")
     st = pool.stats()
@@ -148,7 +134,7 @@ def test_layers_decode_loop_and_prefill(pst, dtype, hq, hkv, c):
     # chunked prefill layer by layer: a new sequence matches two root chunks
     # (no K/V to write), then each block joins the tree and, per layer, gets
     # its K/V written and its rows attended
-    sid, m = pool.insert(root_t[:2 * c])
+    sid, m = tw.insert(root_t[:2 * c])
     assert m == 2 * c
     pk, pv = root_k[:, :2 * c], root_v[:, :2 * c]
     pos = 2 * c
@@ -156,20 +142,19 @@ def test_layers_decode_loop_and_prefill(pst, dtype, hq, hkv, c):
         toks = torch.randint(0, 50, (w,), generator=g, dtype=torch.int32)
         kb = torch.randn(L, w, hkv, d, generator=g).to(dt)
         vb = torch.randn(L, w, hkv, d, generator=g).to(dt)
-        pool.extend(sid, toks)
-        assert pool.seq_length(sid) == pos + w
+        tw.extend(sid, toks)
+        assert tw.seq_length(sid) == pos + w
         for layer in range(L):
-            pool.write_kv(layer, sid, kb[layer].cuda(), vb[layer].cuda())
+            tw.write_kv(layer, sid, kb[layer].cuda(), vb[layer].cuda())
             q = torch.randn(w, hq, d, generator=g).to(dt)
-            out = torch.empty(w, hq, d, dtype=dt, device="cuda")
-            pool.prefill_attend_layer(layer, sid, pos, q.cuda(), out)
+            out, wide = tw.prefill_attend_layer(layer, sid, pos, q.cuda())
             torch.cuda.synchronize()
             want = A.prefill_attention(_f64(torch.cat([pk[layer], kb[layer]])), _f64(torch.cat([pv[layer], vb[layer]])),
                                        _f64(q), pos)
-            _check(out, want, dtype, f"prefill block at {pos}, layer {layer}")
+            PU.check(out, wide, want, dtype, f"layers {dtype} c{c}: prefill block at {pos}, layer {layer}")
         pk, pv = torch.cat([pk, kb], dim=1), torch.cat([pv, vb], dim=1)
         pos += w
-    assert pool.check_device() == 0
+    assert tw.check_device() == 0
 
     # refusals: rows of shared chunks, layers out of range
     n = pool.seq_length(sid)

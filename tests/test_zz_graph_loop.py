@@ -5,20 +5,19 @@ decode step runs from a captured CUDA graph.  Appends that land in a leaf
 chunk change only device-side chunk lengths, so the graph is replayed as is;
 a new chunk, a departure or other q / out buffers change the tables or the
 pointers and make the library capture again.  Checked at every step against
-the regular entry point (within the parity tolerance) and at some steps
-against the fp64 oracle; the number of captures must equal the number of
-distinct (table version, q, out) triples the loop used.
+the regular entry point (bit for bit) and at some steps
+against the fp64 oracle (fp32 outputs of a twin pool within the parity bound,
+the pool-dtype outputs their rounding); the number of captures must equal the
+number of distinct (table version, q, out) triples the loop used.
 """
-import numpy as np
 import pytest
 import torch
 
 from oracle import attention as A
 from prefix_shared_kv_tree_gb300 import workloads as W
+from tests import parity_util as PU
 
 pytestmark = pytest.mark.gpu
-
-TOL = {"f16": 2e-3, "bf16": 2e-3}
 
 
 @pytest.fixture(scope="module")
@@ -31,8 +30,7 @@ def pst():
     return mod
 
 
-def _f64(t):
-    return t.detach().float().cpu().double().numpy()
+_f64 = PU.f64
 
 
 def _tree(seed, dtype, hkv, d, c, n_seqs):
@@ -60,46 +58,50 @@ def _tree(seed, dtype, hkv, d, c, n_seqs):
 def test_graph_decode_loop(pst, dtype, hq, hkv):
     d, c, n_seqs = 128, 64, 6
     dt = W.DTYPES[dtype]
-    pool = pst.Pool(hq, hkv, d, c, 256, dtype, 0, 0, 0, device=0)
+    tw = PU.Twin(pst, hq, hkv, d, c, 256, dtype)
+    pool = tw.native
     kv = {}
     for (t, k, v) in _tree(21, dtype, hkv, d, c, n_seqs):
-        sid, _ = pool.insert(t, k.cuda(), v.cuda())
+        sid, _ = tw.insert(t, k.cuda(), v.cuda())
         kv[sid] = (k, v)
     g = torch.Generator().manual_seed(5)
-    order = pool.batch_order()
-    q = torch.empty(len(order), hq, d, dtype=dt, device="cuda")
-    out = torch.empty_like(q)
-    ref = torch.empty_like(q)
+
+    def buffers():
+        b = len(tw.batch_order())
+        q = torch.empty(b, hq, d, dtype=dt, device="cuda")
+        return q, torch.empty_like(q), torch.empty(b, hq, d, dtype=torch.float32, device="cuda"), torch.empty_like(q)
+
+    order = tw.batch_order()
+    q, out, wide, ref = buffers()
     seen = set()
     for step in range(c + 12):
         ids = sorted(kv)
         k = torch.randn(len(ids), hkv, d, generator=g).to(dt)
         v = torch.randn(len(ids), hkv, d, generator=g).to(dt)
-        pool.append_batch(ids, [9] * len(ids), k.cuda(), v.cuda())
+        tw.append_batch(ids, [9] * len(ids), k.cuda(), v.cuda())
         for i, sid in enumerate(ids):
             kv[sid] = (torch.cat([kv[sid][0], k[i:i + 1]]), torch.cat([kv[sid][1], v[i:i + 1]]))
         if step == 30:  # a departure: the batch shrinks, so new q / out buffers
             victim = ids[len(ids) // 2]
-            pool.remove(victim)
+            tw.remove(victim)
             del kv[victim]
-            order = pool.batch_order()
-            q = torch.empty(len(order), hq, d, dtype=dt, device="cuda")
-            out = torch.empty_like(q)
-            ref = torch.empty_like(q)
+            order = tw.batch_order()
+            q, out, wide, ref = buffers()
         q.copy_(torch.randn(q.shape, generator=g).to(dt))
         out.fill_(float("nan"))
+        wide.fill_(float("nan"))
         pool.decode_attention_graph(q, out)
+        tw.wide.decode_attention_graph(q, wide)
         seen.add((pool.stats()["table_version"], q.data_ptr(), out.data_ptr()))
         pool.decode_attention(q, ref)
         torch.cuda.synchronize()
-        assert pool.check_device() == 0
+        assert tw.check_device() == 0
         assert torch.isfinite(out.float()).all(), f"step {step}"
-        err = (out.float() - ref.float()).abs().max().item()
-        assert err <= TOL[dtype], (step, err)
+        # the same kernels on the same tables: the same bits as the regular entry point
+        assert torch.equal(out, ref), f"step {step}"
         if step % 13 == 0 or step == c + 11:
             want = A.decode_attention([(_f64(kv[s][0]), _f64(kv[s][1])) for s in order], _f64(q))
-            e2 = float(np.abs(_f64(out) - want).max())
-            assert e2 <= TOL[dtype] + 0.5 * 2.0 ** (np.floor(np.log2(np.abs(want).max())) - 7), (step, e2)
+            PU.check(out, wide, want, dtype, f"graph loop {dtype} step {step}")
     st = pool.stats()
     assert st["graph_captures"] == len(seen), (st["graph_captures"], len(seen))
     assert st["graph_captures"] < c  # most steps replayed a captured graph
