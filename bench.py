@@ -46,6 +46,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-configs", action="store_true", help="skip the other workloads' step times")
     ap.add_argument("--no-prefill", action="store_true", help="skip the chunked-prefill measurement")
+    ap.add_argument("--prefill-only", action="store_true",
+                    help="print only the chunked-prefill measurement (the GQA tree's 1137-row prompt)")
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
     ap.add_argument("--min-share", type=int, default=0)
     ap.add_argument("--flags", type=int, default=0)
@@ -765,8 +767,22 @@ def run_sweep(args):
         print(json.dumps(d), flush=True)
 
 
+def run_prefill_only(args):
+    import torch
+    torch.cuda.set_device(0)
+    from prefix_shared_kv_tree_gb300 import build as B
+    B.build_library()
+    from prefix_shared_kv_tree_gb300 import pst
+    from prefix_shared_kv_tree_gb300 import workloads as W
+    res = measure_prefill(pst, W, max(1, args.steps), L2Flush(), torch.cuda.current_stream())
+    print(json.dumps({"prefill": res}), flush=True)
+
+
 def main():
     args = parse()
+    if args.prefill_only:
+        run_prefill_only(args)
+        return
     if args.impl == "reference":
         run_reference(args)
     elif args.sweep:

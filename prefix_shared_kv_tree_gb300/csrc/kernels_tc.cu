@@ -12,7 +12,7 @@
 // query rows of one KV head against a list of chunks of 64 or 128 tokens,
 // taken as tiles of 64 keys); TMEM and the mbarriers are set up once and the
 // pipelines run across item boundaries.
-// Warp roles:
+// Warp roles (384 threads):
 //   warp 0      : producer.  Lane 0 moves each tile's 32 KB K + V^T image
 //                 from the pool into a 5-stage shared-memory ring by bulk
 //                 async copy (TMA engine): one copy for a 64-token chunk; for
@@ -22,26 +22,28 @@
 //                 128-byte-swizzled K-major layout (the swizzle follows the
 //                 row index mod 8, so a 64-row part of a block is itself a
 //                 block of that layout), and Q is written in the same layout.
-//   warp 6      : gathers the next item's query rows into the other half of a
-//                 double-buffered Q tile while the current item computes.
 //   warp 1      : allocates TMEM and issues S = Q K^T (M=128, N=64, K=D) into
 //                 three TMEM buffers (two for bf16), as far ahead of the
 //                 softmax as they allow, across item boundaries.
-//   warp 7      : issues O += P V (M=128, N=D, K=64, A = P read from TMEM) into
+//   warp 2      : issues O += P V (M=128, N=D, K=64, A = P read from TMEM) into
 //                 the item's O buffer (double-buffered by item).
 //                 Both issuer warps run their loops whole; one elected lane
 //                 issues each tcgen05 instruction and commit.  Two issuers,
 //                 because one thread's stream of MMAs and commits for a chunk
 //                 takes longer than the tensor cores need for it.
-//   warps 2..5  : one thread per query row: read S from TMEM, online softmax in
-//                 log2 units against a reference max that moves only when a
-//                 chunk's max passes it by more than 2^8 (then O and the row
-//                 sum are rescaled in TMEM), write the rounded probabilities P
-//                 into TMEM as the A operand of the PV product (for bf16 also
-//                 the rounded remainders, a second PV product), and at the
-//                 item's end stream O out of TMEM: the item's partial rows
-//                 (the merge kernel combines them) or, for a prefill block, the
-//                 normalised output rows.
+//   warp 3      : gathers the next item's query rows into the other half of a
+//                 double-buffered Q tile while the current item computes.
+//   warps 4..11 : two threads per query row, each with half of the row's
+//                 keys and O columns (half-split TMEM access puts both in one
+//                 warp, so they combine by shuffles): read S from TMEM, online
+//                 softmax in log2 units against a reference max that moves
+//                 only when a chunk's max passes it by more than 2^8 (then O
+//                 and the row sum are rescaled in TMEM), write the rounded
+//                 probabilities P into TMEM as the A operand of the PV product
+//                 (for bf16 also the rounded remainders, a second PV
+//                 product), and at the item's end stream O out of TMEM: the
+//                 item's partial rows (the merge kernel combines them) or, for
+//                 a prefill block, the normalised output rows.
 // Every wait is bounded; on a timeout the CTA records an error, drains its
 // copies and MMAs, frees TMEM and exits.
 #include <cuda_bf16.h>
@@ -63,6 +65,7 @@ constexpr int kC = 64;     // tokens per chunk
 constexpr int kBM = 128;   // stacked query rows per item
 constexpr int kNS = 5;     // K/V tile stages
 constexpr int kSB = 3;     // S buffers in TMEM at most: S runs up to kSB - 1 chunks ahead of the PV product
+constexpr int kSoftmaxWarps = 8;  // warps 4..11, two threads per query row; each arrives once per barrier phase
 
 __host__ __device__ constexpr uint32_t tc_tile_bytes(int D) { return 2u * kC * D * 2u; }
 __host__ __device__ constexpr uint32_t tc_q_bytes(int D) { return kBM * D * 2u; }
@@ -82,7 +85,7 @@ __device__ __forceinline__ uint32_t pack2_plain(float a, float b) {
 }
 
 template <typename T, int D, int CP>
-__global__ void __launch_bounds__(256, 1) attn_tc_kernel(const AttnParams p) {
+__global__ void __launch_bounds__(384, 1) attn_tc_kernel(const AttnParams p) {
   constexpr uint32_t HALF = kC * D * 2;
   constexpr uint32_t TILE = tc_tile_bytes(D);
   constexpr int SUB = CP / kC;                    // 64-key tiles per pool chunk
@@ -122,11 +125,11 @@ __global__ void __launch_bounds__(256, 1) attn_tc_kernel(const AttnParams p) {
   uint64_t* qfull = bars + 2 * kNS;  // [2] Q tile written (32 Q-loader lanes)
   uint64_t* qfree = qfull + 2;       // [2] Q tile no longer read by the tensor cores
   uint64_t* sfull = qfree + 2;       // [kSB] S ready in TMEM
-  uint64_t* sfree = sfull + kSB;     // [kSB] S read by the softmax threads (128)
-  uint64_t* pfull = sfree + kSB;     // [2] P written, O rescaled if needed (128)
+  uint64_t* sfree = sfull + kSB;     // [kSB] S read by the softmax warps (8)
+  uint64_t* pfull = sfree + kSB;     // [2] P written, O rescaled if needed (8)
   uint64_t* pfree = pfull + 2;       // [2] the PV product that read P buffer b has completed
   uint64_t* ofull = pfree + 2;       // [2] every PV product of an item has completed (O buffer by item)
-  uint64_t* oempty = ofull + 2;      // [2] the item's O was read out (128)
+  uint64_t* oempty = ofull + 2;      // [2] the item's O was read out (8)
   uint64_t* done = oempty + 2;       // [2] all MMAs of the S / PV issuer completed
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -146,15 +149,15 @@ __global__ void __launch_bounds__(256, 1) attn_tc_kernel(const AttnParams p) {
     }
     for (int b = 0; b < SB; ++b) {
       ptx::mbar_init(&sfull[b], 1);
-      ptx::mbar_init(&sfree[b], 128);
+      ptx::mbar_init(&sfree[b], kSoftmaxWarps);
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(&qfull[b], 32);
       ptx::mbar_init(&qfree[b], 1);
-      ptx::mbar_init(&pfull[b], 128);
+      ptx::mbar_init(&pfull[b], kSoftmaxWarps);
       ptx::mbar_init(&pfree[b], 1);
       ptx::mbar_init(&ofull[b], 1);
-      ptx::mbar_init(&oempty[b], 128);
+      ptx::mbar_init(&oempty[b], kSoftmaxWarps);
     }
     ptx::mbar_init(&done[0], 1);
     ptx::mbar_init(&done[1], 1);
@@ -202,7 +205,7 @@ __global__ void __launch_bounds__(256, 1) attn_tc_kernel(const AttnParams p) {
         }
       }
     }
-  } else if (warp == 6) {
+  } else if (warp == 3) {
     // ---------------------------------------------------------- Q loader
     // Gathers each item's 128 query rows (zero past n_rows) into one half of
     // the double-buffered Q tile, one item ahead of the tensor cores.
@@ -239,7 +242,7 @@ __global__ void __launch_bounds__(256, 1) attn_tc_kernel(const AttnParams p) {
       ptx::fence_proxy_async_smem();
       ptx::mbar_arrive(&qfull[qb]);
     }
-  } else if (warp == 1 || warp == 7) {
+  } else if (warp == 1 || warp == 2) {
     // ---------------------------------------------------- MMA issuers (S, PV)
     // The whole warp runs its loop (operands stay warp-uniform); one elected
     // lane issues each tcgen05 instruction.
@@ -326,21 +329,32 @@ __global__ void __launch_bounds__(256, 1) attn_tc_kernel(const AttnParams p) {
         }
       }
       // Every MMA of this issuer must have finished before TMEM is released.
-      uint64_t* my_done = &done[warp == 1 ? 0 : 1];
+      uint64_t* my_done = &done[warp == 1 ? 0 : 1];  // S issuer, PV issuer
       ptx::mma_commit_warp(my_done);
       ptx::mbar_wait(my_done, 0, nullptr, p.err);
     }
     __syncwarp();
-  } else if (warp >= 2 && warp <= 5) {
+  } else if (warp >= 4) {
     // ------------------------------------------------- softmax / epilogue
-    // One thread per query row.  The item's O accumulates in TMEM; scores
-    // are exponentiated against a per-row reference max that only moves when
-    // a chunk's max exceeds it by more than kRescale (log2 units), so P stays
-    // below 2^kRescale and O (with the row sum) is rescaled rarely.
+    // Two threads per query row.  Warps 4..11 each take 16 rows: the TMEM
+    // lane quadrant is fixed by warp % 4, warps 8..11 take its upper 16
+    // lanes; with half-split TMEM access thread t holds row (t mod 16) of the
+    // warp's 16 and half hf = t div 16 of the row's columns -- keys
+    // [32 hf, 32 hf + 32) of each S tile, O columns [hf D/2, (hf + 1) D/2).
+    // The two halves of a row meet by warp shuffles (xor 16).  The item's O
+    // accumulates in TMEM; scores are exponentiated against a per-row
+    // reference max that only moves when a chunk's max exceeds it by more
+    // than kRescale (log2 units), so P stays below 2^kRescale and O (with the
+    // row sum) is rescaled rarely.
     constexpr float kRescale = 8.f;
-    const int quad = warp & 3;
-    const int r = quad * 32 + lane;
-    const uint32_t tl = tbase + (static_cast<uint32_t>(quad * 32) << 16);
+    constexpr int HK = kC / 2;  // keys of a tile per thread
+    constexpr int HD = D / 2;   // O columns per thread
+    const int quad = warp & 3, sub = (warp >> 3) & 1, hf = lane >> 4;
+    const int r = quad * 32 + sub * 16 + (lane & 15);
+    const uint32_t tl = tbase + (static_cast<uint32_t>(quad * 32 + sub * 16) << 16);
+    auto wait_all = [&](uint64_t* bar, uint32_t parity) {
+      return __all_sync(0xffffffffu, ptx::mbar_wait(bar, parity, abort_flag, p.err));
+    };
     int t = 0;
     bool ok = true;
     for (int ii = i0; ii < i1 && ok; ++ii) {
@@ -354,9 +368,10 @@ __global__ void __launch_bounds__(256, 1) attn_tc_kernel(const AttnParams p) {
         grp = w.group0 + rr / p.g;
         hg = rr % p.g;
       }
-      const int key_limit = (p.causal_p0 >= 0 && row_valid) ? p.causal_p0 + grp + 1 : INT_MAX;
+      // causal: keys of this item up to position p0 + token (item key 0 is at w.key0)
+      const int key_limit = (p.causal_p0 >= 0 && row_valid) ? p.causal_p0 + grp + 1 - w.key0 : INT_MAX;
       const int part_row = (row_valid && !p.final_mode) ? __ldg(p.row_idx + w.part_base + r) : 0;
-      float m = -INFINITY, l = 0.f;  // reference max, row sum relative to it
+      float m = -INFINITY, l = 0.f;  // reference max; this half's row sum relative to it
       int my_len = 0;
 
       for (int c = 0; c < nk; ++c, ++t) {
@@ -367,128 +382,139 @@ __global__ void __launch_bounds__(256, 1) attn_tc_kernel(const AttnParams p) {
             my_len = min(kC, max(0, cl));
           }
         }
-        const int lim = min(__shfl_sync(0xffffffffu, my_len, c & 31), key_limit - c * kC);
+        // valid keys of this thread's half of the tile
+        const int lim = min(__shfl_sync(0xffffffffu, my_len, c & 31), key_limit - c * kC) - hf * HK;
         const int b = t & 1, sb = t % SB;
-        if (!ptx::mbar_wait(&sfull[sb], (t / SB) & 1, abort_flag, p.err)) {
+        // polled now, waited for below: the answer arrives during the max
+        const bool p_ready = t < 2 || ptx::mbar_test_wait(&pfree[b], ((t - 2) >> 1) & 1);
+        if (!wait_all(&sfull[sb], (t / SB) & 1)) {
           ok = false;
           break;
         }
         ptx::tc_fence_after();
-        uint32_t sv0[32], sv1[32];
-        ptx::tmem_ld32(tl + S_COL + sb * kC, sv0);
-        ptx::tmem_ld32(tl + S_COL + sb * kC + 32, sv1);
-        ptx::tmem_ld_wait(sv0);
-        ptx::tmem_ld_wait(sv1);
+        uint32_t sv[32];
+        ptx::tmem_ld32_half<HK>(tl + S_COL + sb * kC, sv);
+        ptx::tmem_ld_wait(sv);
         ptx::tc_fence_before();
-        ptx::mbar_arrive(&sfree[sb]);
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&sfree[sb]);  // one arrival per warp
 
         // Raw scores; the chunk max is taken before scaling (the scale is
         // positive), and the scale is folded into the exponent's FMA below.
-        float x[kC];
+        float x[HK];
 #pragma unroll
-        for (int k2 = 0; k2 < kC; ++k2) x[k2] = __uint_as_float(k2 < 32 ? sv0[k2] : sv1[k2 - 32]);
-        if (lim < kC) {
+        for (int k2 = 0; k2 < HK; ++k2) x[k2] = __uint_as_float(sv[k2]);
+        if (lim < HK) {  // a partial tile (the sequence's last chunk, or the causal limit)
 #pragma unroll
-          for (int k2 = 0; k2 < kC; ++k2)
+          for (int k2 = 0; k2 < HK; ++k2)
             if (k2 >= lim) x[k2] = -INFINITY;
         }
-        float mxr = -INFINITY;
+        float mq[HK / 4];
 #pragma unroll
-        for (int k2 = 0; k2 < kC; ++k2) mxr = fmaxf(mxr, x[k2]);
+        for (int k2 = 0; k2 < HK / 4; ++k2)
+          mq[k2] = fmaxf(fmaxf(x[4 * k2], x[4 * k2 + 1]), fmaxf(x[4 * k2 + 2], x[4 * k2 + 3]));
+#pragma unroll
+        for (int w2 = HK / 8; w2 >= 1; w2 >>= 1)
+#pragma unroll
+          for (int k2 = 0; k2 < w2; ++k2) mq[k2] = fmaxf(mq[k2], mq[k2 + w2]);
+        const float mxr = fmaxf(mq[0], __shfl_xor_sync(0xffffffffu, mq[0], 16));  // the row's other half
         const float mx = mxr * p.scale_log2;
         // Move the reference max: always on the item's first chunk (nothing
         // accumulated yet); later only when this chunk's max runs past it.
+        // Both halves of a row take the same decision.
         const bool move = (c == 0) || (mx > m + kRescale);
         const float m_old_use = (m == -INFINITY) ? 0.f : m;
         if (move) m = fmaxf(m, mx);
         const float m_use = (m == -INFINITY) ? 0.f : m;
         if (c > 0 && __any_sync(0xffffffffu, move)) {
           // O so far (through chunk c-1) and l get the factor 2^(old - new):
-          // wait for that chunk's PV product, then rescale in place.
+          // wait for that chunk's PV product, then rescale this half in place.
           const float alpha = move ? ptx::ex2(m_old_use - m_use) : 1.f;
-          if (!ptx::mbar_wait(&pfree[(t - 1) & 1], ((t - 1) >> 1) & 1, abort_flag, p.err)) {
+          if (!wait_all(&pfree[(t - 1) & 1], ((t - 1) >> 1) & 1)) {
             ok = false;
             break;
           }
           ptx::tc_fence_after();
 #pragma unroll
-          for (int cg = 0; cg < D / 32; ++cg) {
+          for (int cg = 0; cg < HD / 32; ++cg) {
             uint32_t ov[32];
-            ptx::tmem_ld32(tl + O_COL + ob * D + 32 * cg, ov);
+            ptx::tmem_ld32_half<HD>(tl + O_COL + ob * D + 32 * cg, ov);
             ptx::tmem_ld_wait(ov);
 #pragma unroll
             for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
-            ptx::tmem_st32(tl + O_COL + ob * D + 32 * cg, ov);
+            ptx::tmem_st32_half<HD>(tl + O_COL + ob * D + 32 * cg, ov);
           }
           ptx::tmem_st_wait();
           l *= alpha;
         }
         // P buffer b is free once the PV product of chunk t-2 has completed.
-        if (t >= 2 && !ptx::mbar_wait(&pfree[b], ((t - 2) >> 1) & 1, abort_flag, p.err)) {
+        if (__any_sync(0xffffffffu, !p_ready) && !wait_all(&pfree[b], ((t - 2) >> 1) & 1)) {
           ok = false;
           break;
         }
         // P = 2^(x * scale - m), rounded to the operand type (bf16: plus the
-        // rounded remainder); the row sum adds the rounded values the PV
-        // product reads (so o / n stays a weighted mean of V rows), in two
-        // partial sums for a shorter chain.
+        // rounded remainder); the row sum adds the values the PV product reads
+        // (so o / n stays a weighted mean of V rows): the rounded ones for
+        // fp16, for bf16 the unrounded ones, which hi + lo matches to 2^-17.
+        // Four partial sums for a shorter chain.
         const float neg_m = -m_use, sc = p.scale_log2;
-        float ps0 = 0.f, ps1 = 0.f;
-        uint32_t pw[kC / 2], pr[PSPLIT ? kC / 2 : 1];
+        float ps[4] = {0.f, 0.f, 0.f, 0.f};
+        uint32_t pw[HK / 2], pr[HK / 2];  // pr: the remainders (bf16 only)
 #pragma unroll
-        for (int j = 0; j < CCH; ++j) {
+        for (int j = 0; j < HK / 8; ++j) {
           float e[8];
 #pragma unroll
           for (int q = 0; q < 8; ++q) e[q] = ptx::ex2(fmaf(x[8 * j + q], sc, neg_m));
 #pragma unroll
           for (int q = 0; q < 4; ++q) pw[4 * j + q] = pack2_plain<T>(e[2 * q], e[2 * q + 1]);
           if constexpr (PSPLIT) {
-            float h[8];
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-              h[2 * q] = lo16<T>(pw[4 * j + q]);
-              h[2 * q + 1] = hi16<T>(pw[4 * j + q]);
-              pr[4 * j + q] = pack2_plain<T>(e[2 * q] - h[2 * q], e[2 * q + 1] - h[2 * q + 1]);
+              const float h0 = lo16<T>(pw[4 * j + q]), h1 = hi16<T>(pw[4 * j + q]);
+              pr[4 * j + q] = pack2_plain<T>(e[2 * q] - h0, e[2 * q + 1] - h1);
+              ps[q] += e[2 * q] + e[2 * q + 1];
             }
-            ps0 += (h[0] + h[1]) + (h[2] + h[3]) + sum2_16<T>(pr[4 * j]) + sum2_16<T>(pr[4 * j + 1]);
-            ps1 += (h[4] + h[5]) + (h[6] + h[7]) + sum2_16<T>(pr[4 * j + 2]) + sum2_16<T>(pr[4 * j + 3]);
           } else {
-            ps0 += sum2_16<T>(pw[4 * j]) + sum2_16<T>(pw[4 * j + 1]);
-            ps1 += sum2_16<T>(pw[4 * j + 2]) + sum2_16<T>(pw[4 * j + 3]);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) ps[q] += sum2_16<T>(pw[4 * j + q]);
           }
         }
-        const float psum = ps0 + ps1;
-        ptx::tmem_st32(tl + P_COL + b * PW, pw);
-        if constexpr (PSPLIT) ptx::tmem_st32(tl + P_COL + b * PW + 32, pr);
+        // this half's 32 keys are P columns [16 hf, 16 hf + 16) (two keys per column)
+        ptx::tmem_st16_half<HK / 2>(tl + P_COL + b * PW, pw);
+        if constexpr (PSPLIT) ptx::tmem_st16_half<HK / 2>(tl + P_COL + b * PW + 32, pr);
         ptx::tmem_st_wait();
         ptx::tc_fence_before();  // orders the TMEM stores above before the PV product
-        ptx::mbar_arrive(&pfull[b]);
-        l += psum;
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&pfull[b]);  // one arrival per warp
+        l += (ps[0] + ps[1]) + (ps[2] + ps[3]);
       }
       if (!ok) break;
 
       // ---- the item's O: wait for its last PV product, then write out
-      if (!ptx::mbar_wait(&ofull[ob], (it >> 1) & 1, abort_flag, p.err)) ok = false;
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) break;
+      if (!wait_all(&ofull[ob], (it >> 1) & 1)) {
+        ok = false;
+        break;
+      }
       ptx::tc_fence_after();
-      const float inv = 1.f / l;
+      const float lrow = l + __shfl_xor_sync(0xffffffffu, l, 16);  // the row sum of both halves
+      const float inv = 1.f / lrow;
       const size_t out_row = (static_cast<size_t>(grp) * p.Hq + w.kv * p.g + hg) * D;
-      float4* po = reinterpret_cast<float4*>(p.part_o + static_cast<size_t>(part_row) * D);
+      float* po = p.part_o + static_cast<size_t>(part_row) * D;
 #pragma unroll
-      for (int cg = 0; cg < D / 32; ++cg) {
+      for (int cg = 0; cg < HD / 32; ++cg) {
         uint32_t ov[32];
-        ptx::tmem_ld32(tl + O_COL + ob * D + 32 * cg, ov);
+        ptx::tmem_ld32_half<HD>(tl + O_COL + ob * D + 32 * cg, ov);
         ptx::tmem_ld_wait(ov);
+        const int col = hf * HD + 32 * cg;  // first O column of this load
         if (row_valid) {
           if (p.final_mode && p.out_f32) {
-            float4* o4 = reinterpret_cast<float4*>(static_cast<float*>(p.out) + out_row + 32 * cg);
+            float4* o4 = reinterpret_cast<float4*>(static_cast<float*>(p.out) + out_row + col);
 #pragma unroll
             for (int j = 0; j < 8; ++j)
               o4[j] = make_float4(__uint_as_float(ov[4 * j]) * inv, __uint_as_float(ov[4 * j + 1]) * inv,
                                   __uint_as_float(ov[4 * j + 2]) * inv, __uint_as_float(ov[4 * j + 3]) * inv);
           } else if (p.final_mode) {
-            T* out = static_cast<T*>(p.out) + out_row;
+            T* out = static_cast<T*>(p.out) + out_row + col;
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
               const float* o8 = reinterpret_cast<const float*>(ov) + 8 * j;
@@ -497,19 +523,22 @@ __global__ void __launch_bounds__(256, 1) attn_tc_kernel(const AttnParams p) {
               pk.y = pack2_plain<T>(o8[2] * inv, o8[3] * inv);
               pk.z = pack2_plain<T>(o8[4] * inv, o8[5] * inv);
               pk.w = pack2_plain<T>(o8[6] * inv, o8[7] * inv);
-              *reinterpret_cast<uint4*>(out + 32 * cg + 8 * j) = pk;
+              *reinterpret_cast<uint4*>(out + 8 * j) = pk;
             }
           } else {
+            float4* o4 = reinterpret_cast<float4*>(po + col);
 #pragma unroll
             for (int j = 0; j < 8; ++j)
-              po[8 * cg + j] = make_float4(__uint_as_float(ov[4 * j]), __uint_as_float(ov[4 * j + 1]),
-                                           __uint_as_float(ov[4 * j + 2]), __uint_as_float(ov[4 * j + 3]));
+              o4[j] = make_float4(__uint_as_float(ov[4 * j]), __uint_as_float(ov[4 * j + 1]),
+                                  __uint_as_float(ov[4 * j + 2]), __uint_as_float(ov[4 * j + 3]));
           }
         }
       }
       ptx::tc_fence_before();
-      ptx::mbar_arrive(&oempty[ob]);
-      if (row_valid && !p.final_mode) reinterpret_cast<float2*>(p.part_ml)[part_row] = make_float2(m, l);
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&oempty[ob]);  // one arrival per warp
+      if (row_valid && !p.final_mode && hf == 0)
+        reinterpret_cast<float2*>(p.part_ml)[part_row] = make_float2(m, lrow);
     }
   }
 
@@ -534,7 +563,7 @@ cudaError_t launch_tc_t(const AttnParams& p, int grid, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(256);
+  cfg.blockDim = dim3(384);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];

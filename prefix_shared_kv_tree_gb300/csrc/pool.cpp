@@ -189,6 +189,11 @@ struct pst_pool {
   bool sched_zero = true;
   int32_t* d_pre = nullptr;
   size_t pre_cap = 0;
+  // partial rows of a tensor-core prefill block cut along the keys
+  float* d_ppart_o = nullptr;
+  float* d_ppart_ml = nullptr;
+  size_t ppart_cap = 0;  // rows
+  bool split_prefill = true;
   int32_t* h_stage = nullptr;  // pinned upload staging
   size_t stage_cap = 0;
   cudaEvent_t ev_stage = nullptr;
@@ -852,6 +857,7 @@ pst_status pst_pool_create(const pst_config* cfg, int device, pst_pool** out) {
   if (const char* e = std::getenv("PST_TC_MAX_RUN")) p->tc_max_run = std::max(2, std::atoi(e));
   if (const char* e = std::getenv("PST_MERGE_CAP")) p->merge_cap_forced = std::max(0, std::atoi(e));
   if (const char* e = std::getenv("PST_SIMT_TAIL")) p->simt_tail = std::max(0.0, std::atof(e));
+  if (const char* e = std::getenv("PST_SPLIT_PREFILL")) p->split_prefill = std::atoi(e) != 0;
   // Sequence-first kernel shape: up to 8 consumer warps (plus the producer
   // warp) x up to 6 stages of 8 KB pieces, as far as shared memory allows
   p->simt_wpc = attn_simt_max_warps(c.dtype, g);
@@ -925,6 +931,8 @@ pst_status pst_pool_free(pst_pool* p) {
     cudaFree(p->d_err);
     cudaFree(p->d_sched);
     cudaFree(p->d_pre);
+    cudaFree(p->d_ppart_o);
+    cudaFree(p->d_ppart_ml);
     cudaFree(p->d_q);
     cudaFree(p->d_out);
     if (p->h_stage) cudaFreeHost(p->h_stage);
@@ -1422,77 +1430,205 @@ static pst_status append_block(pst_pool* p, int64_t seq_id, Seq& sq, const int32
 // Causal attention of the W query rows at positions [p0, p0 + W) of sequence
 // sq over its keys [0, p0 + r] in layer `layer` (Chunked Prefill, sections
 // 1-2), normalised rows into out.
-static pst_status prefill_attention(pst_pool* p, int32_t layer, Seq& sq, int64_t p0, int64_t W, const void* q,
-                                    void* out, cudaStream_t s) {
-  pst_status st = PST_OK;
-  // work: the sequence's chunk list, then one item per (KV head, row tile)
-  std::vector<int32_t> tab;
-  for (int32_t id : sq.path) tab.push_back(p->nodes[id].chunk);
+// Causal attention of a W-row block on the tensor-core kernel.  Items are
+// (KV head, 128-row tile) over keys [0, p0 + last token of the tile].  When
+// those items are too few to keep the SMs busy, each is cut
+// along the keys into pieces of about T / (2 #SMs) 64-key tiles (T: all
+// tiles of the block); the pieces write (o, m, n) partial rows, grouped per
+// (token, KV head) in key order, and the merge kernel combines them
+// (attn_reduce, then O = o / n; ChunkAttention, Knowl 3) into out.  Pieces
+// go to CTAs longest first, each to the least-loaded CTA.
+static pst_status prefill_attention_tc(pst_pool* p, const AttnParams& base, const std::vector<int32_t>& path_chunks,
+                                       int64_t p0, int64_t W, cudaStream_t s) {
+  const int g = p->g, Hkv = p->cfg.n_kv_heads, C = p->C;
+  const int32_t sub = C / 64;  // 64-key tiles per chunk
+  const int64_t rows = W * g;
+  struct Tile {
+    int32_t kv, r0, n_rows, n_ch, nsplit;
+  };
+  std::vector<Tile> tiles;
+  int64_t T = 0;
+  for (int kv = 0; kv < Hkv; ++kv)
+    for (int64_t r0 = 0; r0 < rows; r0 += 128) {
+      const int32_t n_rows = static_cast<int32_t>(std::min<int64_t>(128, rows - r0));
+      const int64_t t_last = (r0 + n_rows - 1) / g;
+      const int32_t n_ch = static_cast<int32_t>(ceil_div(p0 + t_last + 1, C));
+      tiles.push_back({kv, static_cast<int32_t>(r0), n_rows, n_ch, 1});
+      T += static_cast<int64_t>(n_ch) * sub;
+    }
+  // pieces of about T / (2 #SMs) tiles, at least kMinPiece, when the items
+  // would leave at least half of the SMs idle (measured on the GQA tree's
+  // prompt: with 128 items on 152 SMs the pieces' partial rows and the merge
+  // cost more than the idle SMs; with 32 items cutting them pays)
+  constexpr int64_t kMinPiece = 6;
+  const int64_t piece = std::max<int64_t>(kMinPiece, ceil_div(T, 2 * std::max(1, p->n_sm)));
+  int64_t n_pieces = 0;
+  const bool split = p->split_prefill && 2 * static_cast<int64_t>(tiles.size()) <= p->n_sm;
+  for (auto& t : tiles) {
+    if (split) t.nsplit = static_cast<int32_t>(std::max<int64_t>(1, std::min<int64_t>(t.n_ch, (t.n_ch * sub + piece / 2) / piece)));
+    n_pieces += t.nsplit;
+  }
+
+  // table image: chunk ids, items, per-CTA item ranges, merge CSR, row map
+  std::vector<int32_t> tab(path_chunks);
   while (tab.size() % 8) tab.push_back(0);
   const size_t off_items = tab.size();
-  const int g = p->g, Hkv = p->cfg.n_kv_heads;
-  const int64_t rows = W * g;
-  std::vector<int32_t> warp_items;
-  int32_t n_items = 0;
-  if (p->use_tc) {
-    for (int kv = 0; kv < Hkv; ++kv)
-      for (int64_t r0 = 0; r0 < rows; r0 += 128) {
-        WorkItem w{};
-        w.chunk_off = 0;
-        w.kv = kv;
-        w.group0 = 0;
-        w.row0 = static_cast<int32_t>(r0);
-        w.n_rows = static_cast<int32_t>(std::min<int64_t>(128, rows - r0));
-        const int64_t t_last = (r0 + w.n_rows - 1) / g;
-        w.n_chunks = static_cast<int32_t>(ceil_div(p0 + t_last + 1, p->C));
-        push_item(tab, w);
-        ++n_items;
-      }
-  } else {
-    const std::vector<int32_t> ids(tab.begin(), tab.begin() + off_items);
-    for (int64_t t = 0; t < W; ++t)
-      for (int kv = 0; kv < Hkv; ++kv) {
-        push_simt_item(tab, ids, 0, static_cast<int32_t>(ceil_div(p0 + t + 1, p->C)), kv, static_cast<int32_t>(t), 0);
-        ++n_items;
-      }
+  std::vector<WorkItem> items;
+  items.reserve(n_pieces);
+  std::vector<int32_t> moff, row_idx;
+  if (split) {
+    moff.assign(static_cast<size_t>(W) * Hkv + 1, 0);
+    for (const auto& t : tiles)
+      for (int32_t r = 0; r < t.n_rows; r += g) moff[static_cast<size_t>((t.r0 + r) / g) * Hkv + t.kv + 1] = t.nsplit;
+    for (size_t x = 1; x < moff.size(); ++x) moff[x] += moff[x - 1];
   }
+  for (const auto& t : tiles) {
+    for (int32_t sp = 0; sp < t.nsplit; ++sp) {
+      const int32_t c0 = static_cast<int32_t>(static_cast<int64_t>(sp) * t.n_ch / t.nsplit);
+      const int32_t c1 = static_cast<int32_t>(static_cast<int64_t>(sp + 1) * t.n_ch / t.nsplit);
+      WorkItem w{};
+      w.chunk_off = c0;
+      w.n_chunks = c1 - c0;
+      w.kv = t.kv;
+      w.group0 = 0;
+      w.row0 = t.r0;
+      w.n_rows = t.n_rows;
+      w.key0 = c0 * C;
+      if (split) {
+        w.part_base = static_cast<int32_t>(row_idx.size());
+        for (int32_t r = 0; r < t.n_rows; ++r) {
+          const int32_t tok = (t.r0 + r) / g, hg = (t.r0 + r) % g;
+          row_idx.push_back((moff[static_cast<size_t>(tok) * Hkv + t.kv] + sp) * g + hg);
+        }
+      }
+      items.push_back(w);
+    }
+  }
+  // pieces to CTAs: longest first, each to the least-loaded CTA
+  const int32_t n = static_cast<int32_t>(items.size());
+  const int32_t k = std::max<int32_t>(1, std::min<int32_t>(p->n_sm, n));
+  std::vector<int32_t> order(n);
+  for (int32_t x = 0; x < n; ++x) order[x] = x;
+  std::stable_sort(order.begin(), order.end(), [&](int32_t x, int32_t y) { return items[x].n_chunks > items[y].n_chunks; });
+  std::vector<std::pair<int64_t, int32_t>> heap(k);
+  for (int32_t c = 0; c < k; ++c) heap[c] = {0, c};
+  std::vector<int32_t> cta_of(n), count(k + 1, 0);
+  for (int32_t x : order) {
+    std::pop_heap(heap.begin(), heap.end(), std::greater<>());
+    cta_of[x] = heap.back().second;
+    heap.back().first += items[x].n_chunks + 2;  // + the item's set-up and write-out, in chunk units
+    ++count[heap.back().second + 1];
+    std::push_heap(heap.begin(), heap.end(), std::greater<>());
+  }
+  for (int32_t c = 0; c < k; ++c) count[c + 1] += count[c];
+  std::vector<int32_t> at(count.begin(), count.end() - 1);
+  std::vector<WorkItem> sorted(n);
+  for (int32_t x : order) sorted[at[cta_of[x]]++] = items[x];
+  for (const auto& w : sorted) push_item(tab, w);
   const size_t off_warp = tab.size();
-  int32_t grid = 0, n_warps = 0;
-  if (!p->use_tc) {
-    n_warps = n_items;
-    grid = static_cast<int32_t>(ceil_div(n_warps, p->simt_wpc));
-  }
-  for (int32_t x = 0; x <= n_items; ++x) tab.push_back(x);  // one item per warp (CUDA cores) or CTA (tensor cores)
-  st = upload(p, &p->d_pre, &p->pre_cap, tab, s);
+  tab.insert(tab.end(), count.begin(), count.end());
+  const size_t off_moff = tab.size();
+  tab.insert(tab.end(), moff.begin(), moff.end());
+  const size_t off_rows = tab.size();
+  tab.insert(tab.end(), row_idx.begin(), row_idx.end());
+  pst_status st = upload(p, &p->d_pre, &p->pre_cap, tab, s);
   if (st != PST_OK) return st;
 
+  AttnParams a = base;
+  a.chunks = p->d_pre;
+  a.items = reinterpret_cast<const WorkItem*>(p->d_pre + off_items);
+  a.n_items = n;
+  a.warp_items = p->d_pre + off_warp;
+  int32_t merge_cap = 0;
+  if (split) {
+    const size_t part_rows = static_cast<size_t>(moff.back()) * g;
+    if (part_rows > p->ppart_cap) {
+      if (p->d_ppart_o) {
+        CUDA_TRY(cudaStreamSynchronize(s));
+        CUDA_TRY(cudaFree(p->d_ppart_o));
+        CUDA_TRY(cudaFree(p->d_ppart_ml));
+        p->d_ppart_o = p->d_ppart_ml = nullptr;
+        p->ppart_cap = 0;
+      }
+      const size_t cap = std::max<size_t>(part_rows * 3 / 2, 4096);
+      CUDA_TRY(cudaMalloc(&p->d_ppart_o, cap * p->D * sizeof(float)));
+      CUDA_TRY(cudaMalloc(&p->d_ppart_ml, cap * 2 * sizeof(float)));
+      p->ppart_cap = cap;
+    }
+    a.final_mode = 0;
+    a.part_o = p->d_ppart_o;
+    a.part_ml = p->d_ppart_ml;
+    a.m_off = p->d_pre + off_moff;
+    a.row_idx = p->d_pre + off_rows;
+    int32_t max_ent = 0;
+    for (const auto& t : tiles) max_ent = std::max(max_ent, t.nsplit);
+    const int32_t by_smem = static_cast<int32_t>((64 * 1024) / (4 * static_cast<size_t>(g) * p->D * sizeof(float)));
+    merge_cap = std::min({max_ent, by_smem, 32 / g});
+  }
+  if (p->profiling) CUDA_TRY(cudaEventRecord(p->pev[0], s));
+  cudaError_t e = launch_attn_tc(p->cfg.dtype, p->D, p->C, a, k, s);
+  if (e != cudaSuccess) return fail(PST_ERR_CUDA, "prefill launch: %s", cudaGetErrorString(e));
+  if (split) {
+    AttnParams am = a;
+    am.final_mode = 1;
+    am.pdl = 1;  // a programmatic dependent of the attention kernel: waits for its partial rows
+    am.merge_cap = merge_cap;
+    am.sched = nullptr;
+    e = launch_merge(p->cfg.dtype, p->D, am, static_cast<int32_t>(W), s);
+    if (e != cudaSuccess) return fail(PST_ERR_CUDA, "prefill merge launch: %s", cudaGetErrorString(e));
+  }
+  if (p->profiling) {
+    CUDA_TRY(cudaEventRecord(p->pev[1], s));
+    p->pran[0] = true;
+  }
+  return PST_OK;
+}
+
+// Causal attention of the W query rows at positions [p0, p0 + W) of sequence
+// sq over its keys [0, p0 + r] in layer `layer` (Chunked Prefill, sections
+// 1-2), normalised rows into out.
+static pst_status prefill_attention(pst_pool* p, int32_t layer, Seq& sq, int64_t p0, int64_t W, const void* q,
+                                    void* out, cudaStream_t s) {
   AttnParams a = base_params(p, layer);
   a.q = q;
   a.out = out;
   a.final_mode = 1;
   a.causal_p0 = static_cast<int32_t>(p0);
+  p->pran[0] = p->pran[1] = p->pran[2] = false;
+  std::vector<int32_t> path_chunks;
+  for (int32_t id : sq.path) path_chunks.push_back(p->nodes[id].chunk);
+  if (p->use_tc) return prefill_attention_tc(p, a, path_chunks, p0, W, s);
+
+  // CUDA cores: one item per (token, KV head) over keys [0, p0 + t], one warp each
+  std::vector<int32_t> tab(path_chunks);
+  while (tab.size() % 8) tab.push_back(0);
+  const size_t off_items = tab.size();
+  const int g = p->g, Hkv = p->cfg.n_kv_heads;
+  int32_t n_items = 0;
+  for (int64_t t = 0; t < W; ++t)
+    for (int kv = 0; kv < Hkv; ++kv) {
+      push_simt_item(tab, path_chunks, 0, static_cast<int32_t>(ceil_div(p0 + t + 1, p->C)), kv, static_cast<int32_t>(t),
+                     0);
+      ++n_items;
+    }
+  const size_t off_warp = tab.size();
+  const int32_t grid = static_cast<int32_t>(ceil_div(n_items, p->simt_wpc));
+  for (int32_t x = 0; x <= n_items; ++x) tab.push_back(x);
+  pst_status st = upload(p, &p->d_pre, &p->pre_cap, tab, s);
+  if (st != PST_OK) return st;
   a.chunks = p->d_pre;
   a.items = reinterpret_cast<const WorkItem*>(p->d_pre + off_items);
   a.n_items = n_items;
-  cudaError_t e;
   a.warp_items = p->d_pre + off_warp;
-  // with profiling on, the attention kernel alone is timed: phase 0 for the
-  // tensor-core kernel, phase 1 for the CUDA-core kernel (pst_phase_times)
-  p->pran[0] = p->pran[1] = p->pran[2] = false;
-  if (!p->use_tc) CUDA_TRY(cudaMemsetAsync(p->d_sched, 0, sizeof(int32_t), s));
-  const int ph = p->use_tc ? 0 : 1;
-  if (p->profiling) CUDA_TRY(cudaEventRecord(p->pev[2 * ph], s));
-  if (p->use_tc) {
-    e = launch_attn_tc(p->cfg.dtype, p->D, p->C, a, n_items, s);
-  } else {
-    (void)n_warps;
-    e = launch_attn_simt(p->cfg.dtype, p->D, p->C, g, a, std::min<int32_t>(grid, p->n_sm), s);
-    p->sched_zero = false;  // no merge follows to clear it
-  }
+  // with profiling on, the attention kernel alone is timed: phase 1 (pst_phase_times)
+  CUDA_TRY(cudaMemsetAsync(p->d_sched, 0, sizeof(int32_t), s));
+  if (p->profiling) CUDA_TRY(cudaEventRecord(p->pev[2], s));
+  const cudaError_t e = launch_attn_simt(p->cfg.dtype, p->D, p->C, g, a, std::min<int32_t>(grid, p->n_sm), s);
+  p->sched_zero = false;  // no merge follows to clear it
   if (e != cudaSuccess) return fail(PST_ERR_CUDA, "prefill launch: %s", cudaGetErrorString(e));
   if (p->profiling) {
-    CUDA_TRY(cudaEventRecord(p->pev[2 * ph + 1], s));
-    p->pran[ph] = true;
+    CUDA_TRY(cudaEventRecord(p->pev[3], s));
+    p->pran[1] = true;
   }
   return PST_OK;
 }
