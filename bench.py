@@ -727,7 +727,8 @@ def run_ours(args):
                 "h2d_bytes_per_step": qbytes, "d2h_bytes_per_step": qbytes},
         "gpu_launches": launches,
         "clocks": clk,
-        "pool": {k: st[k] for k in ("used_chunks", "shared_chunks", "phase1_items", "phase2_items", "partial_rows")},
+        "pool": {k: st[k] for k in ("used_chunks", "shared_chunks", "phase1_items", "phase2_items", "partial_rows",
+                                    "phase1_ctas", "phase2_ctas", "simt_first")},
         "decode_loop": loop,
         "configs": configs,
         "prefill": prefill,

@@ -105,6 +105,9 @@ typedef struct {
   int64_t phase2_items;    /* work items of the last build (sequence-first) */
   int64_t partial_rows;    /* (o, m, n) partial rows of the last build */
   int64_t graph_captures;  /* decode steps captured by pst_decode_attention_graph */
+  int64_t phase1_ctas;     /* CTAs of the chunk-first kernel in the last build's decode step */
+  int64_t phase2_ctas;     /* CTAs of the sequence-first kernel in the last build's decode step */
+  int64_t simt_first;      /* 1: the last build's decode step launches the sequence-first kernel first */
 } pst_stats_t;
 
 /* Create a pool.  device >= 0: CUDA device ordinal; the pool allocates its

@@ -12,7 +12,7 @@
 // query rows of one KV head against a list of chunks of 64 or 128 tokens,
 // taken as tiles of 64 keys); TMEM and the mbarriers are set up once and the
 // pipelines run across item boundaries.
-// Warp roles (384 threads):
+// Warp roles (512 threads):
 //   warp 0      : producer.  Lane 0 moves each tile's 32 KB K + V^T image
 //                 from the pool into a 5-stage shared-memory ring by bulk
 //                 async copy (TMA engine): one copy for a 64-token chunk; for
@@ -41,9 +41,13 @@
 //                 and the row sum are rescaled in TMEM), write the rounded
 //                 probabilities P into TMEM as the A operand of the PV product
 //                 (for bf16 also the rounded remainders, a second PV
-//                 product), and at the item's end stream O out of TMEM: the
-//                 item's partial rows (the merge kernel combines them) or, for
-//                 a prefill block, the normalised output rows.
+//                 product); at an item's end they leave the row max and sum in
+//                 shared memory and go on with the next item.
+//   warps 12..15: epilogue, one thread per query row: stream each item's O
+//                 out of TMEM (double-buffered by item) once its last PV
+//                 product has completed: the item's partial rows (the merge
+//                 kernel combines them) or, for a prefill block, the
+//                 normalised output rows.
 // Every wait is bounded; on a timeout the CTA records an error, drains its
 // copies and MMAs, frees TMEM and exits.
 #include <cuda_bf16.h>
@@ -65,12 +69,13 @@ constexpr int kC = 64;     // tokens per chunk
 constexpr int kBM = 128;   // stacked query rows per item
 constexpr int kNS = 5;     // K/V tile stages
 constexpr int kSB = 3;     // S buffers in TMEM at most: S runs up to kSB - 1 chunks ahead of the PV product
-constexpr int kSoftmaxWarps = 8;  // warps 4..11, two threads per query row; each arrives once per barrier phase
+constexpr int kSoftmaxWarps = 8;   // warps 4..11, two threads per query row; each arrives once per barrier phase
+constexpr int kEpilogueWarps = 4;  // warps 12..15, one thread per query row
 
 __host__ __device__ constexpr uint32_t tc_tile_bytes(int D) { return 2u * kC * D * 2u; }
 __host__ __device__ constexpr uint32_t tc_q_bytes(int D) { return kBM * D * 2u; }
 __host__ __device__ constexpr size_t tc_smem_bytes(int D) {
-  return 1024 + 2 * tc_q_bytes(D) + kNS * tc_tile_bytes(D) + 320;
+  return 2 * tc_q_bytes(D) + kNS * tc_tile_bytes(D) + 320 + 2 * kBM * 8;
 }
 
 template <typename T>
@@ -85,7 +90,7 @@ __device__ __forceinline__ uint32_t pack2_plain(float a, float b) {
 }
 
 template <typename T, int D, int CP>
-__global__ void __launch_bounds__(384, 1) attn_tc_kernel(const AttnParams p) {
+__global__ void __launch_bounds__(512, 1) attn_tc_kernel(const AttnParams p) {
   constexpr uint32_t HALF = kC * D * 2;
   constexpr uint32_t TILE = tc_tile_bytes(D);
   constexpr int SUB = CP / kC;                    // 64-key tiles per pool chunk
@@ -115,8 +120,16 @@ __global__ void __launch_bounds__(384, 1) attn_tc_kernel(const AttnParams p) {
   constexpr uint32_t ID_S = ptx::idesc_f16(kBM, kC, BF);
   constexpr uint32_t ID_O = ptx::idesc_f16(kBM, D, BF);
 
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // The swizzled tiles need 1024-byte alignment; the dynamic shared memory
+  // of this kernel (which has no static shared memory) starts there.  A base
+  // that is not aligned is reported and nothing is touched.
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  if (ptx::smem_u32(smem_raw) & 1023u) {
+    if (threadIdx.x == 0) atomicOr(p.err, kErrBadIndex);
+    if (p.pdl) ptx::pdl_wait();
+    return;
+  }
+  uint8_t* smem = smem_raw;
   uint8_t* qs = smem;                 // [2] Q tiles
   uint8_t* kvs = qs + 2 * QB;         // [kNS] K + V^T tiles
   uint64_t* bars = reinterpret_cast<uint64_t*>(kvs + kNS * TILE);
@@ -129,9 +142,11 @@ __global__ void __launch_bounds__(384, 1) attn_tc_kernel(const AttnParams p) {
   uint64_t* pfull = sfree + kSB;     // [2] P written, O rescaled if needed (8)
   uint64_t* pfree = pfull + 2;       // [2] the PV product that read P buffer b has completed
   uint64_t* ofull = pfree + 2;       // [2] every PV product of an item has completed (O buffer by item)
-  uint64_t* oempty = ofull + 2;      // [2] the item's O was read out (8)
-  uint64_t* done = oempty + 2;       // [2] all MMAs of the S / PV issuer completed
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 2);
+  uint64_t* oempty = ofull + 2;      // [2] the item's O was read out (4 epilogue warps)
+  uint64_t* mlfull = oempty + 2;     // [2] the item's row max and sum are in ml_buf (8 softmax warps)
+  uint64_t* done = mlfull + 2;       // [2] all MMAs of the S / PV issuer completed
+  float2* ml_buf = reinterpret_cast<float2*>(done + 2);  // [2][kBM] (m, n) of each row, by O buffer
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ml_buf + 2 * kBM);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* issued_slot = abort_flag + 1;
   volatile int* consumed_slot = abort_flag + 2;
@@ -157,7 +172,8 @@ __global__ void __launch_bounds__(384, 1) attn_tc_kernel(const AttnParams p) {
       ptx::mbar_init(&pfull[b], kSoftmaxWarps);
       ptx::mbar_init(&pfree[b], 1);
       ptx::mbar_init(&ofull[b], 1);
-      ptx::mbar_init(&oempty[b], kSoftmaxWarps);
+      ptx::mbar_init(&oempty[b], kEpilogueWarps);
+      ptx::mbar_init(&mlfull[b], kSoftmaxWarps);
     }
     ptx::mbar_init(&done[0], 1);
     ptx::mbar_init(&done[1], 1);
@@ -208,38 +224,27 @@ __global__ void __launch_bounds__(384, 1) attn_tc_kernel(const AttnParams p) {
   } else if (warp == 3) {
     // ---------------------------------------------------------- Q loader
     // Gathers each item's 128 query rows (zero past n_rows) into one half of
-    // the double-buffered Q tile, one item ahead of the tensor cores.
+    // the double-buffered Q tile, one item ahead of the tensor cores: 16-byte
+    // asynchronous copies, all of an item's in flight at once.
     for (int ii = i0; ii < i1; ++ii) {
       const int it = ii - i0, qb = it & 1;
       bool ok = true;
       if (it >= 2) ok = ptx::mbar_wait(&qfree[qb], ((it - 2) >> 1) & 1, abort_flag, p.err);
       if (!__all_sync(0xffffffffu, ok)) break;
       const WorkItem w = p.items[ii];
-      uint8_t* dst = qs + qb * QB;
+      const uint32_t dst = ptx::smem_u32(qs + qb * QB);
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint4 v[2][DCH];
+      for (int i = 0; i < kBM / 32; ++i) {
+        const int r = lane + 32 * i;
+        const bool valid = r < w.n_rows;
+        const int rr = w.row0 + r;
+        const T* src = valid ? qbase + (static_cast<size_t>(w.group0 + rr / p.g) * p.Hq + w.kv * p.g + rr % p.g) * D
+                             : qbase;
 #pragma unroll
-        for (int r2 = 0; r2 < 2; ++r2) {
-          const int r = lane + 32 * (2 * half + r2);
-          if (r < w.n_rows) {
-            const int rr = w.row0 + r;
-            const T* src = qbase + (static_cast<size_t>(w.group0 + rr / p.g) * p.Hq + w.kv * p.g + rr % p.g) * D;
-#pragma unroll
-            for (int j = 0; j < DCH; ++j) v[r2][j] = *reinterpret_cast<const uint4*>(src + 8 * j);
-          } else {
-#pragma unroll
-            for (int j = 0; j < DCH; ++j) v[r2][j] = make_uint4(0, 0, 0, 0);
-          }
-        }
-#pragma unroll
-        for (int r2 = 0; r2 < 2; ++r2) {
-          const int r = lane + 32 * (2 * half + r2);
-#pragma unroll
-          for (int j = 0; j < DCH; ++j) *reinterpret_cast<uint4*>(dst + tile_off(r, j, D * 2, kBM)) = v[r2][j];
-        }
+        for (int j = 0; j < DCH; ++j) ptx::cp_async_16(dst + tile_off(r, j, D * 2, kBM), src + 8 * j, valid ? 16u : 0u);
       }
-      ptx::fence_proxy_async_smem();
+      ptx::cp_async_wait_all();
+      ptx::fence_proxy_async_smem();  // the tensor cores read the tile through the async proxy
       ptx::mbar_arrive(&qfull[qb]);
     }
   } else if (warp == 1 || warp == 2) {
@@ -334,8 +339,8 @@ __global__ void __launch_bounds__(384, 1) attn_tc_kernel(const AttnParams p) {
       ptx::mbar_wait(my_done, 0, nullptr, p.err);
     }
     __syncwarp();
-  } else if (warp >= 4) {
-    // ------------------------------------------------- softmax / epilogue
+  } else if (warp < 12) {
+    // ---------------------------------------------------------------- softmax
     // Two threads per query row.  Warps 4..11 each take 16 rows: the TMEM
     // lane quadrant is fixed by warp % 4, warps 8..11 take its upper 16
     // lanes; with half-split TMEM access thread t holds row (t mod 16) of the
@@ -355,27 +360,36 @@ __global__ void __launch_bounds__(384, 1) attn_tc_kernel(const AttnParams p) {
     auto wait_all = [&](uint64_t* bar, uint32_t parity) {
       return __all_sync(0xffffffffu, ptx::mbar_wait(bar, parity, abort_flag, p.err));
     };
+    // An item's descriptor and the valid keys of its first 32 tiles are
+    // loaded while the previous item ends, so their latency is hidden.
+    WorkItem wn{};
+    int len_n = 0;
+    auto prefetch = [&](int ii) {
+      if (ii >= i1) return;
+      wn = p.items[ii];
+      len_n = 0;
+      const int nk = wn.n_chunks * SUB;
+      if (lane < nk) {
+        const int cl = p.chunk_len[p.chunks[wn.chunk_off + lane / SUB]] - (lane % SUB) * kC;
+        len_n = min(kC, max(0, cl));
+      }
+    };
+    prefetch(i0);
     int t = 0;
     bool ok = true;
     for (int ii = i0; ii < i1 && ok; ++ii) {
       const int it = ii - i0, ob = it & 1;
-      const WorkItem w = p.items[ii];
+      const WorkItem w = wn;
       const int nk = w.n_chunks * SUB;  // 64-key tiles
       const bool row_valid = r < w.n_rows;
-      int grp = 0, hg = 0;
-      if (row_valid) {
-        const int rr = w.row0 + r;
-        grp = w.group0 + rr / p.g;
-        hg = rr % p.g;
-      }
+      const int grp = row_valid ? w.group0 + (w.row0 + r) / p.g : 0;
       // causal: keys of this item up to position p0 + token (item key 0 is at w.key0)
       const int key_limit = (p.causal_p0 >= 0 && row_valid) ? p.causal_p0 + grp + 1 - w.key0 : INT_MAX;
-      const int part_row = (row_valid && !p.final_mode) ? __ldg(p.row_idx + w.part_base + r) : 0;
       float m = -INFINITY, l = 0.f;  // reference max; this half's row sum relative to it
-      int my_len = 0;
+      int my_len = len_n;
 
       for (int c = 0; c < nk; ++c, ++t) {
-        if ((c & 31) == 0) {  // valid keys of tiles c .. c+31, one per lane
+        if ((c & 31) == 0 && c > 0) {  // valid keys of tiles c .. c+31, one per lane
           my_len = 0;
           if (c + lane < nk) {
             const int cl = p.chunk_len[p.chunks[w.chunk_off + (c + lane) / SUB]] - ((c + lane) % SUB) * kC;
@@ -489,32 +503,65 @@ __global__ void __launch_bounds__(384, 1) attn_tc_kernel(const AttnParams p) {
         l += (ps[0] + ps[1]) + (ps[2] + ps[3]);
       }
       if (!ok) break;
-
-      // ---- the item's O: wait for its last PV product, then write out
-      if (!wait_all(&ofull[ob], (it >> 1) & 1)) {
+      prefetch(ii + 1);
+      // ---- hand the row's max and sum to the epilogue warps, which stream
+      // O out once its last PV product has completed (ml_buf[ob] is free once
+      // the epilogue of item it - 2 has read it)
+      if (it >= 2 && !wait_all(&oempty[ob], ((it - 2) >> 1) & 1)) {
         ok = false;
         break;
       }
-      ptx::tc_fence_after();
       const float lrow = l + __shfl_xor_sync(0xffffffffu, l, 16);  // the row sum of both halves
-      const float inv = 1.f / lrow;
+      if (hf == 0) ml_buf[ob * kBM + r] = make_float2(m, lrow);
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&mlfull[ob]);  // one arrival per warp (release: ml_buf above)
+    }
+  } else {
+    // --------------------------------------------------------------- epilogue
+    // One thread per query row (TMEM lane quadrant warp % 4): once an item's
+    // last PV product has completed and the softmax warps have left the row
+    // max and sum in ml_buf, read O out of TMEM and write the item's partial
+    // rows (the merge kernel combines them) or, for a prefill block, the
+    // normalised output rows; meanwhile the softmax warps run the next item
+    // into the other O buffer.
+    const int quad = warp & 3;
+    const int r = quad * 32 + lane;
+    const uint32_t tl = tbase + (static_cast<uint32_t>(quad * 32) << 16);
+    auto wait_all = [&](uint64_t* bar, uint32_t parity) {
+      return __all_sync(0xffffffffu, ptx::mbar_wait(bar, parity, abort_flag, p.err));
+    };
+    for (int ii = i0; ii < i1; ++ii) {
+      const int it = ii - i0, ob = it & 1;
+      const WorkItem w = p.items[ii];
+      const bool row_valid = r < w.n_rows;
+      int grp = 0, hg = 0;
+      if (row_valid) {
+        const int rr = w.row0 + r;
+        grp = w.group0 + rr / p.g;
+        hg = rr % p.g;
+      }
+      const int part_row = (row_valid && !p.final_mode) ? __ldg(p.row_idx + w.part_base + r) : 0;
+      if (!wait_all(&ofull[ob], (it >> 1) & 1)) break;
+      if (!wait_all(&mlfull[ob], (it >> 1) & 1)) break;
+      ptx::tc_fence_after();
+      const float2 ml = ml_buf[ob * kBM + r];
+      const float inv = 1.f / ml.y;
       const size_t out_row = (static_cast<size_t>(grp) * p.Hq + w.kv * p.g + hg) * D;
       float* po = p.part_o + static_cast<size_t>(part_row) * D;
 #pragma unroll
-      for (int cg = 0; cg < HD / 32; ++cg) {
+      for (int cg = 0; cg < D / 32; ++cg) {
         uint32_t ov[32];
-        ptx::tmem_ld32_half<HD>(tl + O_COL + ob * D + 32 * cg, ov);
+        ptx::tmem_ld32(tl + O_COL + ob * D + 32 * cg, ov);
         ptx::tmem_ld_wait(ov);
-        const int col = hf * HD + 32 * cg;  // first O column of this load
         if (row_valid) {
           if (p.final_mode && p.out_f32) {
-            float4* o4 = reinterpret_cast<float4*>(static_cast<float*>(p.out) + out_row + col);
+            float4* o4 = reinterpret_cast<float4*>(static_cast<float*>(p.out) + out_row + 32 * cg);
 #pragma unroll
             for (int j = 0; j < 8; ++j)
               o4[j] = make_float4(__uint_as_float(ov[4 * j]) * inv, __uint_as_float(ov[4 * j + 1]) * inv,
                                   __uint_as_float(ov[4 * j + 2]) * inv, __uint_as_float(ov[4 * j + 3]) * inv);
           } else if (p.final_mode) {
-            T* out = static_cast<T*>(p.out) + out_row + col;
+            T* out = static_cast<T*>(p.out) + out_row + 32 * cg;
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
               const float* o8 = reinterpret_cast<const float*>(ov) + 8 * j;
@@ -526,7 +573,7 @@ __global__ void __launch_bounds__(384, 1) attn_tc_kernel(const AttnParams p) {
               *reinterpret_cast<uint4*>(out + 8 * j) = pk;
             }
           } else {
-            float4* o4 = reinterpret_cast<float4*>(po + col);
+            float4* o4 = reinterpret_cast<float4*>(po + 32 * cg);
 #pragma unroll
             for (int j = 0; j < 8; ++j)
               o4[j] = make_float4(__uint_as_float(ov[4 * j]), __uint_as_float(ov[4 * j + 1]),
@@ -537,8 +584,7 @@ __global__ void __launch_bounds__(384, 1) attn_tc_kernel(const AttnParams p) {
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&oempty[ob]);  // one arrival per warp
-      if (row_valid && !p.final_mode && hf == 0)
-        reinterpret_cast<float2*>(p.part_ml)[part_row] = make_float2(m, lrow);
+      if (row_valid && !p.final_mode) reinterpret_cast<float2*>(p.part_ml)[part_row] = ml;
     }
   }
 
@@ -563,7 +609,7 @@ cudaError_t launch_tc_t(const AttnParams& p, int grid, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(384);
+  cfg.blockDim = dim3(512);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];

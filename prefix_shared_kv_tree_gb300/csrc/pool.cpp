@@ -157,6 +157,7 @@ struct pst_pool {
   int32_t simt_max_ctas = 0;  // cap on the CUDA-core grid; 0 = one CTA per SM
   bool simt_first = false;     // launch order of the decode step (see launch_overlapped)
   bool tc_first_forced = false;
+  bool simt_first_forced = false;
   int32_t tc_ctas_forced = 0;  // > 0: chunk-first CTAs when both phases run (tuning knob)
   // sequence-first items: about sqrt(g) * T / (simt_unit_div * W) chunks each
   // (at most kSimtInline; an item's set-up and partial rows grow with g), the
@@ -575,7 +576,7 @@ pst_status rebuild(pst_pool* p) {
       // one (it then waits for the first kernel without holding its SMs long).
       const double t_tc = 1.2 * std::max(w_tc / k, max_cost);
       const double t_simt = simt_bytes / std::min(hbm, std::max(1, p->n_sm - k) * per_sm);
-      p->simt_first = k < p->n_sm && t_tc <= 1.1 * t_simt && !p->tc_first_forced;
+      p->simt_first = k < p->n_sm && ((t_tc <= 1.1 * t_simt && !p->tc_first_forced) || p->simt_first_forced);
     }
     if (concurrent && p->n_sm > 1) {
       const double w_simt = static_cast<double>(T) * p->simt_tile_us;
@@ -852,6 +853,7 @@ pst_status pst_pool_create(const pst_config* cfg, int device, pst_pool** out) {
   if (const char* e = std::getenv("PST_HBM_GBS")) p->hbm_gbs = std::atof(e);
   if (const char* e = std::getenv("PST_SIMT_UNIT")) p->simt_unit = std::atoi(e);
   if (const char* e = std::getenv("PST_TC_FIRST")) p->tc_first_forced = std::atoi(e) != 0;
+  if (const char* e = std::getenv("PST_SIMT_FIRST")) p->simt_first_forced = std::atoi(e) != 0;
   if (const char* e = std::getenv("PST_TC_CTAS")) p->tc_ctas_forced = std::max(0, std::atoi(e));
   if (const char* e = std::getenv("PST_SIMT_UNIT_DIV")) p->simt_unit_div = std::max(0.25, std::atof(e));
   if (const char* e = std::getenv("PST_TC_MAX_RUN")) p->tc_max_run = std::max(2, std::atoi(e));
@@ -1814,6 +1816,9 @@ pst_status pst_stats(const pst_pool* p, pst_stats_t* o) {
   o->phase2_items = p->n_simt_items;
   o->partial_rows = p->n_part_rows;
   o->graph_captures = p->graph_captures;
+  o->phase1_ctas = p->n_tc_ctas;
+  o->phase2_ctas = p->n_simt_items > 0 ? p->simt_grid : 0;
+  o->simt_first = p->simt_first ? 1 : 0;
   return PST_OK;
 }
 

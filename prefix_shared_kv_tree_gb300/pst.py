@@ -38,7 +38,8 @@ class pst_stats_t(Structure):
                 ("shared_chunks", c_int64), ("unique_tokens", c_int64), ("logical_tokens", c_int64),
                 ("table_version", c_int64), ("rebuild_count", c_int64), ("last_rebuild_us", c_double),
                 ("phase1_items", c_int64), ("phase2_items", c_int64), ("partial_rows", c_int64),
-                ("graph_captures", c_int64)]
+                ("graph_captures", c_int64), ("phase1_ctas", c_int64), ("phase2_ctas", c_int64),
+                ("simt_first", c_int64)]
 
 
 class PstError(RuntimeError):
