@@ -9,19 +9,24 @@
 // (Chunked Prefill, sections 1-2).
 //
 // Persistent: each CTA walks its own list of work items (up to 128 stacked
-// query rows of one KV head against a list of chunks of 64 or 128 tokens,
-// taken as tiles of 64 keys); TMEM and the mbarriers are set up once and the
-// pipelines run across item boundaries.
+// query rows of one KV head against a list of chunks of 16, 32, 64 or 128
+// tokens, taken as tiles of 64 keys: four or two chunks, one chunk, or half
+// of one); TMEM and the mbarriers are set up once and the pipelines run
+// across item boundaries.
 // Warp roles (512 threads):
 //   warp 0      : producer.  Lane 0 moves each tile's 32 KB K + V^T image
 //                 from the pool into a 5-stage shared-memory ring by bulk
 //                 async copy (TMA engine): one copy for a 64-token chunk; for
 //                 keys [64h, 64h + 64) of a 128-token chunk, rows 64h .. of
-//                 each 128-byte column block of K and column block h of V^T.
-//                 The pool already stores tiles in the tensor cores'
+//                 each 128-byte column block of K and column block h of V^T;
+//                 for 16- or 32-token chunks, per chunk of the tile its K
+//                 rows into each K column block and its V^T core matrices.
+//                 The pool already stores K blocks in the tensor cores'
 //                 128-byte-swizzled K-major layout (the swizzle follows the
-//                 row index mod 8, so a 64-row part of a block is itself a
-//                 block of that layout), and Q is written in the same layout.
+//                 row index mod 8, so a part of a block whose rows start at a
+//                 multiple of 8 is itself a block of that layout), V^T blocks
+//                 with 128-byte rows likewise and shorter ones as plain 8-row
+//                 core matrices; Q is written in the swizzled layout.
 //   warp 1      : allocates TMEM and issues S = Q K^T (M=128, N=64, K=D) into
 //                 three TMEM buffers (two for bf16), as far ahead of the
 //                 softmax as they allow, across item boundaries.
@@ -65,7 +70,7 @@ namespace pst {
 
 namespace {
 
-constexpr int kC = 64;     // tokens per chunk
+constexpr int kC = 64;     // keys per tile
 constexpr int kBM = 128;   // stacked query rows per item
 constexpr int kNS = 5;     // K/V tile stages
 constexpr int kSB = 3;     // S buffers in TMEM at most: S runs up to kSB - 1 chunks ahead of the PV product
@@ -93,10 +98,13 @@ template <typename T, int D, int CP>
 __global__ void __launch_bounds__(512, 1) attn_tc_kernel(const AttnParams p) {
   constexpr uint32_t HALF = kC * D * 2;
   constexpr uint32_t TILE = tc_tile_bytes(D);
-  constexpr int SUB = CP / kC;                    // 64-key tiles per pool chunk
+  // A 64-key tile is one pool chunk (CP = 64), half of one (CP = 128: SUB = 2
+  // tiles per chunk), or CPT consecutive chunks (CP = 16, 32).
+  constexpr int SUB = CP >= kC ? CP / kC : 1;     // 64-key tiles per pool chunk
+  constexpr int CPT = CP < kC ? kC / CP : 1;      // pool chunks per 64-key tile
   constexpr uint32_t PHALF = CP * D * 2;          // a pool chunk's K block (per KV head)
   constexpr uint32_t PTILE = 2 * PHALF;           // a pool chunk's K + V^T blocks
-  static_assert(SUB == 1 || SUB == 2, "chunk size 64 or 128");
+  static_assert(CP == 16 || CP == 32 || CP == 64 || CP == 128, "chunk size");
   constexpr uint32_t QB = tc_q_bytes(D);
   constexpr int DCH = D / 8;    // 16-byte chunks per row when the reduction runs over D
   constexpr int CCH = kC / 8;   // 16-byte chunks per row when the reduction runs over keys
@@ -197,20 +205,39 @@ __global__ void __launch_bounds__(512, 1) attn_tc_kernel(const AttnParams p) {
       bool ok = true;
       for (int ii = i0; ii < i1 && ok; ++ii) {
         const WorkItem w = p.items[ii];
-        const int nt = w.n_chunks * SUB;
+        const int nt = (w.n_chunks * SUB + CPT - 1) / CPT;
         for (int c = 0; c < nt; ++c, ++t) {
           const int s = t % kNS;
           if (t >= kNS && !ptx::mbar_wait(&empty[s], ((t / kNS) - 1) & 1, abort_flag, p.err)) {
             ok = false;
             break;
           }
-          const int chunk = p.chunks[w.chunk_off + c / SUB];
-          const uint8_t* src = p.pool + (static_cast<size_t>(chunk) * p.Hkv + w.kv) * PTILE;
           uint8_t* dst = kvs + s * TILE;
           ptx::mbar_arrive_expect_tx(&full[s], TILE);
-          if constexpr (SUB == 1) {
+          if constexpr (CPT > 1) {
+            // chunks c CPT .. c CPT + CPT - 1: chunk i's K rows become rows
+            // [i CP, i CP + CP) of each 128-byte K column block (CP is a
+            // multiple of 8, so the swizzle phase of every row is kept) and
+            // its V^T core matrices block i of the V^T part.  Past the item's
+            // last chunk the slot gets its first chunk again: finite values,
+            // masked by the softmax.
+#pragma unroll
+            for (int i = 0; i < CPT; ++i) {
+              const int ch = c * CPT + i < w.n_chunks ? c * CPT + i : c * CPT;
+              const int chunk = p.chunks[w.chunk_off + ch];
+              const uint8_t* src = p.pool + (static_cast<size_t>(chunk) * p.Hkv + w.kv) * PTILE;
+#pragma unroll
+              for (int kb = 0; kb < D / 64; ++kb)
+                ptx::bulk_g2s_hint(dst + kb * (kC * 128) + i * (CP * 128), src + kb * (CP * 128), CP * 128, &full[s], pol);
+              ptx::bulk_g2s_hint(dst + HALF + i * PHALF, src + PHALF, PHALF, &full[s], pol);
+            }
+          } else if constexpr (SUB == 1) {
+            const int chunk = p.chunks[w.chunk_off + c];
+            const uint8_t* src = p.pool + (static_cast<size_t>(chunk) * p.Hkv + w.kv) * PTILE;
             ptx::bulk_g2s_hint(dst, src, TILE, &full[s], pol);
           } else {
+            const int chunk = p.chunks[w.chunk_off + c / SUB];
+            const uint8_t* src = p.pool + (static_cast<size_t>(chunk) * p.Hkv + w.kv) * PTILE;
             const int h = c % SUB;
 #pragma unroll
             for (int kb = 0; kb < D / 64; ++kb)  // K column block kb: rows 64h .. 64h + 63
@@ -285,16 +312,27 @@ __global__ void __launch_bounds__(512, 1) attn_tc_kernel(const AttnParams p) {
         if (!wait_all(&pfull[b], (t >> 1) & 1)) return false;
         if (c == 0 && it >= 2 && !wait_all(&oempty[ob], ((it - 2) >> 1) & 1)) return false;
         ptx::tc_fence_after();
-        const uint64_t b0 = ptx::smem_desc_sw128(kv_addr + s * TILE + HALF, 1024);
+        // V^T operand of K step kk (keys [16kk, 16kk+16)): at CP >= 64 the
+        // tile's 128-byte-swizzled block, 32 bytes further per step; at
+        // CP < 64 the core matrices of chunk (16 kk) / CP, unswizzled
+        // (16-byte rows, CP / 8 core matrices per 8-row group, two per step)
+        auto vdesc = [&](int kk) -> uint64_t {
+          if constexpr (CPT > 1) {
+            const uint32_t at = kv_addr + s * TILE + HALF + (16 * kk / CP) * PHALF + ((16 * kk) % CP) / 16 * 256;
+            return ptx::smem_desc(at, 128, 16 * CP);
+          } else {
+            return ptx::smem_desc_sw128(kv_addr + s * TILE + HALF, 1024) + kk * 2;
+          }
+        };
 #pragma unroll
         for (int kk = 0; kk < kC / 16; ++kk)  // K step kk: keys [16kk, 16kk+16) = P columns [8kk, 8kk+8)
-          ptx::mma_f16_tmem_a_warp(tbase + O_COL + ob * D, tbase + P_COL + b * PW + kk * 8, b0 + kk * 2, ID_O,
+          ptx::mma_f16_tmem_a_warp(tbase + O_COL + ob * D, tbase + P_COL + b * PW + kk * 8, vdesc(kk), ID_O,
                                    (c > 0 || kk > 0) ? 1u : 0u);
         if constexpr (PSPLIT) {
 #pragma unroll
           for (int kk = 0; kk < kC / 16; ++kk)  // the remainders: P columns 32 + [8kk, 8kk+8)
-            ptx::mma_f16_tmem_a_warp(tbase + O_COL + ob * D, tbase + P_COL + b * PW + 32 + kk * 8, b0 + kk * 2,
-                                     ID_O, 1u);
+            ptx::mma_f16_tmem_a_warp(tbase + O_COL + ob * D, tbase + P_COL + b * PW + 32 + kk * 8, vdesc(kk), ID_O,
+                                     1u);
         }
         ptx::mma_commit_warp(&pfree[b]);
         ptx::mma_commit_warp(&empty[s]);
@@ -305,7 +343,8 @@ __global__ void __launch_bounds__(512, 1) attn_tc_kernel(const AttnParams p) {
       // ahead as the kSB S buffers allow, so the softmax threads find each S
       // ready when they finish the previous chunk.
       int s_ii = i0, s_c = 0, s_t = 0;
-      int s_nk = i0 < i1 ? p.items[i0].n_chunks * SUB : 0;
+      auto tiles_of = [](const WorkItem& w) { return (w.n_chunks * SUB + CPT - 1) / CPT; };
+      int s_nk = i0 < i1 ? tiles_of(p.items[i0]) : 0;
       auto issue_next_s = [&]() -> bool {
         const int it = s_ii - i0, qb = it & 1;
         if (s_c == 0) {  // the item's Q tile
@@ -318,7 +357,7 @@ __global__ void __launch_bounds__(512, 1) attn_tc_kernel(const AttnParams p) {
         if (++s_c == s_nk) {
           s_c = 0;
           ++s_ii;
-          s_nk = s_ii < i1 ? p.items[s_ii].n_chunks * SUB : 0;
+          s_nk = s_ii < i1 ? tiles_of(p.items[s_ii]) : 0;
         }
         return true;
       };
@@ -329,7 +368,7 @@ __global__ void __launch_bounds__(512, 1) attn_tc_kernel(const AttnParams p) {
         int t = 0;
         for (int ii = i0; ii < i1 && ok; ++ii) {
           const int it = ii - i0;
-          const int nk = p.items[ii].n_chunks * SUB;
+          const int nk = tiles_of(p.items[ii]);
           for (int c = 0; c < nk && ok; ++c, ++t) ok = issue_pv(t, it, c, c + 1 == nk);
         }
       }
@@ -360,6 +399,18 @@ __global__ void __launch_bounds__(512, 1) attn_tc_kernel(const AttnParams p) {
     auto wait_all = [&](uint64_t* bar, uint32_t parity) {
       return __all_sync(0xffffffffu, ptx::mbar_wait(bar, parity, abort_flag, p.err));
     };
+    // Valid keys of tile c of item w: the tile's chunks are full but for the
+    // item's last chunk (only a sequence's last chunk is partial), whose
+    // valid tokens the scatter kernel keeps in chunk_len.
+    auto tile_len = [&](const WorkItem& w, int c) -> int {
+      if constexpr (CPT > 1) {
+        const int first = c * CPT, cnt = min(CPT, w.n_chunks - first);
+        return (cnt - 1) * CP + p.chunk_len[p.chunks[w.chunk_off + first + cnt - 1]];
+      } else {
+        return min(kC, max(0, p.chunk_len[p.chunks[w.chunk_off + c / SUB]] - (c % SUB) * kC));
+      }
+    };
+    auto tiles_of = [](const WorkItem& w) { return (w.n_chunks * SUB + CPT - 1) / CPT; };
     // An item's descriptor and the valid keys of its first 32 tiles are
     // loaded while the previous item ends, so their latency is hidden.
     WorkItem wn{};
@@ -367,12 +418,7 @@ __global__ void __launch_bounds__(512, 1) attn_tc_kernel(const AttnParams p) {
     auto prefetch = [&](int ii) {
       if (ii >= i1) return;
       wn = p.items[ii];
-      len_n = 0;
-      const int nk = wn.n_chunks * SUB;
-      if (lane < nk) {
-        const int cl = p.chunk_len[p.chunks[wn.chunk_off + lane / SUB]] - (lane % SUB) * kC;
-        len_n = min(kC, max(0, cl));
-      }
+      len_n = lane < tiles_of(wn) ? tile_len(wn, lane) : 0;
     };
     prefetch(i0);
     int t = 0;
@@ -380,7 +426,7 @@ __global__ void __launch_bounds__(512, 1) attn_tc_kernel(const AttnParams p) {
     for (int ii = i0; ii < i1 && ok; ++ii) {
       const int it = ii - i0, ob = it & 1;
       const WorkItem w = wn;
-      const int nk = w.n_chunks * SUB;  // 64-key tiles
+      const int nk = tiles_of(w);  // 64-key tiles
       const bool row_valid = r < w.n_rows;
       const int grp = row_valid ? w.group0 + (w.row0 + r) / p.g : 0;
       // causal: keys of this item up to position p0 + token (item key 0 is at w.key0)
@@ -389,13 +435,8 @@ __global__ void __launch_bounds__(512, 1) attn_tc_kernel(const AttnParams p) {
       int my_len = len_n;
 
       for (int c = 0; c < nk; ++c, ++t) {
-        if ((c & 31) == 0 && c > 0) {  // valid keys of tiles c .. c+31, one per lane
-          my_len = 0;
-          if (c + lane < nk) {
-            const int cl = p.chunk_len[p.chunks[w.chunk_off + (c + lane) / SUB]] - ((c + lane) % SUB) * kC;
-            my_len = min(kC, max(0, cl));
-          }
-        }
+        if ((c & 31) == 0 && c > 0)  // valid keys of tiles c .. c+31, one per lane
+          my_len = c + lane < nk ? tile_len(w, c + lane) : 0;
         // valid keys of this thread's half of the tile
         const int lim = min(__shfl_sync(0xffffffffu, my_len, c & 31), key_limit - c * kC) - hf * HK;
         const int b = t & 1, sb = t % SB;
@@ -622,15 +663,19 @@ cudaError_t launch_tc_t(const AttnParams& p, int grid, cudaStream_t s) {
 
 template <typename T, int D>
 cudaError_t launch_tc_c(int C, const AttnParams& p, int grid, cudaStream_t s) {
-  if (C == kC) return launch_tc_t<T, D, kC>(p, grid, s);
-  if (C == 2 * kC) return launch_tc_t<T, D, 2 * kC>(p, grid, s);
+  switch (C) {
+    case 16: return launch_tc_t<T, D, 16>(p, grid, s);
+    case 32: return launch_tc_t<T, D, 32>(p, grid, s);
+    case 64: return launch_tc_t<T, D, 64>(p, grid, s);
+    case 128: return launch_tc_t<T, D, 128>(p, grid, s);
+  }
   return cudaErrorInvalidValue;
 }
 
 }  // namespace
 
 bool tc_supported(int dtype, int D, int C) {
-  return (dtype == kF16 || dtype == kBF16) && (D == 64 || D == 128) && (C == kC || C == 2 * kC);
+  return (dtype == kF16 || dtype == kBF16) && (D == 64 || D == 128) && (C == 16 || C == 32 || C == 64 || C == 128);
 }
 
 size_t attn_tc_smem(int D) { return tc_smem_bytes(D); }

@@ -163,7 +163,7 @@ struct pst_pool {
   // (at most kSimtInline; an item's set-up and partial rows grow with g), the
   // last simt_tail * W chunks as single-chunk items
   double simt_unit_div = 8.0, simt_tail = 2.0;
-  int32_t tc_max_run = 32;  // chunk-first items: at most this many chunks
+  int32_t tc_max_run = 32;  // chunk-first items: at most this many 64-key tiles
   int32_t merge_cap = 0, merge_cap_forced = -1;
   int32_t simt_grid = 0, simt_stages = 3, simt_wpc = 8;
   int64_t n_part_rows = 0, shared_chunks = 0;
@@ -455,25 +455,26 @@ pst_status rebuild(pst_pool* p) {
   streams.clear();
   std::vector<int32_t> warp_items;
 
-  // ---- phase 1: chunk-first over the runs.  The tensor-core kernel takes a
-  // chunk as tiles of 64 keys (two for 128-token chunks): its costs and item
-  // lengths are counted in tiles.
-  const int32_t sub = p->use_tc ? p->C / 64 : 1;
-  int64_t p1_iters = 0;
+  // ---- phase 1: chunk-first over the runs.  The tensor-core kernel takes
+  // chunks as tiles of 64 keys (two per 128-token chunk, a 64-token chunk,
+  // two 32- or four 16-token chunks): its costs and item lengths are counted
+  // in tiles, tpc per chunk.
+  const double tpc = p->use_tc ? p->C / 64.0 : 1.0;
+  double p1_iters = 0;
   for (const auto& r : runs) {
     const int32_t id0 = r.front();
     const int64_t rows = static_cast<int64_t>(nj[id0] - ni[id0]) * g;
-    p1_iters += static_cast<int64_t>(r.size()) * sub * Hkv * (p->use_tc ? ceil_div(rows, 128) : (nj[id0] - ni[id0]));
-    (void)rows;
+    p1_iters += static_cast<double>(r.size()) * tpc * Hkv * (p->use_tc ? ceil_div(rows, 128) : (nj[id0] - ni[id0]));
   }
   // chunk-first items: enough of them to cover every SM when the phases run
-  // back to back; fewer, longer ones when they share the GPU (in chunks)
-  const int64_t split1 =
-      std::max<int64_t>(1, ((p->cfg.flags & PST_FLAG_CONCURRENT_PHASES)
-                                ? 8
-                                : std::min<int64_t>(p->tc_max_run,
-                                                    std::max<int64_t>(2, ceil_div(p1_iters, std::max(1, p->n_sm))))) /
-                               sub);
+  // back to back; fewer, longer ones when they share the GPU (in tiles, then
+  // chunks)
+  const int64_t tiles1 =
+      (p->cfg.flags & PST_FLAG_CONCURRENT_PHASES)
+          ? 8
+          : std::min<int64_t>(p->tc_max_run,
+                              std::max<int64_t>(2, static_cast<int64_t>(std::ceil(p1_iters / std::max(1, p->n_sm)))));
+  const int64_t split1 = std::max<int64_t>(1, static_cast<int64_t>(std::floor(tiles1 / tpc)));
   for (const auto& r : runs) {
     const int32_t i = ni[r.front()], j = nj[r.front()];
     const int32_t rows = (j - i) * g;
@@ -540,7 +541,8 @@ pst_status rebuild(pst_pool* p) {
     double w_tc = 0;
     for (int32_t x = 0; x < n; ++x) {
       const bool first_tile = tc_items[8 * x + 4] == 0;  // row0: the run's first row tile reads its tiles from DRAM
-      cost[x] = tc_items[8 * x + 1] * sub * (p->tc_chunk_us + (first_tile ? p->tc_hbm_us : 0.0)) + p->tc_item_us;
+      cost[x] = std::ceil(tc_items[8 * x + 1] * tpc) * (p->tc_chunk_us + (first_tile ? p->tc_hbm_us : 0.0)) +
+                p->tc_item_us;
       w_tc += cost[x];
     }
     const double max_cost = *std::max_element(cost.begin(), cost.end());
@@ -1443,7 +1445,7 @@ static pst_status append_block(pst_pool* p, int64_t seq_id, Seq& sq, const int32
 static pst_status prefill_attention_tc(pst_pool* p, const AttnParams& base, const std::vector<int32_t>& path_chunks,
                                        int64_t p0, int64_t W, cudaStream_t s) {
   const int g = p->g, Hkv = p->cfg.n_kv_heads, C = p->C;
-  const int32_t sub = C / 64;  // 64-key tiles per chunk
+  const double tpc = C / 64.0;  // 64-key tiles per chunk
   const int64_t rows = W * g;
   struct Tile {
     int32_t kv, r0, n_rows, n_ch, nsplit;
@@ -1456,7 +1458,7 @@ static pst_status prefill_attention_tc(pst_pool* p, const AttnParams& base, cons
       const int64_t t_last = (r0 + n_rows - 1) / g;
       const int32_t n_ch = static_cast<int32_t>(ceil_div(p0 + t_last + 1, C));
       tiles.push_back({kv, static_cast<int32_t>(r0), n_rows, n_ch, 1});
-      T += static_cast<int64_t>(n_ch) * sub;
+      T += static_cast<int64_t>(std::ceil(n_ch * tpc));
     }
   // pieces of about T / (2 #SMs) tiles, at least kMinPiece, when the items
   // would leave at least half of the SMs idle (measured on the GQA tree's
@@ -1467,7 +1469,9 @@ static pst_status prefill_attention_tc(pst_pool* p, const AttnParams& base, cons
   int64_t n_pieces = 0;
   const bool split = p->split_prefill && 2 * static_cast<int64_t>(tiles.size()) <= p->n_sm;
   for (auto& t : tiles) {
-    if (split) t.nsplit = static_cast<int32_t>(std::max<int64_t>(1, std::min<int64_t>(t.n_ch, (t.n_ch * sub + piece / 2) / piece)));
+    if (split)
+      t.nsplit = static_cast<int32_t>(
+          std::max<int64_t>(1, std::min<int64_t>(t.n_ch, std::llround(t.n_ch * tpc / static_cast<double>(piece)))));
     n_pieces += t.nsplit;
   }
 
