@@ -74,10 +74,11 @@ typedef struct {
   int32_t n_q_heads;   /* Hq >= 1 */
   int32_t n_kv_heads;  /* Hkv >= 1, divides Hq, Hq/Hkv in {1,2,4,8} */
   int32_t head_dim;    /* d in {64, 128} */
-  int32_t chunk_size;  /* c in {16, 32, 64, 128}; the chunk-first phase runs on the
-                          tensor cores (tcgen05) for 16-bit K/V at c = 64 and 128
-                          (a 128-token chunk as two 64-key tiles), on the CUDA-core
-                          kernel otherwise */
+  int32_t chunk_size;  /* c in {16, 32, 64, 128}; for 16-bit K/V the chunk-first
+                          phase runs on the tensor cores (tcgen05) in 64-key tiles:
+                          four 16- or two 32-token chunks, one 64-token chunk, or
+                          half of a 128-token chunk; fp32 K/V uses the CUDA-core
+                          kernel for both phases */
   int64_t max_chunks;  /* pool capacity in chunks (>= 1) */
   int32_t dtype;       /* pst_dtype */
   int32_t min_share;   /* chunk-first threshold: a chunk covered by >= min_share live
@@ -168,7 +169,7 @@ pst_status pst_seq_length(const pst_pool* pool, int64_t seq_id, int64_t* n_token
  * q, out: device [B][Hq][d], B = live count.  Rebuilds and uploads the chunk
  * tables first if the tree changed (Knowl 5).  q and out must start on a
  * 16-byte boundary (PST_ERR_INVALID otherwise).  Chunk-first partials run on the
- * tensor cores (tcgen05) for f16/bf16 with c = 64 or 128, sequence-first partials on
+ * tensor cores (tcgen05) for f16/bf16 at every chunk size, sequence-first partials on
  * warp-level tensor-core products (f16/bf16) or the CUDA cores (f32), then a
  * merge kernel combines the partial rows (attn_reduce) and writes out. */
 pst_status pst_decode_attention(pst_pool* pool, const void* q, void* out, void* stream);
@@ -307,8 +308,9 @@ pst_status pst_set_profiling(pst_pool* pool, int enable);
  * call from its first kernel to the end of the merge.  Waits for those
  * events.  (The per-kernel events sit between the kernels and may keep them
  * from overlapping; time the whole call without profiling.)  After a
- * profiled prefill call: the attention kernel alone, in ms[0] (tensor-core
- * kernel) or ms[1] (CUDA-core kernel). */
+ * profiled prefill call: the attention kernel alone (and, when the block was
+ * cut along the keys, the merge of its pieces), in ms[0] (tensor-core kernel)
+ * or ms[1] (CUDA-core kernel). */
 pst_status pst_phase_times(pst_pool* pool, float* ms3);
 
 /* Kernel launches issued by the last pst_decode_attention call. */

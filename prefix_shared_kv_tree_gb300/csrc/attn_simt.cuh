@@ -1,28 +1,35 @@
-// Sequence-first partial attention on the CUDA cores (ChunkAttention, Knowl 2
-// phase 2, with partial_attn / attn_reduce of Knowl 3).  Also runs the
-// chunk-first phase when the tensor-core kernel does not apply (fp32, or a
-// chunk size other than 64), and causal prefill blocks in that case.
+// Sequence-first partial attention (ChunkAttention, Knowl 2 phase 2, with
+// partial_attn / attn_reduce of Knowl 3).  Also runs the chunk-first phase
+// when the tensor-core kernel does not apply (fp32 K/V, or the
+// PST_FLAG_NO_TENSOR_CORES flag), and causal prefill blocks in that case.
 //
 // Warp-specialised, warp-per-stream design.  A CTA holds NW consumer warps and
 // one producer warp; lane c of the producer serves consumer c:
 //   * it claims work items (a run of up to four chunks of one (group, KV
-//     head), chunk ids inline) one at a time from a global counter, largest
-//     first, so consumers whose SM came free late (an earlier kernel held it)
-//     simply get fewer;
+//     head), chunk ids inline; longer prefill runs keep theirs in the chunk
+//     list) for the whole CTA, NW consecutive indices per atomic on a global
+//     counter, largest first: two batches are in hand and the claim of a third
+//     is in flight, and a batch's descriptors land in shared memory by one
+//     bulk copy, so consumers whose SM came free late (an earlier kernel held
+//     it) simply get fewer;
 //   * it fills the consumer's two item slots: the item header by shared
 //     stores, the chunks' valid-token counts by 4-byte async copies, the
 //     query rows by one bulk async copy;
-//   * it keeps the consumer's ring of `stages` pieces full with bulk async
-//     copies (TMA engine): a tile is consumed as 32-row pieces -- each 32-key
-//     half of every 128-byte column block of K, then each 32-row group of
-//     V^T -- each a contiguous block of the pool's tile image.
-// The consumer warps issue no global load and no atomic at all: every latency
-// of the item pipeline (claim, descriptor, chunk lengths, query rows, tiles)
-// sits in the producer, which waits for none of them in the step that issued
-// it.  Consumers wait on mbarriers only.  Scores: lane = key, 128-bit shared
-// loads, fp32 FMAs split over 4 accumulators; tile max by warp shuffles; row
-// sums stay lane-local until the item ends.  Values: lane = output feature row
-// of V^T, 2 accumulators per row.  The item's (o, m, n) rows then go to the
+//   * the consumer's lane 0 keeps its ring of `stages` pieces full with bulk
+//     async copies (TMA engine): a tile is consumed as pieces of up to 64
+//     rows -- each key run of every 128-byte column block of K, then each
+//     row group of V^T -- each a contiguous block of the pool's tile image.
+// The consumer warps issue no global load and no atomic: every latency of the
+// item pipeline (claim, descriptor, chunk lengths, query rows) sits in the
+// producer, which waits for none of them in the step that issued it.  For
+// 16-bit K/V the products run on the tensor cores as warp-level mma.sync
+// m16n8k16: S^T = K Q^T and O^T = V^T P^T with keys / output features on the
+// 16-row side and the item's <= 8 query rows on the 8-column side (bf16
+// probabilities as two bf16 terms, the rounded value and the rounded
+// remainder); the online softmax per query column uses shuffles over the 8
+// lanes that hold it.  fp32 K/V: lane = key, packed fp32 FMAs, warp-shuffle
+// tile max, row sums lane-local until the item ends; values with lane =
+// output feature row of V^T.  The item's (o, m, n) rows then go to the
 // partial buffer; the merge kernel that follows combines the rows of every
 // (batch row, KV head).
 #pragma once
