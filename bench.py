@@ -210,12 +210,39 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows), "samples_under_load": len(loaded)}
 
 
+def strip_comments(src: str) -> str:
+    """C/C++/CUDA source without its comments and with runs of whitespace
+    collapsed, so that a digest of it changes with the code only."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c in "\"'":  # string or character literal: copied as is
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            out.append(" ")
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def source_digest(files) -> str:
-    """sha256 (first 16 hex digits) of the listed kernel sources, concatenated."""
+    """sha256 (first 16 hex digits) of the listed kernel sources, concatenated,
+    comments and whitespace left out: a summary's DRAM counters stay valid for
+    as long as the code they were taken on is unchanged."""
     h = hashlib.sha256()
     for f in files:
-        with open(os.path.join(ROOT, "prefix_shared_kv_tree_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "prefix_shared_kv_tree_gb300", "csrc", f), encoding="utf-8") as fh:
+            h.update(strip_comments(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

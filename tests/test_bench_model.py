@@ -70,3 +70,15 @@ def test_distribution():
     d = bench.distribution([0.001 * x for x in range(1, 101)])  # 1 .. 100 us
     assert d["n"] == 100 and d["median"] == pytest.approx(50.5) and d["mean"] == pytest.approx(50.5)
     assert d["p10"] == pytest.approx(11.0) and d["p90"] == pytest.approx(90.0)
+
+
+def test_source_digest_ignores_comments_only():
+    """A kernel summary's DRAM counters stay attached to the code they were
+    taken on: comments and layout do not change the digest, code does."""
+    a = 'int f(int x) { // twice\n  return 2 * x; /* no overflow\n here */ }\nconst char* s = "//kept";\n'
+    b = 'int f(int x) {\n\n  return 2 * x;   }\n  const char* s = "//kept";  // a literal\n'
+    c = 'int f(int x) { return 3 * x; }\nconst char* s = "//kept";\n'
+    d = 'int f(int x) { return 2 * x; }\nconst char* s = "kept";\n'
+    assert bench.strip_comments(a) == bench.strip_comments(b)
+    assert bench.strip_comments(a) != bench.strip_comments(c)
+    assert bench.strip_comments(a) != bench.strip_comments(d)
