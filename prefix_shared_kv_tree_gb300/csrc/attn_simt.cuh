@@ -219,11 +219,16 @@ __global__ void __launch_bounds__(32 * (simt_max_warps(G, sizeof(T)) + 1), 1) at
   if (warp == NW) {
     // ================================================================ producer
     // Fills lane c's consumer's two item slots (c < NW).  Items are claimed
-    // for the whole CTA, NW consecutive indices per atomic; a batch's
-    // descriptors land in s_batch by one bulk copy.  Two batches are in hand
-    // and the claim of a third is in flight, so this warp never reads a
-    // register that a global load or atomic of the current step still fills
-    // (its lanes share one scoreboard: such a read would stall every lane).
+    // for the whole CTA, NW consecutive indices per atomic while more than
+    // p.claim_tail items are left, then p.claim_batch (fewer items reserved by
+    // one CTA when the list runs out, so the warps end closer together); a
+    // batch's descriptors land in s_batch by one bulk copy.  Two batches are
+    // in hand and the claim of a third is in flight, so this warp never reads
+    // a register that a global load or atomic of the current step still
+    // fills (its lanes share one scoreboard: such a read would stall every
+    // lane).
+    const int small = min(NW, max(1, p.claim_batch));
+    auto claim_size = [&](int next) { return n_items - next > p.claim_tail ? NW : small; };
     const bool mine = lane < NW;
     uint8_t* rb = smem + static_cast<size_t>(mine ? lane : 0) * L.total;
     uint8_t* slots = rb + L.slot;
@@ -231,8 +236,8 @@ __global__ void __launch_bounds__(32 * (simt_max_warps(G, sizeof(T)) + 1), 1) at
     uint64_t* sfull = bars + 2 * S;
     uint64_t* sempty = bars + 2 * S + 2;
     const T* qptr = static_cast<const T*>(p.q);
-    auto fill_batch = [&](int buf, int base) {  // lane 0
-      const int valid = max(0, min(n_items - base, NW));
+    auto fill_batch = [&](int buf, int base, int sz) {  // lane 0
+      const int valid = max(0, min(n_items - base, sz));
       if (valid > 0) {
         ptx::mbar_arrive_expect_tx(&s_bbar[buf], valid * static_cast<uint32_t>(sizeof(SimtItem)));
         ptx::bulk_g2s(&s_batch[buf][0], items + base, valid * static_cast<uint32_t>(sizeof(SimtItem)), &s_bbar[buf]);
@@ -240,17 +245,20 @@ __global__ void __launch_bounds__(32 * (simt_max_warps(G, sizeof(T)) + 1), 1) at
         ptx::mbar_arrive(&s_bbar[buf]);
       }
     };
+    // batch b: items [base_b, base_b + sz_b); pend: the claim in flight
     int base0 = 0, base1 = 0, pend = 0;
+    int sz0 = claim_size(p.claim_base), sz1 = sz0, pend_sz = sz0;
     if (lane == 0) {
-      base0 = atomicAdd(p.sched, NW) + p.claim_base;
-      base1 = atomicAdd(p.sched, NW) + p.claim_base;
+      base0 = atomicAdd(p.sched, sz0) + p.claim_base;
+      base1 = atomicAdd(p.sched, sz1) + p.claim_base;
     }
     base0 = __shfl_sync(0xffffffffu, base0, 0);
     base1 = __shfl_sync(0xffffffffu, base1, 0);
     if (lane == 0) {
-      fill_batch(0, base0);
-      fill_batch(1, base1);
-      pend = base1 + NW < n_items ? atomicAdd(p.sched, NW) + p.claim_base : n_items;
+      fill_batch(0, base0, sz0);
+      fill_batch(1, base1, sz1);
+      pend_sz = claim_size(base1 + sz1);
+      pend = base1 + sz1 < n_items ? atomicAdd(p.sched, pend_sz) + p.claim_base : n_items;
     }
     uint32_t fills0 = 1, fills1 = 1;
     int bcur = 0, bpos = 0;
@@ -260,19 +268,26 @@ __global__ void __launch_bounds__(32 * (simt_max_warps(G, sizeof(T)) + 1), 1) at
     uint64_t idle_since = 0;
     while (true) {
       // ---- next item into the consumer's next slot, once it has released it
-      const bool want = !finished && (written < 2 || ptx::mbar_test_wait(&sempty[qs], ((written >> 1) - 1) & 1));
-      const unsigned wm = __ballot_sync(0xffffffffu, want);
+      bool want = !finished && (written < 2 || ptx::mbar_test_wait(&sempty[qs], ((written >> 1) - 1) & 1));
+      unsigned wm = __ballot_sync(0xffffffffu, want);
+      // at most the rest of the two batches in hand this round
+      const int szc = bcur ? sz1 : sz0;
+      const int room = szc + (bcur ? sz0 : sz1) - bpos;
+      if (__popc(wm) > room) {
+        want = want && __popc(wm & ((1u << lane) - 1u)) < room;
+        wm = __ballot_sync(0xffffffffu, want);
+      }
       if (wm != 0u) {
         const int cnt = __popc(wm);
         // the current batch (and, past its end, the next) must have landed
         bool ok = ptx::mbar_wait(&s_bbar[bcur], ((bcur ? fills1 : fills0) - 1) & 1, abort_flag, p.err);
-        if (bpos + cnt > NW)
+        if (bpos + cnt > szc)
           ok = ok && ptx::mbar_wait(&s_bbar[bcur ^ 1], ((bcur ? fills0 : fills1) - 1) & 1, abort_flag, p.err);
         if (!__all_sync(0xffffffffu, ok)) break;
         if (want) {
           const int pos = bpos + __popc(wm & ((1u << lane) - 1u));
-          const int buf = pos < NW ? bcur : (bcur ^ 1);
-          const int i = pos < NW ? pos : pos - NW;
+          const int buf = pos < szc ? bcur : (bcur ^ 1);
+          const int i = pos < szc ? pos : pos - szc;
           const int idx = (buf ? base1 : base0) + i;
           const int4* d = reinterpret_cast<const int4*>(&s_batch[buf][i]);
           SimtMeta cur;
@@ -304,23 +319,27 @@ __global__ void __launch_bounds__(32 * (simt_max_warps(G, sizeof(T)) + 1), 1) at
           if (++qs == 2) qs = 0;
         }
         bpos += cnt;
-        if (bpos >= NW) {
+        if (bpos >= szc) {
           // The current batch is used up (every read of it above fed a store
           // that has issued): refill its buffer with the batch claimed last time.
           const int nb = __shfl_sync(0xffffffffu, pend, 0);
+          const int nsz = __shfl_sync(0xffffffffu, pend_sz, 0);
           if (bcur == 0) {
             base0 = nb;
+            sz0 = nsz;
             ++fills0;
           } else {
             base1 = nb;
+            sz1 = nsz;
             ++fills1;
           }
           if (lane == 0) {
-            fill_batch(bcur, nb);
-            pend = nb + NW < n_items ? atomicAdd(p.sched, NW) + p.claim_base : n_items;
+            fill_batch(bcur, nb, nsz);
+            pend_sz = claim_size(nb + nsz);
+            pend = nb + nsz < n_items ? atomicAdd(p.sched, pend_sz) + p.claim_base : n_items;
           }
           bcur ^= 1;
-          bpos -= NW;
+          bpos -= szc;
         }
       }
       if (__all_sync(0xffffffffu, finished)) break;

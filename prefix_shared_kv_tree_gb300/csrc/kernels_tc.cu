@@ -421,6 +421,7 @@ __global__ void __launch_bounds__(512, 1) attn_tc_kernel(const AttnParams p) {
       len_n = lane < tiles_of(wn) ? tile_len(wn, lane) : 0;
     };
     prefetch(i0);
+    const float sc = p.scale_log2;
     int t = 0;
     bool ok = true;
     for (int ii = i0; ii < i1 && ok; ++ii) {
@@ -440,7 +441,7 @@ __global__ void __launch_bounds__(512, 1) attn_tc_kernel(const AttnParams p) {
         // valid keys of this thread's half of the tile
         const int lim = min(__shfl_sync(0xffffffffu, my_len, c & 31), key_limit - c * kC) - hf * HK;
         const int b = t & 1, sb = t % SB;
-        // polled now, waited for below: the answer arrives during the max
+        // polled now, waited for below: the answer arrives during the exponentials
         const bool p_ready = t < 2 || ptx::mbar_test_wait(&pfree[b], ((t - 2) >> 1) & 1);
         if (!wait_all(&sfull[sb], (t / SB) & 1)) {
           ok = false;
@@ -454,8 +455,8 @@ __global__ void __launch_bounds__(512, 1) attn_tc_kernel(const AttnParams p) {
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(&sfree[sb]);  // one arrival per warp
 
-        // Raw scores; the chunk max is taken before scaling (the scale is
-        // positive), and the scale is folded into the exponent's FMA below.
+        // Raw scores; the max is taken before scaling (the scale is positive),
+        // and the scale is folded into the exponent's FMA.
         float x[HK];
 #pragma unroll
         for (int k2 = 0; k2 < HK; ++k2) x[k2] = __uint_as_float(sv[k2]);
@@ -464,75 +465,86 @@ __global__ void __launch_bounds__(512, 1) attn_tc_kernel(const AttnParams p) {
           for (int k2 = 0; k2 < HK; ++k2)
             if (k2 >= lim) x[k2] = -INFINITY;
         }
-        float mq[HK / 4];
-#pragma unroll
-        for (int k2 = 0; k2 < HK / 4; ++k2)
-          mq[k2] = fmaxf(fmaxf(x[4 * k2], x[4 * k2 + 1]), fmaxf(x[4 * k2 + 2], x[4 * k2 + 3]));
-#pragma unroll
-        for (int w2 = HK / 8; w2 >= 1; w2 >>= 1)
-#pragma unroll
-          for (int k2 = 0; k2 < w2; ++k2) mq[k2] = fmaxf(mq[k2], mq[k2 + w2]);
-        const float mxr = fmaxf(mq[0], __shfl_xor_sync(0xffffffffu, mq[0], 16));  // the row's other half
-        const float mx = mxr * p.scale_log2;
-        // Move the reference max: always on the item's first chunk (nothing
-        // accumulated yet); later only when this chunk's max runs past it.
-        // Both halves of a row take the same decision.
-        const bool move = (c == 0) || (mx > m + kRescale);
-        const float m_old_use = (m == -INFINITY) ? 0.f : m;
-        if (move) m = fmaxf(m, mx);
-        const float m_use = (m == -INFINITY) ? 0.f : m;
-        if (c > 0 && __any_sync(0xffffffffu, move)) {
-          // O so far (through chunk c-1) and l get the factor 2^(old - new):
-          // wait for that chunk's PV product, then rescale this half in place.
-          const float alpha = move ? ptx::ex2(m_old_use - m_use) : 1.f;
-          if (!wait_all(&pfree[(t - 1) & 1], ((t - 1) >> 1) & 1)) {
-            ok = false;
-            break;
-          }
-          ptx::tc_fence_after();
-#pragma unroll
-          for (int cg = 0; cg < HD / 32; ++cg) {
-            uint32_t ov[32];
-            ptx::tmem_ld32_half<HD>(tl + O_COL + ob * D + 32 * cg, ov);
-            ptx::tmem_ld_wait(ov);
-#pragma unroll
-            for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
-            ptx::tmem_st32_half<HD>(tl + O_COL + ob * D + 32 * cg, ov);
-          }
-          ptx::tmem_st_wait();
-          l *= alpha;
-        }
-        // P buffer b is free once the PV product of chunk t-2 has completed.
-        if (__any_sync(0xffffffffu, !p_ready) && !wait_all(&pfree[b], ((t - 2) >> 1) & 1)) {
-          ok = false;
-          break;
-        }
         // P = 2^(x * scale - m), rounded to the operand type (bf16: plus the
         // rounded remainder); the row sum adds the values the PV product reads
         // (so o / n stays a weighted mean of V rows): the rounded ones for
         // fp16, for bf16 the unrounded ones, which hi + lo matches to 2^-17.
-        // Four partial sums for a shorter chain.
-        const float neg_m = -m_use, sc = p.scale_log2;
-        float ps[4] = {0.f, 0.f, 0.f, 0.f};
         uint32_t pw[HK / 2], pr[HK / 2];  // pr: the remainders (bf16 only)
+        float2 ps[2];
+        auto exps = [&](float m_ref) {
+          const float2 sc2 = make_float2(sc, sc), nm2 = make_float2(-m_ref, -m_ref);
+          ps[0] = ps[1] = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int j = 0; j < HK / 8; ++j) {
-          float e[8];
-#pragma unroll
-          for (int q = 0; q < 8; ++q) e[q] = ptx::ex2(fmaf(x[8 * j + q], sc, neg_m));
-#pragma unroll
-          for (int q = 0; q < 4; ++q) pw[4 * j + q] = pack2_plain<T>(e[2 * q], e[2 * q + 1]);
-          if constexpr (PSPLIT) {
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const float h0 = lo16<T>(pw[4 * j + q]), h1 = hi16<T>(pw[4 * j + q]);
-              pr[4 * j + q] = pack2_plain<T>(e[2 * q] - h0, e[2 * q + 1] - h1);
-              ps[q] += e[2 * q] + e[2 * q + 1];
+          for (int q = 0; q < HK / 2; ++q) {
+            const float2 a = __ffma2_rn(make_float2(x[2 * q], x[2 * q + 1]), sc2, nm2);
+            const float2 e = make_float2(ptx::ex2(a.x), ptx::ex2(a.y));
+            pw[q] = pack2_plain<T>(e.x, e.y);
+            if constexpr (PSPLIT) {
+              const float2 h = make_float2(lo16<T>(pw[q]), hi16<T>(pw[q]));
+              const float2 d = __ffma2_rn(h, make_float2(-1.f, -1.f), e);  // e - h, exact
+              pr[q] = pack2_plain<T>(d.x, d.y);
+              ps[q & 1] = __fadd2_rn(ps[q & 1], e);
+            } else {
+              ps[q & 1] = __fadd2_rn(ps[q & 1], make_float2(lo16<T>(pw[q]), hi16<T>(pw[q])));
             }
-          } else {
-#pragma unroll
-            for (int q = 0; q < 4; ++q) ps[q] += sum2_16<T>(pw[4 * j + q]);
           }
+        };
+        // this half's max
+        float mq[HK / 4];
+#pragma unroll
+        for (int k2 = 0; k2 < HK / 4; ++k2)
+          mq[k2] = ptx::fmax3(fmaxf(x[4 * k2], x[4 * k2 + 1]), x[4 * k2 + 2], x[4 * k2 + 3]);
+#pragma unroll
+        for (int w2 = HK / 8; w2 >= 1; w2 >>= 1)
+#pragma unroll
+          for (int k2 = 0; k2 < w2; ++k2) mq[k2] = fmaxf(mq[k2], mq[k2 + w2]);
+        const float hmax = mq[0];
+        // Past an item's first tile the exponentials are taken against the
+        // current reference at once; they stand unless some row of the warp
+        // has a score past the reference by more than kRescale (then the
+        // reference moves and they are taken again below).
+        bool redo = (c == 0);
+        if (!redo) {
+          exps(m == -INFINITY ? 0.f : m);
+          redo = __any_sync(0xffffffffu, hmax * sc > m + kRescale);
+        }
+        if (redo) {
+          const float mxr = fmaxf(hmax, __shfl_xor_sync(0xffffffffu, hmax, 16));  // the row's other half
+          const float mx = mxr * sc;
+          // Move the reference max: always on the item's first tile (nothing
+          // accumulated yet); later only when this tile's max runs past it.
+          // Both halves of a row take the same decision.
+          const bool move = (c == 0) || (mx > m + kRescale);
+          const float m_old_use = (m == -INFINITY) ? 0.f : m;
+          if (move) m = fmaxf(m, mx);
+          const float m_use = (m == -INFINITY) ? 0.f : m;
+          if (c > 0 && __any_sync(0xffffffffu, move)) {
+            // O so far (through tile c-1) and l get the factor 2^(old - new):
+            // wait for that tile's PV product, then rescale this half in place.
+            const float alpha = move ? ptx::ex2(m_old_use - m_use) : 1.f;
+            if (!wait_all(&pfree[(t - 1) & 1], ((t - 1) >> 1) & 1)) {
+              ok = false;
+              break;
+            }
+            ptx::tc_fence_after();
+#pragma unroll 1
+            for (int cg = 0; cg < HD / 32; ++cg) {
+              uint32_t ov[32];
+              ptx::tmem_ld32_half<HD>(tl + O_COL + ob * D + 32 * cg, ov);
+              ptx::tmem_ld_wait(ov);
+#pragma unroll
+              for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+              ptx::tmem_st32_half<HD>(tl + O_COL + ob * D + 32 * cg, ov);
+            }
+            ptx::tmem_st_wait();
+            l *= alpha;
+          }
+          exps(m_use);
+        }
+        // P buffer b is free once the PV product of tile t-2 has completed.
+        if (__any_sync(0xffffffffu, !p_ready) && !wait_all(&pfree[b], ((t - 2) >> 1) & 1)) {
+          ok = false;
+          break;
         }
         // this half's 32 keys are P columns [16 hf, 16 hf + 16) (two keys per column)
         ptx::tmem_st16_half<HK / 2>(tl + P_COL + b * PW, pw);
@@ -541,7 +553,8 @@ __global__ void __launch_bounds__(512, 1) attn_tc_kernel(const AttnParams p) {
         ptx::tc_fence_before();  // orders the TMEM stores above before the PV product
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(&pfull[b]);  // one arrival per warp
-        l += (ps[0] + ps[1]) + (ps[2] + ps[3]);
+        const float2 ps2 = __fadd2_rn(ps[0], ps[1]);
+        l += ps2.x + ps2.y;
       }
       if (!ok) break;
       prefetch(ii + 1);

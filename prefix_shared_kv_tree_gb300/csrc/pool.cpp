@@ -166,6 +166,10 @@ struct pst_pool {
   int32_t tc_max_run = 32;  // chunk-first items: at most this many 64-key tiles
   int32_t merge_cap = 0, merge_cap_forced = -1;
   int32_t simt_grid = 0, simt_stages = 3, simt_wpc = 8;
+  // sequence-first claims: simt_wpc items each until at most
+  // simt_claim_tail * (consumer warps) items are left, then simt_batch
+  int32_t simt_batch = 2;
+  double simt_claim_tail = 4.0;
   int64_t n_part_rows = 0, shared_chunks = 0;
   std::vector<int32_t> canon_shared;   // 4 per row
   std::vector<int32_t> canon_entries;  // 2 per entry
@@ -794,6 +798,8 @@ AttnParams base_params(const pst_pool* p, int32_t layer) {
   a.scale_log2 = p->scale_log2;
   a.stages = p->simt_stages;
   a.warps_per_cta = p->simt_wpc;
+  a.claim_batch = p->simt_batch > 0 ? p->simt_batch : p->simt_wpc;
+  a.claim_tail = static_cast<int32_t>(std::min<double>(INT32_MAX, p->simt_claim_tail * p->n_simt_warps));
   a.err = p->d_err;
   a.sched = p->d_sched;
   a.merge_cap = p->merge_cap;
@@ -862,6 +868,8 @@ pst_status pst_pool_create(const pst_config* cfg, int device, pst_pool** out) {
   if (const char* e = std::getenv("PST_MERGE_CAP")) p->merge_cap_forced = std::max(0, std::atoi(e));
   if (const char* e = std::getenv("PST_SIMT_TAIL")) p->simt_tail = std::max(0.0, std::atof(e));
   if (const char* e = std::getenv("PST_SPLIT_PREFILL")) p->split_prefill = std::atoi(e) != 0;
+  if (const char* e = std::getenv("PST_SIMT_BATCH")) p->simt_batch = std::max(0, std::atoi(e));
+  if (const char* e = std::getenv("PST_SIMT_CLAIM_TAIL")) p->simt_claim_tail = std::max(0.0, std::atof(e));
   // Sequence-first kernel shape: up to 8 consumer warps (plus the producer
   // warp) x up to 6 stages of 8 KB pieces, as far as shared memory allows
   p->simt_wpc = attn_simt_max_warps(c.dtype, g);

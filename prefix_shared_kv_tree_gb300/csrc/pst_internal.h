@@ -76,7 +76,8 @@ struct AttnParams {
   int32_t first_items;        // CUDA-core kernel: items [0, first_items) go to consumer blockIdx * NW + warp
   int32_t claim_base;         // CUDA-core kernel: claimed index = counter value + claim_base
   int32_t n_items;
-  int32_t n_warps;            // unused
+  int32_t claim_batch;        // CUDA-core kernel: items per claim once at most claim_tail are left
+  int32_t claim_tail;         //   (before that, warps_per_cta per claim)
   const void* q;              // [groups][Hq][D]
   void* out;                  // final mode: [groups][Hq][D]
   float* part_o;              // partial mode: [rows][D]
