@@ -51,12 +51,24 @@ constexpr int kSimtPieceRows = PST_SIMT_PIECE_ROWS;
 
 static_assert(kSimtPieceRows == 32 || kSimtPieceRows == 64, "piece rows");
 
+// Pieces per ring stage.  With 16-bit K/V, chunks shorter than a piece
+// (16 or 32 keys) make pieces of 2 or 4 KB that are consecutive, equal blocks
+// of the tile image (each 128-byte K column block of C rows, then each run of
+// 64 V^T rows of C * 2 bytes): a stage then holds up to 8 KB of consecutive
+// pieces, staged by one bulk copy and waited for once.
+__host__ __device__ inline int simt_pieces_per_stage(int C, int D, int es) {
+  if (es != 2 || C >= kSimtPieceRows) return 1;
+  const int np = D / 32;         // pieces per tile: 2 C D bytes in pieces of 128 C bytes
+  const int fit = 8192 / (128 * C);
+  return np < fit ? np : fit;
+}
+
 __host__ __device__ inline size_t simt_stage_bytes(int C, int D, int es) {
   const int kr = C < kSimtPieceRows ? C : kSimtPieceRows;
   const int vr = D < kSimtPieceRows ? D : kSimtPieceRows;
   const size_t kpb = static_cast<size_t>(kr) * 128;
   const size_t vpb = ((C * es) % 128 == 0) ? static_cast<size_t>(vr) * 128 : static_cast<size_t>(vr) * C * es;
-  return kpb > vpb ? kpb : vpb;
+  return (kpb > vpb ? kpb : vpb) * simt_pieces_per_stage(C, D, es);
 }
 
 // Consumer warps per CTA at most (one more warp produces).  16-bit K/V take
@@ -171,11 +183,16 @@ __global__ void __launch_bounds__(32 * (simt_max_warps(G, sizeof(T)) + 1), 1) at
   constexpr int VG = D / VPR;                            // V^T pieces per column block
   constexpr int VT = VPR / 32;                           // feature rows per lane per V^T piece
   constexpr int NP = KB * KPC + VB * VG;                 // pieces per tile
+  constexpr int PPS = C < kSimtPieceRows && ES == 2 ? (D / 32 < 8192 / (128 * C) ? D / 32 : 8192 / (128 * C)) : 1;
   constexpr int DPL = D / 32;      // output features per lane
   constexpr int KCH = 128 / 16;    // 16-byte chunks per K piece row
   constexpr int VCH = VSW ? 8 : C * ES / 16;             // 16-byte chunks per V^T piece row
   constexpr uint32_t KPB = static_cast<uint32_t>(KPR) * 128u;
   constexpr uint32_t VPB = VSW ? static_cast<uint32_t>(VPR) * 128u : static_cast<uint32_t>(VPR) * C * ES;
+  // several pieces per stage (see simt_pieces_per_stage): equal, consecutive
+  // blocks of the tile image
+  static_assert(PPS == 1 || (KPC == 1 && !VSW && VPR == 64 && KPB == VPB && NP % PPS == 0 && PPS * KPB <= 8192),
+                "pieces per stage");
   constexpr uint32_t HALF = static_cast<uint32_t>(C) * D * ES;
   constexpr size_t TILE = 2 * static_cast<size_t>(HALF);
   constexpr uint32_t QBYTES = static_cast<uint32_t>(G) * D * ES;
@@ -441,6 +458,7 @@ __global__ void __launch_bounds__(32 * (simt_max_warps(G, sizeof(T)) + 1), 1) at
         src = tile + HALF + (VSW ? (static_cast<size_t>(vb) * D * 128 + vg * VPB) : static_cast<size_t>(vg) * VPB);
         bytes = VPB;
       }
+      bytes *= PPS;  // the stage's PPS consecutive pieces
       if (lane == 0) {
         ptx::mbar_arrive_expect_tx_relaxed(&full[ps], bytes);
         if (p.kv_evict_first)
@@ -450,7 +468,8 @@ __global__ void __launch_bounds__(32 * (simt_max_warps(G, sizeof(T)) + 1), 1) at
       }
       ++issued;
       if (++ps == S) ps = 0;
-      if (++pp == NP) {
+      pp += PPS;
+      if (pp == NP) {
         pp = 0;
         if (++pc == s_n) {
           ++si;
@@ -584,11 +603,11 @@ __global__ void __launch_bounds__(32 * (simt_max_warps(G, sizeof(T)) + 1), 1) at
 #pragma unroll
           for (int kp = 0; kp < KB * KPC; ++kp) {
             const int kb = kp / KPC, kh = kp % KPC;  // feature block of 64, key run kh * KPR
-            if (!ptx::mbar_wait(&full[cs], cph, abort_flag, p.err)) {
+            if (kp % PPS == 0 && !ptx::mbar_wait(&full[cs], cph, abort_flag, p.err)) {
               aborted = true;
               break;
             }
-            const uint32_t kt = ptx::smem_u32(stages + static_cast<size_t>(cs) * L.stage);
+            const uint32_t kt = ptx::smem_u32(stages + static_cast<size_t>(cs) * L.stage) + (kp % PPS) * KPB;
             // A fragments one k-step ahead of the products that use them, so
             // every product finds its operands loaded
             uint32_t af[2][KMT][4];
@@ -607,13 +626,15 @@ __global__ void __launch_bounds__(32 * (simt_max_warps(G, sizeof(T)) + 1), 1) at
               for (int t = 0; t < KMT; ++t)
                 ptx::mma_16816<BF>(sacc[kh * KMT + t], af[ks & 1][t], qf[kb * 4 + ks][0], qf[kb * 4 + ks][1]);
             }
-            __syncwarp();  // every lane is done with the stage
-            ++consumed;
-            if (++cs == S) {
-              cs = 0;
-              cph ^= 1u;
+            if (kp % PPS == PPS - 1) {
+              __syncwarp();  // every lane is done with the stage
+              ++consumed;
+              if (++cs == S) {
+                cs = 0;
+                cph ^= 1u;
+              }
+              issue_next();
             }
-            issue_next();
           }
           if (aborted) break;
 
@@ -702,11 +723,12 @@ __global__ void __launch_bounds__(32 * (simt_max_warps(G, sizeof(T)) + 1), 1) at
 #pragma unroll
           for (int vp = 0; vp < VB * VG; ++vp) {
             const int vb = vp / VG, vg = vp % VG;
-            if (!ptx::mbar_wait(&full[cs], cph, abort_flag, p.err)) {
+            const int jp = KB * KPC + vp;  // the piece's index in the tile
+            if (jp % PPS == 0 && !ptx::mbar_wait(&full[cs], cph, abort_flag, p.err)) {
               aborted = true;
               break;
             }
-            const uint32_t vt = ptx::smem_u32(stages + static_cast<size_t>(cs) * L.stage);
+            const uint32_t vt = ptx::smem_u32(stages + static_cast<size_t>(cs) * L.stage) + (jp % PPS) * VPB;
             uint32_t af[2][VMT][4];
             auto load_v = [&](int ks, uint32_t (&dst)[VMT][4]) {
               const int j = ks * 2 + a_hi;
@@ -727,13 +749,15 @@ __global__ void __launch_bounds__(32 * (simt_max_warps(G, sizeof(T)) + 1), 1) at
                   ptx::mma_16816<BF>(o[vg * VMT + t], af[ks & 1][t], pfr[vb * VKS + ks][0], pfr[vb * VKS + ks][1]);
               }
             }
-            __syncwarp();  // every lane is done with the stage (and with P^T before the next chunk)
-            ++consumed;
-            if (++cs == S) {
-              cs = 0;
-              cph ^= 1u;
+            if (jp % PPS == PPS - 1) {
+              __syncwarp();  // every lane is done with the stage (and with P^T before the next chunk)
+              ++consumed;
+              if (++cs == S) {
+                cs = 0;
+                cph ^= 1u;
+              }
+              issue_next();
             }
-            issue_next();
           }
         }
         if (aborted) break;
