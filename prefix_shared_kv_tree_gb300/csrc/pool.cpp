@@ -683,18 +683,29 @@ pst_status rebuild(pst_pool* p) {
       it[7] = 0;
     }
     warp_items.assign(1, 0);
-    // Claims near the end: two items while the last items carry at least
-    // 18 KiB each on average (measured best for 32 KiB tiles: fewer items
-    // reserved by one CTA, so the warps end together); one per consumer warp
-    // for smaller items (d = 64 tiles, short chunks), whose warps would
-    // otherwise wait for their claims (measured: 44.0 against 32.6 us per
-    // step at d = 64, c = 64, two items against eight).
+    // Claims near the end of the list: two items (fewer items reserved by one
+    // CTA, so the warps end together) where that was measured to pay: this
+    // kernel's end is the step's end (it runs alone, or first as the longer
+    // phase), the last items take a warp at least ~2.7 us each (about two
+    // claim round trips, so a claim of two comes back before the warps run
+    // out), and the chunk-first kernel holds at most a quarter of the SMs or
+    // the query group is 2 or more.  Otherwise one item per consumer warp.
+    // (Measured, two against eight, us per step: share1k 52.2 / 53.6,
+    // gqa_tree 60.9 / 63.6, d = 128 with c = 16 58.9 / 59.7, noshare
+    // 302 / 308; against: d = 64, c = 64 44.0 / 32.6, b = 96 with 64
+    // private tokens 39.9 / 34.3, 4096 shared + 512 private tokens 66.6 /
+    // 60.6, 1024 + 256 35.9 / 32.9.)  A warp streams at the GPU's DRAM rate
+    // shared by the W streaming warps, at most ~110 GB/s per SM.
     const size_t n_tail = std::min(ordered.size(), static_cast<size_t>(p->simt_claim_tail * p->n_simt_warps));
     int64_t tail_chunks = 0;
     for (size_t x = ordered.size() - n_tail; x < ordered.size(); ++x) tail_chunks += ordered[x].n;
     const double tile_bytes = 2.0 * p->C * p->D * p->es;
     const double mean_bytes = n_tail > 0 ? tile_bytes * static_cast<double>(tail_chunks) / n_tail : 0.0;
-    p->simt_batch_end = mean_bytes >= 18.0 * 1024 ? 2 : p->simt_wpc;
+    const double warp_gbs = std::min(p->hbm_gbs / std::max<int64_t>(1, W), 110.0 / p->simt_wpc);
+    const double item_us = mean_bytes / (warp_gbs * 1e3);
+    const bool ends_step = p->n_tc_items == 0 || p->simt_first;
+    const bool pays = 4 * p->n_tc_ctas <= p->n_sm || g >= 2;
+    p->simt_batch_end = (ends_step && pays && item_us >= 2.7) ? 2 : p->simt_wpc;
   }
   p->n_simt_items = static_cast<int32_t>(simt_items.size() / 8);
   p->n_part_rows = static_cast<int64_t>(ents.size()) * g;
