@@ -594,7 +594,13 @@ __global__ void __launch_bounds__(512, 1) attn_tc_kernel(const AttnParams p) {
         grp = w.group0 + rr / p.g;
         hg = rr % p.g;
       }
-      const int part_row = (row_valid && !p.final_mode) ? __ldg(p.row_idx + w.part_base + r) : 0;
+      // partial row: from the decode tables' row map, or, for a prefill block
+      // cut along the keys (piece part_base of its rows), entry part_base of
+      // the (token, KV head) pair's entries
+      int part_row = 0;
+      if (row_valid && !p.final_mode)
+        part_row = p.causal_p0 >= 0 ? (__ldg(p.m_off + grp * p.Hkv + w.kv) + w.part_base) * p.g + hg
+                                    : __ldg(p.row_idx + w.part_base + r);
       if (!wait_all(&ofull[ob], (it >> 1) & 1)) break;
       if (!wait_all(&mlfull[ob], (it >> 1) & 1)) break;
       ptx::tc_fence_after();

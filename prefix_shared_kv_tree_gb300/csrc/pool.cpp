@@ -200,10 +200,13 @@ struct pst_pool {
   float* d_ppart_ml = nullptr;
   size_t ppart_cap = 0;  // rows
   bool split_prefill = true;
-  int32_t* h_stage = nullptr;  // pinned upload staging
-  size_t stage_cap = 0;
-  cudaEvent_t ev_stage = nullptr;
-  bool stage_pending = false;
+  // pinned upload staging, two buffers used in turn: an upload waits only for
+  // the copy out of the buffer two uploads back, not for the one just issued
+  int32_t* h_stage[2] = {nullptr, nullptr};
+  size_t stage_cap[2] = {0, 0};
+  cudaEvent_t ev_stage[2] = {nullptr, nullptr};
+  bool stage_pending[2] = {false, false};
+  int stage_next = 0;
   void* d_q = nullptr;
   void* d_out = nullptr;
   size_t qo_cap = 0;  // bytes each
@@ -350,20 +353,22 @@ pst_status upload(pst_pool* p, int32_t** dbuf, size_t* dcap, const std::vector<i
     CUDA_TRY(cudaMalloc(dbuf, cap * sizeof(int32_t)));
     *dcap = cap;
   }
-  if (p->stage_pending) {
-    CUDA_TRY(cudaEventSynchronize(p->ev_stage));
-    p->stage_pending = false;
+  const int b = p->stage_next;
+  p->stage_next ^= 1;
+  if (p->stage_pending[b]) {
+    CUDA_TRY(cudaEventSynchronize(p->ev_stage[b]));
+    p->stage_pending[b] = false;
   }
-  if (n > p->stage_cap) {
-    if (p->h_stage) CUDA_TRY(cudaFreeHost(p->h_stage));
+  if (n > p->stage_cap[b]) {
+    if (p->h_stage[b]) CUDA_TRY(cudaFreeHost(p->h_stage[b]));
     size_t cap = std::max<size_t>(n * 3 / 2, 4096);
-    CUDA_TRY(cudaMallocHost(&p->h_stage, cap * sizeof(int32_t)));
-    p->stage_cap = cap;
+    CUDA_TRY(cudaMallocHost(&p->h_stage[b], cap * sizeof(int32_t)));
+    p->stage_cap[b] = cap;
   }
-  std::memcpy(p->h_stage, src.data(), n * sizeof(int32_t));
-  CUDA_TRY(cudaMemcpyAsync(*dbuf, p->h_stage, n * sizeof(int32_t), cudaMemcpyHostToDevice, s));
-  CUDA_TRY(cudaEventRecord(p->ev_stage, s));
-  p->stage_pending = true;
+  std::memcpy(p->h_stage[b], src.data(), n * sizeof(int32_t));
+  CUDA_TRY(cudaMemcpyAsync(*dbuf, p->h_stage[b], n * sizeof(int32_t), cudaMemcpyHostToDevice, s));
+  CUDA_TRY(cudaEventRecord(p->ev_stage[b], s));
+  p->stage_pending[b] = true;
   return PST_OK;
 }
 
@@ -938,7 +943,8 @@ pst_status pst_pool_create(const pst_config* cfg, int device, pst_pool** out) {
     if ((e = cudaStreamCreateWithFlags(&p->aux, cudaStreamNonBlocking)) != cudaSuccess) return bail(e, "stream");
     if ((e = cudaEventCreateWithFlags(&p->ev_fork, cudaEventDisableTiming)) != cudaSuccess) return bail(e, "event");
     if ((e = cudaEventCreateWithFlags(&p->ev_join, cudaEventDisableTiming)) != cudaSuccess) return bail(e, "event");
-    if ((e = cudaEventCreateWithFlags(&p->ev_stage, cudaEventDisableTiming)) != cudaSuccess) return bail(e, "event");
+    for (int b = 0; b < 2; ++b)
+      if ((e = cudaEventCreateWithFlags(&p->ev_stage[b], cudaEventDisableTiming)) != cudaSuccess) return bail(e, "event");
     for (auto& ev : p->pev)
       if ((e = cudaEventCreate(&ev)) != cudaSuccess) return bail(e, "event");
     // The fixed area of pst_decode_attention_noalloc belongs to a module of
@@ -971,14 +977,16 @@ pst_status pst_pool_free(pst_pool* p) {
     cudaFree(p->d_ppart_ml);
     cudaFree(p->d_q);
     cudaFree(p->d_out);
-    if (p->h_stage) cudaFreeHost(p->h_stage);
+    for (int b = 0; b < 2; ++b)
+      if (p->h_stage[b]) cudaFreeHost(p->h_stage[b]);
     if (p->aux) cudaStreamDestroy(p->aux);
     for (auto& gc : p->graphs)
       if (gc.exec) cudaGraphExecDestroy(gc.exec);
     if (p->cap_stream) cudaStreamDestroy(p->cap_stream);
     if (p->ev_fork) cudaEventDestroy(p->ev_fork);
     if (p->ev_join) cudaEventDestroy(p->ev_join);
-    if (p->ev_stage) cudaEventDestroy(p->ev_stage);
+    for (int b = 0; b < 2; ++b)
+      if (p->ev_stage[b]) cudaEventDestroy(p->ev_stage[b]);
     for (auto& ev : p->pev)
       if (ev) cudaEventDestroy(ev);
   }
@@ -1507,13 +1515,13 @@ static pst_status prefill_attention_tc(pst_pool* p, const AttnParams& base, cons
     n_pieces += t.nsplit;
   }
 
-  // table image: chunk ids, items, per-CTA item ranges, merge CSR, row map
+  // table image: chunk ids, items, per-CTA item ranges, merge CSR
   std::vector<int32_t> tab(path_chunks);
   while (tab.size() % 8) tab.push_back(0);
   const size_t off_items = tab.size();
   std::vector<WorkItem> items;
   items.reserve(n_pieces);
-  std::vector<int32_t> moff, row_idx;
+  std::vector<int32_t> moff;
   if (split) {
     moff.assign(static_cast<size_t>(W) * Hkv + 1, 0);
     for (const auto& t : tiles)
@@ -1532,13 +1540,7 @@ static pst_status prefill_attention_tc(pst_pool* p, const AttnParams& base, cons
       w.row0 = t.r0;
       w.n_rows = t.n_rows;
       w.key0 = c0 * C;
-      if (split) {
-        w.part_base = static_cast<int32_t>(row_idx.size());
-        for (int32_t r = 0; r < t.n_rows; ++r) {
-          const int32_t tok = (t.r0 + r) / g, hg = (t.r0 + r) % g;
-          row_idx.push_back((moff[static_cast<size_t>(tok) * Hkv + t.kv] + sp) * g + hg);
-        }
-      }
+      w.part_base = sp;  // partial rows: entry moff[token * Hkv + kv] + sp of each row's pair (the kernel)
       items.push_back(w);
     }
   }
@@ -1567,8 +1569,6 @@ static pst_status prefill_attention_tc(pst_pool* p, const AttnParams& base, cons
   tab.insert(tab.end(), count.begin(), count.end());
   const size_t off_moff = tab.size();
   tab.insert(tab.end(), moff.begin(), moff.end());
-  const size_t off_rows = tab.size();
-  tab.insert(tab.end(), row_idx.begin(), row_idx.end());
   pst_status st = upload(p, &p->d_pre, &p->pre_cap, tab, s);
   if (st != PST_OK) return st;
 
@@ -1597,7 +1597,7 @@ static pst_status prefill_attention_tc(pst_pool* p, const AttnParams& base, cons
     a.part_o = p->d_ppart_o;
     a.part_ml = p->d_ppart_ml;
     a.m_off = p->d_pre + off_moff;
-    a.row_idx = p->d_pre + off_rows;
+    a.row_idx = nullptr;  // the kernel places each row from m_off and its piece index
     int32_t max_ent = 0;
     for (const auto& t : tiles) max_ent = std::max(max_ent, t.nsplit);
     const int32_t by_smem = static_cast<int32_t>((64 * 1024) / (4 * static_cast<size_t>(g) * p->D * sizeof(float)));

@@ -47,7 +47,8 @@ struct WorkItem {
   int32_t group0;
   int32_t row0;
   int32_t n_rows;
-  int32_t part_base;  // partial mode: row r's partial row is row_idx[part_base + r]
+  int32_t part_base;  // partial mode: row r's partial row is row_idx[part_base + r] (decode), or,
+                      // for a prefill block cut along the keys, entry m_off[pair] + part_base
   int32_t key0;       // causal mode: position of the item's first key in its sequence
 };
 static_assert(sizeof(WorkItem) == 32, "WorkItem layout");
