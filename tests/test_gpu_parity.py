@@ -128,7 +128,8 @@ CASES = [
     ("f16", 2, 2, 128, 128, 0, 2**31 - 1),
     ("f32", 8, 2, 128, 128, 0, 0),          # one fp32 accumulator pair per key
     ("f32", 8, 1, 128, 128, 0, 0),
-    # c = 16: one 16-key tile per chunk (16-bit), half a warp of keys (fp32)
+    # c = 16: four chunks per 64-key tile of the tensor-core kernel; a whole
+    # chunk per sequence-first stage (16-bit), half a warp of keys (fp32)
     ("f16", 4, 4, 128, 16, 0, 0),
     ("bf16", 8, 2, 64, 16, 0, 0),
     ("bf16", 8, 1, 128, 16, 0, 2**31 - 1),
@@ -137,6 +138,9 @@ CASES = [
     # the largest query group with the smallest chunks, and g = 8 on tensor cores
     ("bf16", 8, 1, 128, 32, 0, 0),
     ("f16", 8, 1, 128, 64, 0, 0),
+    # d = 64, c = 32: a sequence-first stage holds a chunk's K and V^T pieces
+    ("f16", 4, 2, 64, 32, 0, 2**31 - 1),
+    ("bf16", 8, 2, 64, 32, 0, 0),
 ]
 
 
