@@ -602,6 +602,7 @@ def run_ours(args):
         launches[0] += pool.last_launch_count()
     times = time_steps(step, args.steps, args.warmup, flush, stream)
     launches = launches[0] * args.steps // (args.steps + max(3, args.warmup))
+    st = pool.stats()  # the timed workload's tables (the decode loop below grows the tree)
     if world > 1:
         torch.distributed.barrier()
     clk = clocks.stop()
@@ -699,7 +700,6 @@ def run_ours(args):
         assert pool.check_device() == 0
 
     hbm, tf_peak, peak_kind = measured_peaks()
-    st = pool.stats()
     phase_ms = [sum(p[j] for p in phase) / len(phase) for j in range(3)]
     names = ["chunk_first_tc", "sequence_first_simt", "whole_call"]
     dom = max(range(2), key=lambda j: phase_ms[j])  # the dominant kernel (not the whole call)
