@@ -712,7 +712,8 @@ def run_ours(args):
     del wl
     torch.cuda.empty_cache()
 
-    # ---- the other workloads of the survey's table, measured in this run
+    # ---- the other decode workloads (share4k, noshare, gqa_tree, and the
+    # sequence-first-only controls), measured in this run
     configs = None
     if world == 1 and not args.no_configs:
         csteps = max(20, min(args.steps, 200))
