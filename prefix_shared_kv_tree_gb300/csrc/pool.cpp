@@ -164,6 +164,7 @@ struct pst_pool {
   // last simt_tail * W chunks as single-chunk items
   double simt_unit_div = 8.0, simt_tail = 2.0;
   int32_t tc_max_run = 32;  // chunk-first items: at most this many 64-key tiles
+  int32_t tc_tiles_forced = 0;  // > 0: chunk-first item length in tiles (tuning knob)
   int32_t merge_cap = 0, merge_cap_forced = -1;
   int32_t simt_grid = 0, simt_stages = 3, simt_wpc = 8;
   // sequence-first claims: simt_wpc items each until at most
@@ -484,7 +485,8 @@ pst_status rebuild(pst_pool* p) {
           ? 8
           : std::min<int64_t>(p->tc_max_run,
                               std::max<int64_t>(2, static_cast<int64_t>(std::ceil(p1_iters / std::max(1, p->n_sm)))));
-  const int64_t split1 = std::max<int64_t>(1, static_cast<int64_t>(std::floor(tiles1 / tpc)));
+  const int64_t split1 =
+      std::max<int64_t>(1, static_cast<int64_t>(std::floor((p->tc_tiles_forced > 0 ? p->tc_tiles_forced : tiles1) / tpc)));
   for (const auto& r : runs) {
     const int32_t i = ni[r.front()], j = nj[r.front()];
     const int32_t rows = (j - i) * g;
@@ -894,6 +896,7 @@ pst_status pst_pool_create(const pst_config* cfg, int device, pst_pool** out) {
   if (const char* e = std::getenv("PST_TC_CTAS")) p->tc_ctas_forced = std::max(0, std::atoi(e));
   if (const char* e = std::getenv("PST_SIMT_UNIT_DIV")) p->simt_unit_div = std::max(0.25, std::atof(e));
   if (const char* e = std::getenv("PST_TC_MAX_RUN")) p->tc_max_run = std::max(2, std::atoi(e));
+  if (const char* e = std::getenv("PST_TC_TILES")) p->tc_tiles_forced = std::max(0, std::atoi(e));
   if (const char* e = std::getenv("PST_MERGE_CAP")) p->merge_cap_forced = std::max(0, std::atoi(e));
   if (const char* e = std::getenv("PST_SIMT_TAIL")) p->simt_tail = std::max(0.0, std::atof(e));
   if (const char* e = std::getenv("PST_SPLIT_PREFILL")) p->split_prefill = std::atoi(e) != 0;
