@@ -165,6 +165,9 @@ struct pst_pool {
   double simt_unit_div = 8.0, simt_tail = 2.0;
   int32_t tc_max_run = 32;  // chunk-first items: at most this many 64-key tiles
   int32_t tc_tiles_forced = 0;  // > 0: chunk-first item length in tiles (tuning knob)
+  // chunk-first kernel first: the sequence-first CTAs that start at once take
+  // their first items statically (measured 1.5 to 3.4 us per step faster)
+  bool tcf_static = true;
   int32_t merge_cap = 0, merge_cap_forced = -1;
   int32_t simt_grid = 0, simt_stages = 3, simt_wpc = 8;
   // sequence-first claims: simt_wpc items each until at most
@@ -897,6 +900,7 @@ pst_status pst_pool_create(const pst_config* cfg, int device, pst_pool** out) {
   if (const char* e = std::getenv("PST_SIMT_UNIT_DIV")) p->simt_unit_div = std::max(0.25, std::atof(e));
   if (const char* e = std::getenv("PST_TC_MAX_RUN")) p->tc_max_run = std::max(2, std::atoi(e));
   if (const char* e = std::getenv("PST_TC_TILES")) p->tc_tiles_forced = std::max(0, std::atoi(e));
+  if (const char* e = std::getenv("PST_TCF_STATIC")) p->tcf_static = std::atoi(e) != 0;
   if (const char* e = std::getenv("PST_MERGE_CAP")) p->merge_cap_forced = std::max(0, std::atoi(e));
   if (const char* e = std::getenv("PST_SIMT_TAIL")) p->simt_tail = std::max(0.0, std::atof(e));
   if (const char* e = std::getenv("PST_SPLIT_PREFILL")) p->split_prefill = std::atoi(e) != 0;
@@ -1132,7 +1136,8 @@ pst_status pst_seq_length(const pst_pool* p, int64_t seq_id, int64_t* n_tokens) 
 // not use; the chunk-first kernel (its CTAs take the free SMs at once); the
 // merge.  Otherwise the chunk-first kernel first and the
 // sequence-first kernel behind it on the whole grid (its CTAs start on the
-// free SMs at once, on the others as chunk-first CTAs leave); the merge.
+// free SMs at once, each of their warps on one item of the first wave, and on
+// the others as chunk-first CTAs leave, claiming every item); the merge.
 static pst_status launch_overlapped(pst_pool* p, const AttnParams& a, int32_t B, cudaStream_t s) {
   const bool tc = p->n_tc_items > 0, simt = p->n_simt_items > 0;
   const int32_t grid_a =
@@ -1168,8 +1173,11 @@ static pst_status launch_overlapped(pst_pool* p, const AttnParams& a, int32_t B,
   }
   if (grid_b > 0) {
     a2.pdl = before ? 1 : 0;
-    a2.first_items = 0;  // its CTAs start at different times: every item is claimed
-    a2.claim_base = 0;
+    // CTAs that find a free SM at once (those the chunk-first kernel leaves)
+    // start on one item each of the first wave; the others, which start as
+    // chunk-first CTAs leave, claim every item
+    a2.first_items = p->tcf_static ? std::min(grid_b, std::max(0, p->n_sm - (tc ? p->n_tc_ctas : 0))) * p->simt_wpc : 0;
+    a2.claim_base = a2.first_items;
     cudaError_t e = launch_attn_simt(p->cfg.dtype, p->D, p->C, p->g, a2, grid_b, s);
     if (e != cudaSuccess) return fail(PST_ERR_CUDA, "sequence-first launch: %s", cudaGetErrorString(e));
     p->last_launches++;

@@ -222,6 +222,33 @@ def test_dynamic_tree_appends_and_removes(pst, dtype, hq, hkv, c):
             PU.check(n, w, ref, dtype, f"dynamic {dtype} c{c} step {step}")
 
 
+# Both launch orders of a decode step with both phases (the cost model picks
+# one; the environment forces either, read when a pool is created): the
+# sequence-first kernel first beside the chunk-first kernel, or the chunk-first
+# kernel first with the sequence-first kernel behind it on the whole grid, its
+# first wave on static items or every item claimed.
+ORDERS = {"seq_first": {"PST_SIMT_FIRST": "1"},
+          "chunk_first": {"PST_TC_FIRST": "1"},
+          "chunk_first_claimed": {"PST_TC_FIRST": "1", "PST_TCF_STATIC": "0"}}
+
+
+@pytest.mark.parametrize("order", sorted(ORDERS))
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_launch_orders_all_rows(pst, monkeypatch, order, dtype):
+    for k, v in ORDERS[order].items():
+        monkeypatch.setenv(k, v)
+    spec = W.WorkloadSpec("orders", 8, 2, 128, 64, dtype, ((640, 1), (200, 3), (150, 8)), 81)
+    wl = W.generate(spec)
+    tw = _twin(pst, spec)
+    _insert_all(tw, wl)
+    n, w = tw.decode(wl.q.cuda())
+    st = tw.native.stats()  # the tables the decode just built
+    assert st["phase1_items"] > 0 and st["phase2_items"] > 0
+    assert st["simt_first"] == (1 if order == "seq_first" else 0)
+    ref = A.decode_attention([(_f64(wl.seq_k(s)), _f64(wl.seq_v(s))) for s in range(wl.n_sequences)], _f64(wl.q))
+    PU.check(n, w, ref, dtype, f"launch order {order} {dtype}")
+
+
 def test_nan_in_matched_rows_is_ignored(pst):
     spec = W.WorkloadSpec("nan", 4, 2, 128, 64, "f16", ((256, 1), (128, 3)), 77)
     wl = W.generate(spec)
