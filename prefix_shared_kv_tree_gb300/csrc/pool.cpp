@@ -159,10 +159,12 @@ struct pst_pool {
   bool tc_first_forced = false;
   bool simt_first_forced = false;
   int32_t tc_ctas_forced = 0;  // > 0: chunk-first CTAs when both phases run (tuning knob)
-  // sequence-first items: about sqrt(g) * T / (simt_unit_div * W) chunks each
-  // (at most kSimtInline; an item's set-up and partial rows grow with g), the
-  // last simt_tail * W chunks as single-chunk items
-  double simt_unit_div = 8.0, simt_tail = 2.0;
+  // sequence-first items: about g * T / (simt_unit_div * W) chunks each (at
+  // most kSimtInline; an item's set-up and partial rows grow with g), the last
+  // simt_tail * W chunks as single-chunk items.  Measured, us per step, this
+  // rule against sqrt(g) * T / (8 W): share4k 96.0 / 98.4, noshare 303.2 /
+  // 306.8, the others equal (the same items at g = 4 and for share1k)
+  double simt_unit_div = 16.0, simt_tail = 2.0;
   int32_t tc_max_run = 32;  // chunk-first items: at most this many 64-key tiles
   int32_t tc_tiles_forced = 0;  // > 0: chunk-first item length in tiles (tuning knob)
   // chunk-first kernel first: the sequence-first CTAs that start at once take
@@ -631,9 +633,9 @@ pst_status rebuild(pst_pool* p) {
   }
 
   // ---- cut the CUDA-core tile streams into work items that warps claim at
-  // run time: items of about T / (8 W) chunks (W = warps in the grid), the
-  // largest claimed first, and the last ~2W chunks as single-chunk items so the
-  // kernel ends evenly.
+  // run time: items of about g T / (16 W) chunks (W = warps in the grid) and
+  // at least 16 KiB, the largest claimed first, and the last ~2W chunks as
+  // single-chunk items so the kernel ends evenly.
   const int32_t simt_sms = (p->n_tc_ctas > 0 && (p->cfg.flags & PST_FLAG_CONCURRENT_PHASES))
                                ? std::max(1, p->n_sm - p->n_tc_ctas)
                                : p->n_sm;
@@ -646,12 +648,16 @@ pst_status rebuild(pst_pool* p) {
     const bool beside_tc = p->n_tc_ctas > 0 && p->n_tc_ctas < p->n_sm;
     const int64_t W =
         static_cast<int64_t>(beside_tc ? std::min(p->simt_grid, p->n_sm - p->n_tc_ctas) : p->simt_grid) * p->simt_wpc;
+    // items of at least 16 KiB of K/V, for small chunks (an item's fixed cost
+    // against its bytes; measured at d = 64, c = 16: 54 us per step with 16 KiB
+    // items, 60 with 8 KiB)
+    const int64_t min_unit = ceil_div(int64_t{16384}, static_cast<int64_t>(2) * p->C * p->D * p->es);
     const int32_t unit = std::min<int32_t>(
         kSimtInline,
         p->simt_unit > 0 ? p->simt_unit
                          : static_cast<int32_t>(std::max<int64_t>(
-                               1, static_cast<int64_t>(static_cast<double>(T) * std::sqrt(static_cast<double>(g)) /
-                                                       (p->simt_unit_div * W)))));
+                               min_unit, static_cast<int64_t>(static_cast<double>(T) * static_cast<double>(g) /
+                                                              (p->simt_unit_div * W)))));
     // the units, largest first and in stream order among equals: a stable
     // bucket pass (a unit has 1 .. unit <= kSimtInline chunks)
     std::vector<int32_t> of_len(kSimtInline + 2, 0);
