@@ -159,11 +159,12 @@ struct pst_pool {
   bool tc_first_forced = false;
   bool simt_first_forced = false;
   int32_t tc_ctas_forced = 0;  // > 0: chunk-first CTAs when both phases run (tuning knob)
-  // sequence-first items: about g * T / (simt_unit_div * W) chunks each (at
-  // most kSimtInline; an item's set-up and partial rows grow with g), the last
-  // simt_tail * W chunks as single-chunk items.  Measured, us per step, this
-  // rule against sqrt(g) * T / (8 W): share4k 96.0 / 98.4, noshare 303.2 /
-  // 306.8, the others equal (the same items at g = 4 and for share1k)
+  // sequence-first items: about g * T / (simt_unit_div * W) chunks each when
+  // every tile they stage is read once (at most kSimtInline; an item's set-up
+  // and partial rows grow with g), the last simt_tail * W chunks as
+  // single-chunk items.  Measured, us per step, this rule against
+  // sqrt(g) * T / (8 W): share4k 96.0 / 98.4, noshare 303.2 / 306.8, the
+  // others equal (the same items at g = 4 and for share1k)
   double simt_unit_div = 16.0, simt_tail = 2.0;
   int32_t tc_max_run = 32;  // chunk-first items: at most this many 64-key tiles
   int32_t tc_tiles_forced = 0;  // > 0: chunk-first item length in tiles (tuning knob)
@@ -633,9 +634,9 @@ pst_status rebuild(pst_pool* p) {
   }
 
   // ---- cut the CUDA-core tile streams into work items that warps claim at
-  // run time: items of about g T / (16 W) chunks (W = warps in the grid) and
-  // at least 16 KiB, the largest claimed first, and the last ~2W chunks as
-  // single-chunk items so the kernel ends evenly.
+  // run time: items of about g T / (16 W) chunks (W = warps in the grid; see
+  // below) and at least 16 KiB, the largest claimed first, and the last ~2W
+  // chunks as single-chunk items so the kernel ends evenly.
   const int32_t simt_sms = (p->n_tc_ctas > 0 && (p->cfg.flags & PST_FLAG_CONCURRENT_PHASES))
                                ? std::max(1, p->n_sm - p->n_tc_ctas)
                                : p->n_sm;
@@ -652,12 +653,19 @@ pst_status rebuild(pst_pool* p) {
     // against its bytes; measured at d = 64, c = 16: 54 us per step with 16 KiB
     // items, 60 with 8 KiB)
     const int64_t min_unit = ceil_div(int64_t{16384}, static_cast<int64_t>(2) * p->C * p->D * p->es);
+    // g T / (16 W) chunks when every tile staged here is read by one item
+    // only (the shared chunks on the tensor cores); when shared chunks are
+    // streamed here by every sequence that holds them (read again from L2),
+    // larger items pay: sqrt(g) T / (8 W) (measured, share1k with no sharing:
+    // 67.7 us per step against 76.5 with the first rule)
+    const bool read_once = p->use_tc && p->cfg.min_share <= 2;
+    const double per_warp = read_once ? static_cast<double>(g) / p->simt_unit_div
+                                      : std::sqrt(static_cast<double>(g)) / 8.0;
     const int32_t unit = std::min<int32_t>(
         kSimtInline,
         p->simt_unit > 0 ? p->simt_unit
                          : static_cast<int32_t>(std::max<int64_t>(
-                               min_unit, static_cast<int64_t>(static_cast<double>(T) * static_cast<double>(g) /
-                                                              (p->simt_unit_div * W)))));
+                               min_unit, static_cast<int64_t>(static_cast<double>(T) * per_warp / W))));
     // the units, largest first and in stream order among equals: a stable
     // bucket pass (a unit has 1 .. unit <= kSimtInline chunks)
     std::vector<int32_t> of_len(kSimtInline + 2, 0);
