@@ -287,7 +287,7 @@ __global__ void __launch_bounds__(32 * (simt_max_warps(G, sizeof(T)) + 1), 1) at
       // ---- next item into the consumer's next slot, once it has released it
       bool want = !finished && (written < 2 || ptx::mbar_test_wait(&sempty[qs], ((written >> 1) - 1) & 1));
       unsigned wm = __ballot_sync(0xffffffffu, want);
-      // at most the rest of the two batches in hand this round
+      // at most the rest of the two batches in hand on this pass
       const int szc = bcur ? sz1 : sz0;
       const int room = szc + (bcur ? sz0 : sz1) - bpos;
       if (__popc(wm) > room) {
