@@ -275,9 +275,16 @@ def test_empty_batch_and_host_api(pst):
     n, w = tw.decode(q)
     q_host = wl.q.clone().pin_memory()
     for pool, dev_out, dt in ((tw.native, n, torch.bfloat16), (tw.wide, w, torch.float32)):
-        out_host = torch.empty(q_host.shape, dtype=dt).pin_memory()
-        pool.decode_attention_host(q_host, out_host)
-        assert torch.equal(out_host, dev_out.cpu())
+        # pinned buffers (copies inside the step's graph): captured, replayed,
+        # captured again for other buffers; pageable buffers (separate copies)
+        out_pinned = torch.empty(q_host.shape, dtype=dt).pin_memory()
+        cases = ((q_host, out_pinned), (q_host, out_pinned),
+                 (wl.q.clone().pin_memory(), torch.empty(q_host.shape, dtype=dt).pin_memory()),
+                 (wl.q.clone(), torch.empty(q_host.shape, dtype=dt)))
+        for qh, out_host in cases:
+            out_host.fill_(float("nan"))
+            pool.decode_attention_host(qh, out_host)
+            assert torch.equal(out_host, dev_out.cpu())
     ref = A.decode_attention([(_f64(wl.seq_k(s)), _f64(wl.seq_v(s))) for s in range(wl.n_sequences)], _f64(wl.q))
     PU.check(n, w, ref, "bf16", "host api")
 
